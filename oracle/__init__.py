@@ -1,0 +1,158 @@
+"""CPU oracle for the sparse latent attention hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import
+this package.  The CUDA library never imports, links or calls it, and this package never touches
+the CUDA library: the two share nothing but the seeded input generators.
+
+The arithmetic lives in ``oracle.c`` (plain C11 loops, f32 where the pages fix f32, with a
+float64 variant of ``sparse_attn``); this module only marshals numpy arrays through ctypes.
+bf16 tensors travel as their raw ``uint16`` bit patterns.
+
+Sources, by page title and section:
+  * "DeepSeek V4.1", attention/attend: ``get_window_topk_idxs``, ``sparse_attn_kernel``.
+  * "DeepSeek V4.1", attention/query-latent: ``Attention.__init__`` (ring buffer),
+    ``Attention.forward`` (window and compressed rows concatenated before ``sparse_attn``).
+  * "Module attn" (deepseek_v41_ref API page): Precision paragraph, ring-cache paragraph,
+    ``FP8_BLOCK``, ``act_quant_inplace``, ``pow2_ceil``, ``sparse_attn``, ``window_topk_idxs``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+FP8_BLOCK = 32
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` beside it (plain gcc, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC,
+             "-lm", "-lpthread"],
+            check=True,
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        lib.oracle_window_topk_idxs.argtypes = [P, i32, i64, i32]
+        lib.oracle_window_topk_idxs.restype = i32
+        lib.oracle_pow2_ceil.argtypes = [f32]
+        lib.oracle_pow2_ceil.restype = f32
+        lib.oracle_e4m3_round.argtypes = [f32]
+        lib.oracle_e4m3_round.restype = f32
+        lib.oracle_act_quant_inplace.argtypes = [P, i64]
+        lib.oracle_act_quant_inplace.restype = i32
+        lib.oracle_kv_quant_ring_write.argtypes = [P, i64, P, i64, i32, i32, i32, i64, i32]
+        lib.oracle_kv_quant_ring_write.restype = i32
+        attn_args = [P, P, i64, P, P, i32, f32, P, i32, i32, i32, i32, P, i64, i32]
+        lib.oracle_sparse_attn.argtypes = attn_args
+        lib.oracle_sparse_attn.restype = i32
+        lib.oracle_sparse_attn_f64.argtypes = attn_args
+        lib.oracle_sparse_attn_f64.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def window_topk_idxs(s: int, start_pos: int, window: int) -> np.ndarray:
+    """Index rows ``[queries][cols]`` int32 for one sequence (replicate over the batch yourself)."""
+    lib = _load()
+    rows = s if start_pos == 0 else 1
+    out = np.empty((rows, max(min(s, window) if start_pos == 0 else window, 0)), dtype=np.int32)
+    cols = lib.oracle_window_topk_idxs(_ptr(out), s, start_pos, window)
+    if cols < 0:
+        raise ValueError(f"window_topk_idxs undefined for s={s}, start_pos={start_pos}, window={window}")
+    return out
+
+
+def pow2_ceil(v: float) -> float:
+    return float(_load().oracle_pow2_ceil(v))
+
+
+def e4m3_round(y: float) -> float:
+    return float(_load().oracle_e4m3_round(y))
+
+
+def act_quant_inplace(x_bits: np.ndarray) -> np.ndarray:
+    """fp8 round trip of bf16 bit patterns (uint16, size a multiple of 32), in place."""
+    assert x_bits.dtype == np.uint16
+    if _load().oracle_act_quant_inplace(_ptr(x_bits), x_bits.size) != 0:
+        raise ValueError("act_quant_inplace needs a multiple of 32 values")
+    return x_bits
+
+
+def kv_quant_ring_write(kv_bits: np.ndarray, ring_bits: np.ndarray, start_pos: int, window: int) -> None:
+    """kv_bits ``[b][s][d]`` (rounded in place) and ring_bits ``[b][window][d]`` (updated)."""
+    assert kv_bits.dtype == np.uint16 and ring_bits.dtype == np.uint16
+    b, s, d = kv_bits.shape
+    assert ring_bits.shape == (b, window, d)
+    rc = _load().oracle_kv_quant_ring_write(_ptr(kv_bits), s * d, _ptr(ring_bits), window * d, b, s, d,
+                                            start_pos, window)
+    if rc != 0:
+        raise ValueError("kv_quant_ring_write: bad arguments")
+
+
+def sparse_attn(q_bits: np.ndarray, kv_bits: np.ndarray, sink: np.ndarray, idx: np.ndarray, scale: float,
+                tokens: np.ndarray | None = None, nthreads: int | None = None, f64: bool = False) -> np.ndarray:
+    """Oracle sparse_attn.
+
+    q_bits ``[b][m][h][d]`` uint16 (bf16 bits); kv_bits ``[b][n][d]`` uint16; sink ``[h]`` f32;
+    idx ``[b][m][topk]`` int32.  ``tokens``: optional flattened token numbers ``bi*m + t`` to
+    compute.  Returns bf16 bits ``[ntok][h][d]`` (uint16) from the f32 oracle, or float64 values
+    from the f64 variant.  Without ``tokens`` the result is shaped ``[b][m][h][d]``.
+    """
+    lib = _load()
+    b, m, h, d = q_bits.shape
+    n = kv_bits.shape[1]
+    topk = idx.shape[2]
+    assert kv_bits.shape == (b, n, d) and idx.shape[:2] == (b, m)
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    kv_bits = np.ascontiguousarray(kv_bits, dtype=np.uint16)
+    sink = np.ascontiguousarray(sink, dtype=np.float32)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    if tokens is not None:
+        tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+        ntok = tokens.size
+    else:
+        ntok = b * m
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    if f64:
+        out = np.zeros((ntok, h, d), dtype=np.float64)
+        fn = lib.oracle_sparse_attn_f64
+    else:
+        out = np.zeros((ntok, h, d), dtype=np.uint16)
+        fn = lib.oracle_sparse_attn
+    rc = fn(_ptr(q_bits), _ptr(kv_bits), n, _ptr(sink), _ptr(idx), topk, float(scale), _ptr(out), b, m, h, d,
+            _ptr(tokens) if tokens is not None else None, ntok, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle sparse_attn: bad arguments or index out of range")
+    if tokens is None:
+        out = out.reshape(b, m, h, d)
+    return out
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float32 values (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)

@@ -1,0 +1,370 @@
+/*
+ * oracle.c -- plain, slow CPU oracle for the DeepSeek-V4.1 sparse latent attention hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file exists to check the CUDA library against the pages that
+ * define the method.  Only the tests, the smoke check and the CPU-baseline leg of the benchmark
+ * may load it.  It shares no code, header, table or constant with the CUDA path, and the CUDA
+ * path never calls it.
+ *
+ * Sources (page title, section):
+ *   [attend]   "DeepSeek V4.1", blocks/.../attention/attend: get_window_topk_idxs,
+ *              sparse_attn_kernel, sparse_attn wrapper.
+ *   [latent]   "DeepSeek V4.1", blocks/.../attention/query-latent: Attention.__init__
+ *              (window_kv_cache ring buffer), Attention.forward (window + compressed concat).
+ *   [attn]     "Module attn" (deepseek_v41_ref API page): the Precision paragraph, the ring-cache
+ *              paragraph, FP8_BLOCK, act_quant_inplace, pow2_ceil, sparse_attn, window_topk_idxs.
+ *
+ * Everything here is written as plain loops in the order the pages state the steps.  The
+ * precision is the pages' own: the fp8 round trip decides its scale in f32 ([attn] pow2_ceil
+ * works on the IEEE fields of an f32), and sparse_attn runs in f32 with a bf16 result ([attn]
+ * Precision).  A float64 variant of sparse_attn is kept for the pinning tests.
+ *
+ * Every function is pinned by tests that do not re-type it: the ring-cache worked example of
+ * [attn], brute-force dense masked softmax, closed forms, invariances, and PyTorch's own
+ * float8_e4m3fn conversion (see tests/test_oracle_pins.py).
+ *
+ * Build (plain C11, no intrinsics, no fast-math, no contraction so x86 and Arm agree):
+ *   gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared -o liboracle.so oracle.c -lm -lpthread
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------------------------ */
+/* bf16 <-> f32, written from the format: bf16 is the top 16 bits of an IEEE binary32.         */
+/* ------------------------------------------------------------------------------------------ */
+
+static float bf16_bits_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round an f32 to the nearest bf16, ties to even.  NaN stays NaN (quiet). */
+static uint16_t f32_to_bf16_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t kept = u >> 16;          /* truncated result                     */
+    uint32_t dropped = u & 0xffffu;   /* the 16 bits that do not fit          */
+    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))
+        kept += 1u;                   /* carries into the exponent if needed  */
+    return (uint16_t)kept;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* window_topk_idxs  ([attend] get_window_topk_idxs; [attn] window_topk_idxs)                  */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * Ring-slot index rows for the sliding window.
+ * start_pos == 0 (prefill, s queries): cols = min(s, window); row q lists the causal window of
+ *   query q starting at max(0, q - window + 1); an entry past q holds nothing and is -1.
+ * start_pos > 0 (decode, one query): cols = window; the whole ring oldest first, i.e. slots
+ *   oldest..window-1 then 0..oldest-1 with oldest = start_pos % window + 1; a slot whose value
+ *   exceeds start_pos is still empty and is -1.
+ * Writes out[q * cols + j].  Returns cols, or -1 for a chunked prefill (start_pos > 0, s > 1),
+ * which the pages do not define.
+ */
+int oracle_window_topk_idxs(int32_t *out, int s, int64_t start_pos, int window) {
+    if (s <= 0 || window <= 0 || start_pos < 0) return -1;
+    if (start_pos == 0) {
+        int cols = s < window ? s : window;
+        for (int q = 0; q < s; ++q) {
+            int first = q - window + 1;
+            if (first < 0) first = 0;
+            for (int j = 0; j < cols; ++j) {
+                int v = first + j;
+                out[(int64_t)q * cols + j] = v > q ? -1 : v;
+            }
+        }
+        return cols;
+    }
+    if (s != 1) return -1;
+    int oldest = (int)(start_pos % window) + 1;
+    int k = 0;
+    for (int v = oldest; v < window; ++v) out[k++] = (int64_t)v > start_pos ? -1 : v;
+    for (int v = 0; v < oldest; ++v) out[k++] = (int64_t)v > start_pos ? -1 : v;
+    return window;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* fp8 round trip  ([attn] FP8_BLOCK, pow2_ceil, act_quant_inplace, Precision)                 */
+/* ------------------------------------------------------------------------------------------ */
+
+#define ORACLE_FP8_BLOCK 32
+#define ORACLE_E4M3_MAX 448.0f
+
+/* 2 ** ceil(log2(v)) for a positive normal f32, read off the IEEE fields: a value whose
+ * mantissa field is zero is already a power of two; otherwise the next power up is the one
+ * with the exponent field plus one and a zero mantissa. */
+float oracle_pow2_ceil(float v) {
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    uint32_t exponent = (u >> 23) & 0xffu;
+    uint32_t mantissa = u & 0x7fffffu;
+    if (mantissa == 0u) return v;
+    uint32_t r = (exponent + 1u) << 23;
+    float out;
+    memcpy(&out, &r, sizeof out);
+    return out;
+}
+
+/* The 127 non-negative finite values of e4m3fn (1 sign, 4 exponent, 3 mantissa bits, bias 7;
+ * exponent field 0 is subnormal with step 2^-9; code 0x7f is NaN and is not a value).  The codes
+ * are in ascending order of value. */
+static double e4m3_table[127];
+static pthread_once_t e4m3_once = PTHREAD_ONCE_INIT;
+
+static void e4m3_build_table(void) {
+    for (int code = 0; code < 127; ++code) {
+        int e = code >> 3, m = code & 7;
+        e4m3_table[code] = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    }
+}
+
+/* Nearest e4m3fn value to y, ties to the even code (even mantissa).  y must lie in [-448, 448]. */
+float oracle_e4m3_round(float y) {
+    pthread_once(&e4m3_once, e4m3_build_table);
+    double a = fabs((double)y);
+    int k = 0;                               /* largest code with value <= a */
+    while (k + 1 < 127 && e4m3_table[k + 1] <= a) ++k;
+    int pick = k;
+    if (k + 1 < 127 && a > e4m3_table[k]) {
+        double below = a - e4m3_table[k], above = e4m3_table[k + 1] - a;
+        if (above < below) pick = k + 1;
+        else if (above == below) pick = (k % 2 == 0) ? k : k + 1;
+    }
+    double r = e4m3_table[pick];
+    return (float)(signbit(y) ? -r : r);     /* sign-magnitude: -0 stays -0 */
+}
+
+/* One block of FP8_BLOCK bf16 values, in place: amax floored at 1e-4, scale = pow2_ceil of
+ * amax / 448 (f32 division), each value divided by the scale, clamped to +-448, rounded to
+ * e4m3 (RNE), multiplied back and rounded to bf16 (exact: e4m3 times a power of two). */
+static void quant_block(uint16_t *x) {
+    float amax = 0.0f;
+    for (int i = 0; i < ORACLE_FP8_BLOCK; ++i) {
+        float a = fabsf(bf16_bits_to_f32(x[i]));
+        if (a > amax) amax = a;
+    }
+    if (amax < 1e-4f) amax = 1e-4f;
+    float scale = oracle_pow2_ceil(amax / ORACLE_E4M3_MAX);
+    for (int i = 0; i < ORACLE_FP8_BLOCK; ++i) {
+        float y = bf16_bits_to_f32(x[i]) / scale;
+        if (y > ORACLE_E4M3_MAX) y = ORACLE_E4M3_MAX;
+        if (y < -ORACLE_E4M3_MAX) y = -ORACLE_E4M3_MAX;
+        float qv = oracle_e4m3_round(y);
+        x[i] = f32_to_bf16_bits(qv * scale);
+    }
+}
+
+/* act_quant_inplace over n bf16 values (n a multiple of FP8_BLOCK).  Returns 0, or -1. */
+int oracle_act_quant_inplace(uint16_t *x, int64_t n) {
+    if (n < 0 || n % ORACLE_FP8_BLOCK != 0) return -1;
+    for (int64_t i = 0; i < n; i += ORACLE_FP8_BLOCK) quant_block(x + i);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Ring write  ([latent] window_kv_cache; [attn] ring-cache paragraph, WindowCache, attention) */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * New KV rows kv[bi][t][0:d] (row stride d, batch stride kv_bstride) are rounded through fp8 in
+ * place; the token at absolute position start_pos + t is then stored in ring slot
+ * (start_pos + t) % window when it is among the last `window` rows of the chunk
+ * (t >= s - window).  ring[bi][slot][0:d] has batch stride ring_bstride.
+ */
+int oracle_kv_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride,
+                               int b, int s, int d, int64_t start_pos, int window) {
+    if (b < 0 || s < 0 || d <= 0 || d % ORACLE_FP8_BLOCK != 0 || window <= 0 || start_pos < 0) return -1;
+    for (int bi = 0; bi < b; ++bi) {
+        for (int t = 0; t < s; ++t) {
+            uint16_t *row = kv + (int64_t)bi * kv_bstride + (int64_t)t * d;
+            oracle_act_quant_inplace(row, d);
+            if (t >= s - window) {
+                int64_t slot = (start_pos + t) % window;
+                memcpy(ring + (int64_t)bi * ring_bstride + slot * d, row, (size_t)d * sizeof(uint16_t));
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* sparse_attn  ([attn] sparse_attn and Precision; [attend] sparse_attn_kernel, wrapper)       */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * For query token (bi, t) and head hh:
+ *   s_j = scale * sum_c q[bi][t][hh][c] * kv[bi][idx_j][c]     for every entry idx_j >= 0
+ *   M   = max(sink[hh], max_j s_j)                              (subtracted for range only)
+ *   den = exp(sink[hh] - M) + sum_j exp(s_j - M)                the sink is in the denominator only
+ *   o   = sum_j exp(s_j - M) / den * kv[bi][idx_j][:]           V is the same gathered row
+ * Entries < 0 are skipped; a row with no entry >= 0 gives o = 0.  All arithmetic in f32 in the
+ * order written, result rounded to bf16 (f32 variant) or kept as double (f64 variant).
+ *
+ * Layouts: q, o [b][m][h][d]; kv [b][n][d]; sink [h]; idx [b][m][topk]; all contiguous.
+ * tokens: optional list of flattened token numbers bi*m + t to compute (NULL = all b*m); the
+ * output then holds one [h][d] block per listed token, in list order.
+ */
+typedef struct {
+    const uint16_t *q, *kv;
+    int64_t n;
+    const float *sink;
+    const int32_t *idx;
+    int topk;
+    float scale;
+    int b, m, h, d;
+    const int64_t *tokens;
+    int64_t ntok;
+    uint16_t *o_bf16;     /* f32 variant */
+    double *o_f64;        /* f64 variant */
+    int thread_id, nthreads;
+    int status;
+} attn_job;
+
+static void attn_token_f32(const attn_job *J, int64_t tok, int64_t out_slot, float *qf, float *sc, float *acc) {
+    const int d = J->d, topk = J->topk;
+    const int64_t bi = tok / J->m;
+    const int32_t *irow = J->idx + tok * topk;
+    const uint16_t *kvb = J->kv + bi * J->n * d;
+    for (int hh = 0; hh < J->h; ++hh) {
+        const uint16_t *qrow = J->q + (tok * J->h + hh) * (int64_t)d;
+        for (int c = 0; c < d; ++c) qf[c] = bf16_bits_to_f32(qrow[c]);
+        /* scores, and their maximum together with the sink */
+        float M = J->sink[hh];
+        for (int j = 0; j < topk; ++j) {
+            if (irow[j] < 0) continue;
+            const uint16_t *r = kvb + (int64_t)irow[j] * d;
+            float dot = 0.0f;
+            for (int c = 0; c < d; ++c) dot += qf[c] * bf16_bits_to_f32(r[c]);
+            sc[j] = J->scale * dot;
+            if (sc[j] > M) M = sc[j];
+        }
+        /* denominator: every gathered row plus the sink */
+        float den = expf(J->sink[hh] - M);
+        for (int j = 0; j < topk; ++j)
+            if (irow[j] >= 0) den += expf(sc[j] - M);
+        /* probabilities, then the weighted sum of the same gathered rows */
+        for (int c = 0; c < d; ++c) acc[c] = 0.0f;
+        for (int j = 0; j < topk; ++j) {
+            if (irow[j] < 0) continue;
+            float p = expf(sc[j] - M) / den;
+            const uint16_t *r = kvb + (int64_t)irow[j] * d;
+            for (int c = 0; c < d; ++c) acc[c] += p * bf16_bits_to_f32(r[c]);
+        }
+        uint16_t *orow = J->o_bf16 + (out_slot * J->h + hh) * (int64_t)d;
+        for (int c = 0; c < d; ++c) orow[c] = f32_to_bf16_bits(acc[c]);
+    }
+}
+
+static void attn_token_f64(const attn_job *J, int64_t tok, int64_t out_slot, double *qf, double *sc, double *acc) {
+    const int d = J->d, topk = J->topk;
+    const int64_t bi = tok / J->m;
+    const int32_t *irow = J->idx + tok * topk;
+    const uint16_t *kvb = J->kv + bi * J->n * d;
+    for (int hh = 0; hh < J->h; ++hh) {
+        const uint16_t *qrow = J->q + (tok * J->h + hh) * (int64_t)d;
+        for (int c = 0; c < d; ++c) qf[c] = (double)bf16_bits_to_f32(qrow[c]);
+        double M = (double)J->sink[hh];
+        for (int j = 0; j < topk; ++j) {
+            if (irow[j] < 0) continue;
+            const uint16_t *r = kvb + (int64_t)irow[j] * d;
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) dot += qf[c] * (double)bf16_bits_to_f32(r[c]);
+            sc[j] = (double)J->scale * dot;
+            if (sc[j] > M) M = sc[j];
+        }
+        double den = exp((double)J->sink[hh] - M);
+        for (int j = 0; j < topk; ++j)
+            if (irow[j] >= 0) den += exp(sc[j] - M);
+        for (int c = 0; c < d; ++c) acc[c] = 0.0;
+        for (int j = 0; j < topk; ++j) {
+            if (irow[j] < 0) continue;
+            double p = exp(sc[j] - M) / den;
+            const uint16_t *r = kvb + (int64_t)irow[j] * d;
+            for (int c = 0; c < d; ++c) acc[c] += p * (double)bf16_bits_to_f32(r[c]);
+        }
+        double *orow = J->o_f64 + (out_slot * J->h + hh) * (int64_t)d;
+        for (int c = 0; c < d; ++c) orow[c] = acc[c];
+    }
+}
+
+static void *attn_worker(void *arg) {
+    attn_job *J = (attn_job *)arg;
+    int use64 = J->o_f64 != NULL;
+    size_t es = use64 ? sizeof(double) : sizeof(float);
+    void *qf = malloc((size_t)J->d * es);
+    void *acc = malloc((size_t)J->d * es);
+    void *sc = malloc((size_t)(J->topk > 0 ? J->topk : 1) * es);
+    if (!qf || !sc || !acc) {
+        J->status = -1;
+    } else {
+        for (int64_t k = J->thread_id; k < J->ntok; k += J->nthreads) {
+            int64_t tok = J->tokens ? J->tokens[k] : k;
+            if (use64) attn_token_f64(J, tok, k, (double *)qf, (double *)sc, (double *)acc);
+            else attn_token_f32(J, tok, k, (float *)qf, (float *)sc, (float *)acc);
+        }
+    }
+    free(qf);
+    free(sc);
+    free(acc);
+    return NULL;
+}
+
+static int attn_run(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink, const int32_t *idx,
+                    int topk, float scale, int b, int m, int h, int d, const int64_t *tokens, int64_t ntok,
+                    uint16_t *o_bf16, double *o_f64, int nthreads) {
+    if (b < 0 || m < 0 || h <= 0 || d <= 0 || topk < 0 || n < 0) return -1;
+    if (!tokens) ntok = (int64_t)b * m;
+    for (int64_t k = 0; k < ntok; ++k) {       /* caller contract: every index < n */
+        int64_t tok = tokens ? tokens[k] : k;
+        if (tok < 0 || tok >= (int64_t)b * m) return -1;
+        for (int j = 0; j < topk; ++j)
+            if (idx[tok * topk + j] >= n) return -1;
+    }
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    attn_job jobs[256];
+    pthread_t th[256];
+    for (int i = 0; i < nthreads; ++i) {
+        attn_job J = {q, kv, n, sink, idx, topk, scale, b, m, h, d, tokens, ntok, o_bf16, o_f64, i, nthreads, 0};
+        jobs[i] = J;
+    }
+    int started = 0;
+    for (int i = 1; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, attn_worker, &jobs[i]) != 0) break;
+        started = i;
+    }
+    if (started < nthreads - 1) {              /* could not start every thread: run serially */
+        for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
+        attn_job J = {q, kv, n, sink, idx, topk, scale, b, m, h, d, tokens, ntok, o_bf16, o_f64, 0, 1, 0};
+        attn_worker(&J);
+        return J.status;
+    }
+    attn_worker(&jobs[0]);
+    int status = jobs[0].status;
+    for (int i = 1; i < nthreads; ++i) {
+        pthread_join(th[i], NULL);
+        if (jobs[i].status) status = jobs[i].status;
+    }
+    return status;
+}
+
+int oracle_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink, const int32_t *idx,
+                       int topk, float scale, uint16_t *o, int b, int m, int h, int d,
+                       const int64_t *tokens, int64_t ntok, int nthreads) {
+    return attn_run(q, kv, n, sink, idx, topk, scale, b, m, h, d, tokens, ntok, o, NULL, nthreads);
+}
+
+int oracle_sparse_attn_f64(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink, const int32_t *idx,
+                           int topk, float scale, double *o, int b, int m, int h, int d,
+                           const int64_t *tokens, int64_t ntok, int nthreads) {
+    return attn_run(q, kv, n, sink, idx, topk, scale, b, m, h, d, tokens, ntok, NULL, o, nthreads);
+}

@@ -1,0 +1,452 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test checks the oracle against something the pages or the mathematics fix: the ring-cache
+worked example printed in "Module attn" (golden files), an independent enumeration of the window
+(brute force), PyTorch's own float8_e4m3fn conversion and softmax / scaled_dot_product_attention
+(library routines), closed forms, and invariances stated in "DeepSeek V4.1", attention/attend.
+A plausible slip in the oracle (a dropped sink, a wrong scale, a transposed operand, an off-by-one
+in the ring, a wrong rounding tie) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------------------------
+# helpers (bf16 <-> numbers through torch, independent of the oracle's C conversions)
+# ----------------------------------------------------------------------------------------------
+
+def to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def from_bits(b: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+
+
+def bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return from_bits(b).to(torch.float64).numpy()
+
+
+def read_golden_ring():
+    rows = {}
+    with open(os.path.join(GOLDEN, "ring_cache_example.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].split()
+            if not line:
+                continue
+            if line[0] == "decode":
+                step = int(line[1])
+                slot = int(line[3])
+                ring = [int(x) for x in line[5:13]]
+                row = [int(x) for x in line[14:22]]
+                rows.setdefault("decode", []).append((step, slot, ring, row))
+            else:
+                rows[line[0]] = [int(x) for x in line[1:]]
+    return rows
+
+
+# ----------------------------------------------------------------------------------------------
+# window_topk_idxs
+# ----------------------------------------------------------------------------------------------
+
+def test_window_rows_prefill_golden(oracle_mod):
+    rows = oracle_mod.window_topk_idxs(12, 0, 8)
+    assert rows.shape == (12, 8)
+    with open(os.path.join(GOLDEN, "window_rows_prefill.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].split()
+            if not line:
+                continue
+            q = int(line[0][1:])
+            assert rows[q].tolist() == [int(x) for x in line[1:]], q
+
+
+def test_window_rows_decode_golden(oracle_mod):
+    g = read_golden_ring()
+    for step, _slot, _ring, row in g["decode"]:
+        got = oracle_mod.window_topk_idxs(1, step, g["window"][0])
+        assert got.shape == (1, 8)
+        assert got[0].tolist() == row
+
+
+def _brute_decode_row(p, W):
+    # the W most recent tokens p-W+1 .. p, oldest first; token t sits in slot t mod W; a token
+    # before the sequence start leaves its slot empty
+    return [(t % W) if t >= 0 else -1 for t in range(p - W + 1, p + 1)]
+
+
+def _brute_prefill_rows(s, W):
+    cols = min(s, W)
+    out = []
+    for q in range(s):
+        seen = list(range(max(0, q - W + 1), q + 1))
+        out.append(seen + [-1] * (cols - len(seen)))
+    return out
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8, 128])
+def test_window_rows_decode_bruteforce(oracle_mod, W):
+    for p in list(range(1, 3 * W + 2)) + [10000, 16384, 131072]:
+        got = oracle_mod.window_topk_idxs(1, p, W)[0].tolist()
+        assert got == _brute_decode_row(p, W), (p, W)
+
+
+@pytest.mark.parametrize("s,W", [(1, 8), (5, 8), (8, 8), (12, 8), (37, 16), (300, 128)])
+def test_window_rows_prefill_bruteforce(oracle_mod, s, W):
+    got = oracle_mod.window_topk_idxs(s, 0, W)
+    assert got.tolist() == _brute_prefill_rows(s, W)
+
+
+def test_window_rows_ring_filling_case(oracle_mod):
+    # position 3 in an 8-slot ring: only slots 0..3 hold tokens yet
+    assert oracle_mod.window_topk_idxs(1, 3, 8)[0].tolist() == [-1, -1, -1, -1, 0, 1, 2, 3]
+
+
+def test_window_rows_chunked_prefill_undefined(oracle_mod):
+    with pytest.raises(ValueError):
+        oracle_mod.window_topk_idxs(4, 5, 8)
+
+
+# ----------------------------------------------------------------------------------------------
+# fp8 round trip
+# ----------------------------------------------------------------------------------------------
+
+def _pow2_ceil_math(v: float) -> float:
+    m, e = math.frexp(v)       # v = m * 2**e, 0.5 <= m < 1
+    return v if m == 0.5 else math.ldexp(1.0, e)
+
+
+def test_pow2_ceil_matches_math(oracle_mod):
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        (2.0 ** rng.integers(-120, 120, 500)).astype(np.float32),
+        rng.uniform(1e-30, 1e30, 2000).astype(np.float32),
+        (rng.standard_normal(2000).astype(np.float32) ** 2 + np.float32(1e-20)),
+        np.array([1.0, 0.75, 1.5, 2.0 ** -126, 3.0e38], dtype=np.float32),
+    ])
+    for v in vals:
+        v = float(v)
+        # 2**128 is not an f32: the power above the largest binade overflows to inf
+        with np.errstate(over="ignore"):
+            want = float(np.float32(_pow2_ceil_math(v)))
+        assert oracle_mod.pow2_ceil(v) == want, v
+
+
+def _torch_e4m3(y: torch.Tensor) -> torch.Tensor:
+    return y.to(torch.float8_e4m3fn).to(torch.float32)
+
+
+def test_e4m3_round_matches_torch_cast(oracle_mod):
+    # every e4m3 value, every midpoint between neighbours (ties), and random points, both signs
+    codes = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    mids = (codes[:-1] + codes[1:]) / 2
+    rng = np.random.default_rng(2)
+    rand = torch.from_numpy(rng.uniform(0, 448, 3000))
+    ys = torch.cat([codes, mids, rand, codes[1:] * (1 + 2 ** -12), codes[1:] * (1 - 2 ** -12)])
+    ys = torch.cat([ys, -ys]).to(torch.float32).clamp(-448, 448)
+    want = _torch_e4m3(ys)
+    got = torch.tensor([oracle_mod.e4m3_round(float(y)) for y in ys], dtype=torch.float32)
+    assert torch.equal(got, want)
+
+
+def _quant_reference_torch(x_bf16: torch.Tensor) -> torch.Tensor:
+    """The round trip with library primitives: f32 amax/448, frexp pow2 ceiling, torch fp8 cast."""
+    x = x_bf16.to(torch.float32).view(-1, 32)
+    amax = x.abs().amax(dim=1).clamp(min=torch.tensor(1e-4, dtype=torch.float32))
+    r = amax / torch.tensor(448.0, dtype=torch.float32)
+    m, e = torch.frexp(r)
+    scale = torch.where(m == 0.5, r, torch.ldexp(torch.ones_like(r), e))
+    y = (x / scale[:, None]).clamp(-448, 448)
+    return (_torch_e4m3(y) * scale[:, None]).to(torch.bfloat16).view(x_bf16.shape)
+
+
+def test_quant_exhaustive_bf16_patterns_consecutive_blocks(oracle_mod):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = from_bits(pats).to(torch.float32)
+    finite = torch.isfinite(vals).numpy()
+    pats = np.where(finite, pats, np.uint16(0))
+    x = from_bits(pats).clone()
+    want = to_bits(_quant_reference_torch(x))
+    got = oracle_mod.act_quant_inplace(pats.copy())
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("anchor_exp", [-20, -9, -6, -1, 0, 3, 7, 12, 40])
+def test_quant_every_bf16_value_at_fixed_scale(oracle_mod, anchor_exp):
+    # each finite bf16 value of magnitude <= anchor goes through a block whose amax is the anchor,
+    # so the whole e4m3 range (subnormals and ties included) is exercised at one scale
+    anchor = 448.0 * 2.0 ** anchor_exp
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = from_bits(pats).to(torch.float64)
+    keep = torch.isfinite(vals) & (vals.abs() <= anchor)
+    vals = vals[keep].to(torch.bfloat16)
+    nb = (vals.numel() + 30) // 31
+    blocks = torch.zeros((nb, 32), dtype=torch.bfloat16)
+    flat = torch.zeros(nb * 31, dtype=torch.bfloat16)
+    flat[: vals.numel()] = vals
+    blocks[:, :31] = flat.view(nb, 31)
+    blocks[:, 31] = anchor
+    want = to_bits(_quant_reference_torch(blocks))
+    got = oracle_mod.act_quant_inplace(to_bits(blocks).reshape(-1))
+    assert np.array_equal(got, want.reshape(-1))
+
+
+def test_quant_random_blocks_match_library(oracle_mod):
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn((4096, 32), generator=g) * torch.exp(torch.randn((4096, 1), generator=g) * 6)
+    x = x.to(torch.bfloat16)
+    want = to_bits(_quant_reference_torch(x))
+    got = oracle_mod.act_quant_inplace(to_bits(x).reshape(-1))
+    assert np.array_equal(got, want.reshape(-1))
+
+
+def test_quant_properties(oracle_mod):
+    g = torch.Generator().manual_seed(4)
+    x = to_bits(torch.randn((512, 32), generator=g)).reshape(-1)
+    once = oracle_mod.act_quant_inplace(x.copy())
+    twice = oracle_mod.act_quant_inplace(once.copy())
+    assert np.array_equal(once, twice)                       # idempotent
+    zero = np.zeros(64, dtype=np.uint16)
+    assert np.array_equal(oracle_mod.act_quant_inplace(zero.copy()), zero)   # amax floor, no NaN
+    # values already on the e4m3 grid times a block-wide power of two are unchanged
+    codes = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32)
+    rng = np.random.default_rng(5)
+    for k in (-12, -3, 0, 5, 20):
+        blk = codes[rng.integers(0, 127, 32)] * (2.0 ** k)
+        blk[0] = 448.0 * 2.0 ** k
+        blk = blk * torch.from_numpy(rng.choice([-1.0, 1.0], 32)).to(torch.float32)
+        b = to_bits(blk)
+        assert np.array_equal(oracle_mod.act_quant_inplace(b.copy()), b)
+    # every output is e4m3 * 2^k for the block's scale: dividing by the scale lands on the grid
+    vals = bits_to_f64(once).reshape(-1, 32)
+    src = bits_to_f64(x).reshape(-1, 32)
+    for r in range(0, 512, 37):
+        amax = max(np.abs(src[r]).max(), 1e-4)
+        scale = _pow2_ceil_math(float(np.float32(np.float32(amax) / np.float32(448.0))))
+        y = torch.from_numpy(vals[r] / scale).to(torch.float32)
+        assert torch.equal(_torch_e4m3(y), y)
+
+
+# ----------------------------------------------------------------------------------------------
+# ring write: the worked example
+# ----------------------------------------------------------------------------------------------
+
+def _token_rows(tokens, d):
+    # row of token t holds the value t+1 everywhere: small integers sit on the fp8 grid, so the
+    # round trip leaves them unchanged and the ring contents name their tokens
+    return to_bits(torch.tensor([[float(t + 1)] * d for t in tokens], dtype=torch.float32))
+
+
+def test_ring_worked_example(oracle_mod):
+    g = read_golden_ring()
+    W, S = g["window"][0], g["prefill_tokens"][0]
+    d = 64
+    ring = np.zeros((1, W, d), dtype=np.uint16)
+    chunk = _token_rows(range(S), d).reshape(1, S, d)
+    oracle_mod.kv_quant_ring_write(chunk, ring, 0, W)
+    slot_tokens = bits_to_f64(ring)[0, :, 0].astype(int) - 1
+    assert slot_tokens.tolist() == g["ring_after_prefill"]
+    for step, slot, ring_after, _row in g["decode"]:
+        new = _token_rows([step], d).reshape(1, 1, d)
+        before = ring.copy()
+        oracle_mod.kv_quant_ring_write(new, ring, step, W)
+        changed = np.nonzero((ring != before).any(axis=2)[0])[0].tolist()
+        assert changed == [slot]
+        assert (bits_to_f64(ring)[0, :, 0].astype(int) - 1).tolist() == ring_after
+
+
+def test_ring_write_rounds_in_place_and_keeps_last_window(oracle_mod):
+    g = torch.Generator().manual_seed(6)
+    b, s, d, W, p0 = 3, 20, 64, 8, 37
+    raw = to_bits(torch.randn((b, s, d), generator=g))
+    kv = raw.copy()
+    ring = np.full((b, W, d), 0x7f7f, dtype=np.uint16)
+    oracle_mod.kv_quant_ring_write(kv, ring, p0, W)
+    want = oracle_mod.act_quant_inplace(raw.copy().reshape(-1)).reshape(b, s, d)
+    assert np.array_equal(kv, want)
+    for t in range(s - W, s):
+        assert np.array_equal(ring[:, (p0 + t) % W], want[:, t])
+
+
+# ----------------------------------------------------------------------------------------------
+# sparse_attn
+# ----------------------------------------------------------------------------------------------
+
+def _rand_case(seed, b=2, m=3, h=5, d=32, n=40, topk=24, neg=0.2, dup=False):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((b, m, h, d), generator=g).to(torch.bfloat16)
+    kv = torch.randn((b, n, d), generator=g).to(torch.bfloat16)
+    sink = torch.randn((h,), generator=g)
+    if dup:
+        idx = torch.randint(0, n, (b, m, topk), generator=g)
+    else:
+        idx = torch.stack([torch.randperm(n, generator=g)[:topk] for _ in range(b * m)]).view(b, m, topk)
+    mask = torch.rand((b, m, topk), generator=g) < neg
+    idx = torch.where(mask, -1, idx).to(torch.int32)
+    return q, kv, sink, idx
+
+
+def _dense_masked_reference(q, kv, sink, idx, scale):
+    """Textbook dense attention over all n rows with a -inf mask for rows not in the index set,
+    plus one sink column appended to the scores and dropped after the softmax.  Requires distinct
+    indices per row (a set, like the mask it builds)."""
+    q64, kv64 = q.to(torch.float64), kv.to(torch.float64)
+    b, m, h, d = q.shape
+    n = kv.shape[1]
+    out = torch.zeros((b, m, h, d), dtype=torch.float64)
+    for bi in range(b):
+        scores = torch.einsum("mhd,nd->mhn", q64[bi], kv64[bi]) * scale
+        mask = torch.full((m, n), float("-inf"), dtype=torch.float64)
+        for t in range(m):
+            sel = idx[bi, t][idx[bi, t] >= 0].long()
+            mask[t, sel] = 0.0
+        scores = scores + mask[:, None, :]
+        scores = torch.cat([scores, sink.to(torch.float64)[None, :, None].expand(m, h, 1)], dim=-1)
+        p = torch.softmax(scores, dim=-1)[..., :n]
+        out[bi] = torch.einsum("mhn,nd->mhd", p, kv64[bi])
+    return out
+
+
+def _gathered_reference(q, kv, sink, idx, scale):
+    """Softmax over the gathered list (duplicates count as often as listed) plus the sink."""
+    q64, kv64 = q.to(torch.float64), kv.to(torch.float64)
+    b, m, h, d = q.shape
+    out = torch.zeros((b, m, h, d), dtype=torch.float64)
+    for bi in range(b):
+        for t in range(m):
+            sel = idx[bi, t][idx[bi, t] >= 0].long()
+            rows = kv64[bi, sel]                                   # [k, d]
+            sc = (q64[bi, t] @ rows.T) * scale                     # [h, k]
+            sc = torch.cat([sc, sink.to(torch.float64)[:, None]], dim=1)
+            p = torch.softmax(sc, dim=1)[:, :-1]
+            out[bi, t] = p @ rows
+    return out
+
+
+def f32(x: float) -> float:
+    """The softmax scale crosses every interface as an f32."""
+    return float(np.float32(x))
+
+
+def _run_oracle(oracle_mod, q, kv, sink, idx, scale, f64=True, tokens=None):
+    return oracle_mod.sparse_attn(to_bits(q), to_bits(kv), sink.numpy(), idx.numpy(), scale,
+                                  tokens=tokens, f64=f64, nthreads=2)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_attn_matches_dense_masked_softmax(oracle_mod, seed):
+    q, kv, sink, idx = _rand_case(seed)
+    scale = f32(32 ** -0.5)
+    want = _dense_masked_reference(q, kv, sink, idx, scale).numpy()
+    got64 = _run_oracle(oracle_mod, q, kv, sink, idx, scale)
+    np.testing.assert_allclose(got64, want, rtol=1e-12, atol=1e-13)
+    got32 = bits_to_f64(_run_oracle(oracle_mod, q, kv, sink, idx, scale, f64=False))
+    # f32 arithmetic then one bf16 rounding: within half a bf16 ulp plus f32 noise
+    np.testing.assert_allclose(got32, want, rtol=2 ** -8 + 1e-5, atol=1e-6)
+
+
+def test_attn_duplicates_count_as_listed(oracle_mod):
+    q, kv, sink, idx = _rand_case(7, dup=True, n=10, topk=24)
+    scale = f32(0.3)
+    want = _gathered_reference(q, kv, sink, idx, scale).numpy()
+    got = _run_oracle(oracle_mod, q, kv, sink, idx, scale)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+def test_attn_sink_to_minus_infinity_is_sdpa(oracle_mod):
+    q, kv, sink, idx = _rand_case(8, neg=0.0)
+    scale = f32(32 ** -0.5)
+    sink_off = torch.full_like(sink, -1e30)
+    got = _run_oracle(oracle_mod, q, kv, sink_off, idx, scale)
+    b, m, h, d = q.shape
+    for bi in range(b):
+        for t in range(m):
+            rows = kv[bi, idx[bi, t].long()].to(torch.float64)
+            want = torch.nn.functional.scaled_dot_product_attention(
+                q[bi, t].to(torch.float64)[None], rows[None], rows[None], scale=scale)[0]
+            np.testing.assert_allclose(got[bi * m + t] if got.ndim == 3 else got[bi, t], want.numpy(),
+                                       rtol=1e-12, atol=1e-13)
+
+
+def test_attn_probability_mass_below_one_and_tends_to_one(oracle_mod):
+    # with every gathered row equal to v, o = v * sum_j p_j, so the mass is read off o / v
+    g = torch.Generator().manual_seed(9)
+    d, h, k = 16, 3, 6
+    v = torch.randn((d,), generator=g).to(torch.bfloat16)
+    kv = v[None, None, :].expand(1, k, d).contiguous()
+    q = torch.randn((1, 1, h, d), generator=g).to(torch.bfloat16)
+    idx = torch.arange(k, dtype=torch.int32).view(1, 1, k)
+    scale = f32(0.25)
+    s = (q[0, 0].to(torch.float64) @ v.to(torch.float64)) * scale               # [h]
+    v64 = v.to(torch.float64).numpy()
+    masses = []
+    for sink_val in (3.0, 0.0, -5.0, -40.0, -1e30):
+        sink = torch.full((h,), sink_val)
+        got = _run_oracle(oracle_mod, q, kv, sink, idx, scale)[0, 0]
+        mass_closed = 1.0 / (1.0 + torch.exp(torch.tensor(sink_val, dtype=torch.float64) - s - math.log(k)))
+        np.testing.assert_allclose(got, (mass_closed[:, None] * v.to(torch.float64)[None]).numpy(),
+                                   rtol=1e-12, atol=1e-14)
+        masses.append(got @ v64 / (v64 @ v64))               # the mass each head put on the rows
+    masses = np.array(masses)
+    assert (masses[:3] < 1).all()                           # the sink takes a share
+    assert (np.diff(masses, axis=0) >= 0).all()             # and gives it back as it falls
+    np.testing.assert_allclose(masses[-1], 1.0, rtol=1e-14)
+
+
+def test_attn_single_valid_row_closed_form(oracle_mod):
+    q, kv, sink, idx = _rand_case(10, topk=9, neg=0.0)
+    idx[:] = -1
+    idx[:, :, 4] = 7
+    scale = f32(0.2)
+    got = _run_oracle(oracle_mod, q, kv, sink, idx, scale)
+    b, m, h, d = q.shape
+    for bi in range(b):
+        row = kv[bi, 7].to(torch.float64)
+        for t in range(m):
+            s = (q[bi, t].to(torch.float64) @ row) * scale
+            w = torch.sigmoid(s - sink.to(torch.float64))
+            np.testing.assert_allclose(got[bi, t], (w[:, None] * row[None]).numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_attn_all_invalid_row_is_zero(oracle_mod):
+    q, kv, sink, idx = _rand_case(11)
+    idx[1, 2] = -1
+    got32 = _run_oracle(oracle_mod, q, kv, sink, idx, 0.5, f64=False)
+    got64 = _run_oracle(oracle_mod, q, kv, sink, idx, 0.5)
+    assert (got32[1, 2] == 0).all() and (got64[1, 2] == 0).all()
+    assert (got64[0, 0] != 0).any()
+
+
+def test_attn_order_and_padding_invariance(oracle_mod):
+    q, kv, sink, idx = _rand_case(12, neg=0.3)
+    scale = f32(0.17)
+    base = _run_oracle(oracle_mod, q, kv, sink, idx, scale)
+    g = torch.Generator().manual_seed(13)
+    perm = torch.randperm(idx.shape[-1], generator=g)
+    np.testing.assert_allclose(_run_oracle(oracle_mod, q, kv, sink, idx[..., perm].contiguous(), scale), base,
+                               rtol=1e-12, atol=1e-14)
+    padded = torch.cat([torch.full_like(idx[..., :5], -1), idx, torch.full_like(idx[..., :3], -1)], dim=-1)
+    np.testing.assert_allclose(_run_oracle(oracle_mod, q, kv, sink, padded.contiguous(), scale), base,
+                               rtol=1e-12, atol=1e-14)
+
+
+def test_attn_token_subset_matches_full(oracle_mod):
+    q, kv, sink, idx = _rand_case(14, b=3, m=4)
+    full = _run_oracle(oracle_mod, q, kv, sink, idx, 0.3, f64=False)
+    toks = np.array([11, 0, 5], dtype=np.int64)
+    sub = _run_oracle(oracle_mod, q, kv, sink, idx, 0.3, f64=False, tokens=toks)
+    for k, tok in enumerate(toks):
+        assert np.array_equal(sub[k], full.reshape(-1, *full.shape[2:])[tok])
+
+
+def test_attn_rejects_out_of_range_index(oracle_mod):
+    q, kv, sink, idx = _rand_case(15)
+    idx[0, 0, 0] = kv.shape[1]
+    with pytest.raises(ValueError):
+        _run_oracle(oracle_mod, q, kv, sink, idx, 0.3)
