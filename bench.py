@@ -1,0 +1,448 @@
+"""Benchmark of the sparse latent attention hot path on GB300.
+
+One step = the whole hot path over one batch: the fp8 round trip of the step's new KV rows into
+the ring, the window index rows, and sparse_attn over [ring | compressed rows] (all through the
+C ABI of libdsattn).  The metric is gathered (token, head, valid row) units per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 4] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (weak scaling, no data
+path collective); rank 0 prints one JSON line with value = units of all ranks / max time.
+`--impl reference` times the CPU oracle (plain C, all host cores) on a bounded sample of the
+same workload; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sparse_latent_attention_attn_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "decode sparse_attn gathered (token·head·row)/s; % of tensor/HBM roofline"
+UNIT = "(token·head·row)/s"
+DEFAULT_CONFIG = 4
+L2_BYTES = 129 * 1024 * 1024
+ATTN_KERNEL_SOURCES = ["sparse_latent_attention_attn_gb300/csrc/sparse_attn_simt.cu"]
+PROFILE_SUMMARY = "profiles/sparse_attn_{workload}.txt"
+
+
+# ----------------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no collective on the data path)
+# ----------------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def aggregate(units_local: float, seconds_local: float, world: int, device=None):
+    """Whole-job units and the slowest rank's time (max over ranks), via two all-reduces."""
+    if world == 1:
+        return units_local, seconds_local
+    t = torch.tensor([units_local], dtype=torch.float64, device=device)
+    s = torch.tensor([seconds_local], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    torch.distributed.all_reduce(s, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item()), float(s.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# ----------------------------------------------------------------------------------------------
+# peaks, clocks, profile summary
+# ----------------------------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.count(",") >= 9]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[2]))
+                smax = float(r[3])
+            except ValueError:
+                continue
+            for name, val in zip(names, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ATTN_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, launches_units: float):
+    """dram bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, PROFILE_SUMMARY.format(workload=workload))
+    if not os.path.exists(path):
+        return None
+    src_hash, traffic = None, None
+    with open(path) as f:
+        for line in f:
+            if line.startswith("kernel_source_sha256_16:"):
+                src_hash = line.split(":", 1)[1].strip()
+            if line.startswith("dram_bytes_per_launch:"):
+                traffic = float(line.split(":", 1)[1].strip())
+    if src_hash != kernel_source_hash():
+        return None
+    return traffic
+
+
+# ----------------------------------------------------------------------------------------------
+# one set of step inputs on the device
+# ----------------------------------------------------------------------------------------------
+
+class StepSet:
+    def __init__(self, w: wl.Workload, device, seed: int):
+        from sparse_latent_attention_attn_gb300 import dsattn
+        self.w = w
+        inp = wl.make_step_inputs(w, device=device, seed=seed)
+        self.q, self.kv, self.sink = inp.q, inp.kv, inp.sink
+        self.cidx = inp.cidx
+        self.idx = torch.empty((w.b, w.m, w.topk), dtype=torch.int32, device=device)
+        self.idx[..., w.win_cols:] = inp.cidx
+        self.o = torch.empty_like(inp.q)
+        if w.decode:
+            dsattn.kv_quant_ring_write(inp.hist, self.kv[:, : w.window], w.start_pos - w.window, w.window)
+            self.new_kv = inp.new_kv
+            self.ring = self.kv[:, : w.window]
+        else:
+            self.new_kv = None
+            self.ring = torch.zeros((w.b, w.window, w.d), dtype=torch.bfloat16, device=device)
+        del inp
+        need = dsattn.sparse_attn_workspace_bytes(w.b, w.m, w.h, w.d, w.topk)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+
+    def run(self, ev_attn=None):
+        """The whole step; events (start, end) bracket the sparse_attn launch when given."""
+        from sparse_latent_attention_attn_gb300 import dsattn
+        w = self.w
+        if w.decode:
+            dsattn.kv_quant_ring_write(self.new_kv, self.ring, w.start_pos, w.window)
+            dsattn.window_topk_idxs(self.idx, w.b, 1, w.start_pos, w.window)
+        else:
+            dsattn.kv_quant_ring_write(self.kv[:, : w.s], self.ring, 0, w.window)
+            dsattn.window_topk_idxs(self.idx, w.b, w.s, 0, w.window)
+        if ev_attn is not None:
+            ev_attn[0].record()
+        dsattn.sparse_attn(self.q, self.kv, self.sink, self.idx, w.scale, o=self.o, workspace=self.ws)
+        if ev_attn is not None:
+            ev_attn[1].record()
+
+    def counts(self):
+        """units, algorithmic bytes and flops of one sparse_attn launch (idx as the step leaves it)."""
+        w = self.w
+        valid = int((self.idx >= 0).sum().item())
+        units = valid * w.h
+        bytes_ = valid * w.d * 2 + 2 * w.b * w.m * w.h * w.d * 2 + self.idx.numel() * 4 + w.h * 4
+        flops = 4 * w.d * units
+        return units, bytes_, flops
+
+    def io_bytes(self):
+        """Bytes a step takes from and gives back to the host in the end-to-end measurement."""
+        w = self.w
+        h2d = self.q.numel() * 2 + self.cidx.numel() * 4
+        h2d += (self.new_kv.numel() * 2) if w.decode else (w.b * w.s * w.d * 2)
+        return h2d, self.o.numel() * 2
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ----------------------------------------------------------------------------------------------
+
+def oracle_sample_rate(w: wl.Workload, sset: StepSet | None, budget_s: float, device):
+    """Time the oracle (plain C, all host cores) on a bounded sample of the workload's tokens."""
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    if sset is None:
+        inp = wl.make_step_inputs(w, device=device)
+        idx = torch.empty((w.b, w.m, w.topk), dtype=torch.int32, device=device)
+        idx[..., w.win_cols:] = inp.cidx
+        q, kv, sink = inp.q, inp.kv, inp.sink
+    else:
+        idx, q, kv, sink = sset.idx, sset.q, sset.kv, sset.sink
+    # window columns as the oracle computes them
+    win = oracle.window_topk_idxs(w.s if not w.decode else 1, w.start_pos, w.window)
+    idx_host = idx.cpu().numpy()
+    idx_host[..., : w.win_cols] = win[None] if w.decode else win[None]
+    sink_h = sink.cpu().numpy()
+    # sample whole sequences (decode) or query tokens of the one sequence (prefill)
+    tokens_per_seq = w.m
+
+    def run(nseq_or_tok):
+        if w.decode:
+            seqs = torch.arange(nseq_or_tok, device=q.device)
+            qb = wl.bits(q.index_select(0, seqs))
+            kvb = wl.bits(kv.index_select(0, seqs))
+            ib = np.ascontiguousarray(idx_host[:nseq_or_tok])
+            t0 = time.perf_counter()
+            oracle.sparse_attn(qb, kvb, sink_h, ib, w.scale, nthreads=cores)
+            dt = time.perf_counter() - t0
+            units = int((ib >= 0).sum()) * w.h
+        else:
+            toks = np.linspace(0, w.m - 1, nseq_or_tok).astype(np.int64)
+            qb, kvb = wl.bits(q), wl.bits(kv)
+            t0 = time.perf_counter()
+            oracle.sparse_attn(qb, kvb, sink_h, idx_host, w.scale, tokens=toks, nthreads=cores)
+            dt = time.perf_counter() - t0
+            units = int((idx_host[0, toks] >= 0).sum()) * w.h
+        return dt, units
+
+    limit = w.b if w.decode else tokens_per_seq
+    n = min(limit, max(1, cores))
+    dt, units = run(n)
+    if dt < budget_s / 4 and n < limit:
+        n = int(min(limit, max(n + 1, n * budget_s / max(dt, 1e-3) * 0.8)))
+        dt, units = run(n)
+    what = "sequences" if w.decode else "query tokens"
+    return {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {limit} {what} of {w.name} ({units} units, {dt:.2f} s wall, plain C, {cores} threads)",
+            "_units": units, "_seconds": dt}
+
+
+def public(d):
+    return None if d is None else {k: v for k, v in d.items() if not k.startswith("_")}
+
+
+# ----------------------------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------------------------
+
+def workload_config(w: wl.Workload, nsets: int):
+    return {"workload": f"{w.name}: b={w.b} h={w.h} d={w.d} window={w.window} start_pos={w.start_pos} "
+                        f"queries/seq={w.m} compressed={w.topk_comp} of {w.n_comp} rows, "
+                        f"{w.neg_frac:.0%} of them -1",
+            "global_batch": w.b, "seq_len": w.m, "topk": w.topk, "heads": w.h, "head_dim": w.d,
+            "parallelism": "replicas (one independent batch per GPU)",
+            "l2": f"{nsets} rotating input sets; each step's gathered rows exceed or rotate past the "
+                  f"{L2_BYTES >> 20} MiB L2"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    w = wl.WORKLOADS[args.config]
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    total_units, total_s = 0, 0.0
+    per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    cb = None
+    for k in range(args.warmup + args.steps):
+        cb = oracle_sample_rate(w, None, per_step_budget, device)
+        if k >= args.warmup:
+            total_units += cb["_units"]
+            total_s += cb["_seconds"]
+    value = total_units / total_s if total_s else 0.0
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": 1e3 * total_s / max(1, args.steps), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, N(0,1))",
+           "config": workload_config(w, 1),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+                            "sample": cb["sample"]},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    from sparse_latent_attention_attn_gb300 import dsattn
+    w = wl.WORKLOADS[args.config]
+    peaks = load_peaks()
+
+    # enough independent input sets that the gathered rows of consecutive steps miss in L2
+    per_set_bytes = w.b * w.m * w.topk * w.d * 2
+    nsets = args.sets or max(1, min(24, -(-4 * L2_BYTES // max(per_set_bytes, 1))))
+    if w.n_comp * w.b * w.d * 2 > 4 * L2_BYTES:
+        nsets = args.sets or 2
+    sets = [StepSet(w, device, seed=w.seed + 7919 * k + 104729 * rank) for k in range(nsets)]
+    torch.cuda.synchronize()
+
+    # warm-up
+    for k in range(args.warmup):
+        sets[k % nsets].run()
+    torch.cuda.synchronize()
+    units, alg_bytes, flops = sets[0].counts()
+    dsattn.device_status()
+
+    # timed region: exactly K steps, barrier + synchronize on both sides
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for k in range(args.steps):
+        sets[k % nsets].run(ev_attn[k])
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_s = start.elapsed_time(end) / 1e3
+    attn_ms = [a.elapsed_time(b) for a, b in ev_attn]
+    status = dsattn.device_status()
+    units_all, slowest_s = aggregate(float(units) * args.steps, elapsed_s, world, device)
+    value = units_all / slowest_s
+
+    # end to end through the public API: host inputs in, host output out, every step
+    h2d, d2h = sets[0].io_bytes()
+    e2e = None
+    if args.e2e_steps > 0:
+        s0 = sets[0]
+        q_h = s0.q.cpu().pin_memory()
+        c_h = s0.cidx.cpu().pin_memory()
+        new_h = (s0.new_kv.cpu() if w.decode else s0.kv[:, : w.s].cpu()).pin_memory()
+        o_h = torch.empty(s0.o.shape, dtype=s0.o.dtype).pin_memory()
+        s0.run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.e2e_steps):
+            s0.q.copy_(q_h, non_blocking=True)
+            s0.idx[..., w.win_cols:].copy_(c_h, non_blocking=True)
+            if w.decode:
+                s0.new_kv.copy_(new_h, non_blocking=True)
+            else:
+                s0.kv[:, : w.s].copy_(new_h, non_blocking=True)
+            s0.run()
+            o_h.copy_(s0.o, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_units, e2e_s = aggregate(float(units) * args.e2e_steps, e0.elapsed_time(e1) / 1e3, world, device)
+        e2e = {"value": e2e_units / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample_rate(w, sets[0], args.cpu_budget, device)
+
+    if rank == 0:
+        attn_s = statistics.mean(attn_ms) / 1e3
+        t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+        if t_hbm >= t_tc:
+            roof = {"bound": "hbm", "achieved": alg_bytes / attn_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        else:
+            roof = {"bound": "tensor", "achieved": flops / attn_s / 1e12, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["traffic"] = profiled_traffic(w.name, 1)
+        roof["peak_source"] = peaks["source"]
+        roof["kernel"] = "sparse_attn"
+        roof["kernel_ms"] = attn_s * 1e3
+        roof["roofline_ms"] = max(t_hbm, t_tc) * 1e3
+        roof["algorithmic_bytes"] = alg_bytes
+        roof["algorithmic_flops"] = flops
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": 1e3 * slowest_s / args.steps, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, f32 accumulate",
+               "data": "synthetic (seeded, N(0,1) bf16 q/kv, N(0,1) f32 sink)",
+               "config": workload_config(w, nsets), "roofline": roof, "cpu_baseline": public(cpu), "e2e": e2e,
+               "gpu_launches": 3 * args.steps, "clocks": clk, "device_status": status,
+               "units_per_step": units}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate through (0 = automatic)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+/*
+ * dsattn.h -- C ABI of libdsattn, the GB300 (sm_103a) hot path of DeepSeek-V4.1 sparse latent
+ * attention: the sliding-window index rows, the fp8 round trip of new KV rows into the ring,
+ * and sparse_attn itself (gathered-row latent attention with an attention sink).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers, owned by the caller.  The library allocates no
+ *     device memory and keeps no state between calls (apart from one device status word per
+ *     device, see ds_device_status).
+ *   - bf16 tensors are passed as uint16_t bit patterns; all tensors are dense, row-major.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *     and never synchronises.  A returned DS_OK means the work was enqueued.
+ *   - Errors are returned as negative codes (below); nothing is enqueued on an argument error.
+ *
+ * Sources are cited by page title and section:
+ *   "DeepSeek V4.1", attention/attend        get_window_topk_idxs, sparse_attn_kernel, sparse_attn
+ *   "DeepSeek V4.1", attention/query-latent  Attention.__init__ (window_kv_cache ring),
+ *                                            Attention.forward (window + compressed concatenation)
+ *   "Module attn" (deepseek_v41_ref)         Precision paragraph, ring-cache paragraph, FP8_BLOCK,
+ *                                            act_quant_inplace, pow2_ceil, sparse_attn,
+ *                                            window_topk_idxs, WindowCache, attention
+ */
+#ifndef DSATTN_H
+#define DSATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st *ds_stream_t;
+
+/* Status codes. */
+#define DS_OK 0
+#define DS_EINVAL (-1)        /* null pointer, negative size, misaligned pointer or stride    */
+#define DS_EUNSUPPORTED (-2)  /* a shape outside the compiled set (see each call)              */
+#define DS_EWORKSPACE (-3)    /* workspace smaller than ds_sparse_attn_workspace_bytes()      */
+#define DS_ECUDA (-4)         /* a CUDA runtime call or kernel launch failed                  */
+#define DS_EDEVICE (-5)       /* ds_device_status: a kernel flagged a problem (see bits below) */
+
+/* Bits of the device status word (ds_device_status). */
+#define DS_DEV_TIMEOUT 1u     /* a bounded wait inside a kernel gave up; that launch's output is invalid */
+#define DS_DEV_BAD_INDEX 2u   /* an index >= n was seen; the entry was skipped                       */
+
+/*
+ * ds_window_topk_idxs -- sliding-window ring-slot index rows.
+ * Source: "DeepSeek V4.1", attention/attend, get_window_topk_idxs; "Module attn", window_topk_idxs.
+ *
+ *   start_pos == 0 (prefill, s queries): cols = min(s, window).  Row q, column j holds
+ *       v = max(0, q - window + 1) + j, or -1 when v > q (the causal window of query q into the
+ *       chunk itself).  Rows are written for q = 0..s-1.
+ *   start_pos  > 0 (decode, s must be 1): cols = window.  The single row lists the whole ring
+ *       oldest first: column j holds v = (start_pos % window + 1 + j) mod window, or -1 when
+ *       v > start_pos (ring still filling).
+ *
+ * idx        device int32, row (bi, q) starts at idx + (bi * rows + q) * ld, rows = s (prefill)
+ *            or 1 (decode); only columns [0, cols) are written, so compressed indices can sit in
+ *            columns [cols, ld) of the same rows (the concatenation of Attention.forward).
+ * ld         row stride in int32 elements, >= cols.
+ * b          sequences; the rows are the same for every sequence.
+ * cols_out   optional HOST pointer that receives cols.
+ * Errors: DS_EINVAL (null idx, b < 0, s < 1, window < 1, start_pos < 0, ld < cols);
+ *         DS_EUNSUPPORTED for a chunked prefill (start_pos > 0 and s > 1), which the pages do not
+ *         define.
+ */
+int ds_window_topk_idxs(int32_t *idx, int64_t ld, int b, int s, int64_t start_pos, int window,
+                        int *cols_out, ds_stream_t stream);
+
+/*
+ * ds_kv_quant_ring_write -- fp8 round trip of new KV rows, in place, and their ring store.
+ * Sources: "Module attn", FP8_BLOCK, pow2_ceil, act_quant_inplace, the Precision paragraph (the
+ * round trip is bf16-exact) and the ring-cache paragraph; "DeepSeek V4.1", attention/query-latent,
+ * Attention.__init__ (window_kv_cache [max_batch][window][head_dim]).
+ *
+ * Every block of 32 consecutive values of each row: amax = max |x| floored at 1e-4;
+ * scale = 2^ceil(log2(amax / 448)) (f32 division, IEEE fields); x / scale clamped to +-448 and
+ * rounded to e4m3 (round to nearest even); the result times scale, which is exact in bf16,
+ * replaces x.  Then the token at position start_pos + t is stored to ring slot
+ * (start_pos + t) % window when t >= s - window (the last `window` rows of the chunk).
+ *
+ * kv         device bf16 [b][s][d] rows, row stride d, batch stride kv_bstride (elements); in/out.
+ * ring       device bf16, slot (bi, k) at ring + bi * ring_bstride + k * d; may be NULL when no
+ *            ring store is wanted.  The ring may live inside a larger kv tensor (ring_bstride =
+ *            that tensor's batch stride) so sparse_attn reads it without a copy.
+ * d          multiple of 32; pointers 16-byte aligned; strides multiples of 8 elements.
+ * Bit-exact with the definition above.  The ring slots written must not overlap the rows read.
+ * Errors: DS_EINVAL (null kv, d % 32 != 0, misalignment, negative sizes, window < 1).
+ */
+int ds_kv_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride,
+                           int b, int s, int d, int64_t start_pos, int window, ds_stream_t stream);
+
+/*
+ * ds_sparse_attn_workspace_bytes -- bytes of device workspace ds_sparse_attn needs for this
+ * shape on the current device (0 when none).  Pure host function; the result depends on the
+ * current device's SM count.  Returns 0 for shapes ds_sparse_attn rejects.
+ */
+size_t ds_sparse_attn_workspace_bytes(int b, int m, int h, int d, int topk);
+
+/*
+ * ds_sparse_attn -- gathered-row latent attention with an attention sink.
+ * Sources: "Module attn", sparse_attn and the Precision paragraph; "DeepSeek V4.1",
+ * attention/attend, sparse_attn_kernel and its sparse_attn wrapper; attention/query-latent,
+ * Attention.forward (kv = window rows then compressed rows, indices concatenated likewise).
+ *
+ * For each sequence bi, query t and head hh, over the entries j of idx[bi][t] with idx >= 0:
+ *     s_j = scale * dot(q[bi][t][hh], kv[bi][idx_j])
+ *     o[bi][t][hh] = sum_j exp(s_j) * kv[bi][idx_j] / (sum_j exp(s_j) + exp(sink[hh]))
+ * The sink counts in the denominator only; the gathered rows are both keys and values; entries
+ * < 0 are skipped; a query with no entry gives o = 0.  Scores, softmax and accumulation are f32;
+ * the probabilities are rounded to bf16 before the value product (as the pages' kernel does);
+ * o is bf16.  Agreement with an f32 evaluation: |diff| <= 1e-2 + 1.6e-2 * |ref| elementwise.
+ * Duplicate indices count as often as they are listed.
+ *
+ * q          device bf16 [b][m][h][d]
+ * kv         device bf16 [b][n][d]
+ * n          rows per sequence in kv (indices must be < n; larger ones are skipped and flagged
+ *            with DS_DEV_BAD_INDEX)
+ * sink       device f32 [h]
+ * idx        device int32 [b][m][topk]
+ * scale      softmax scale (head_dim^-0.5 in the model)
+ * o          device bf16 [b][m][h][d], written
+ * workspace  device scratch of at least ds_sparse_attn_workspace_bytes(b, m, h, d, topk) bytes,
+ *            256-byte aligned (may be NULL when that size is 0); contents need no initialisation
+ *            and are not meaningful after the call.
+ * Supported: d in {64, 128, 256, 512}; 1 <= h <= 128; topk >= 0; pointers 16-byte aligned.
+ * Errors: DS_EINVAL, DS_EUNSUPPORTED, DS_EWORKSPACE, DS_ECUDA.
+ */
+int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink,
+                   const int32_t *idx, int topk, float scale, uint16_t *o, int b, int m, int h, int d,
+                   void *workspace, size_t workspace_bytes, ds_stream_t stream);
+
+/*
+ * ds_device_status -- synchronise `stream`, then read and clear the current device's status word
+ * (DS_DEV_* bits set by kernels since the last read).  Returns DS_OK when the word was 0,
+ * DS_EDEVICE when a bit was set (the bits are stored to *bits_out when it is not NULL), or
+ * DS_ECUDA.  This is the only call that synchronises.
+ */
+int ds_device_status(ds_stream_t stream, unsigned int *bits_out);
+
+/* ds_status_string -- static text for a status code. */
+const char *ds_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSATTN_H */

@@ -1,0 +1,108 @@
+// abi.cu -- the extern "C" entry points of libdsattn (declared in include/dsattn.h): argument
+// checks, the per-device status word, and dispatch to the kernels.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace dsattn {
+namespace {
+
+// One status word per device; kernels OR DS_DEV_* bits into it.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mutex;
+unsigned int *g_status_ptr[kMaxDevices];
+
+// Device address of this device's status word (host code may not take &g_status_word).
+unsigned int *status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
+
+}  // namespace
+}  // namespace dsattn
+
+using namespace dsattn;
+
+extern "C" {
+
+int ds_window_topk_idxs(int32_t *idx, int64_t ld, int b, int s, int64_t start_pos, int window, int *cols_out,
+                        ds_stream_t stream) {
+    if (!idx || b < 0 || s < 1 || window < 1 || start_pos < 0) return DS_EINVAL;
+    if (start_pos > 0 && s != 1) return DS_EUNSUPPORTED;
+    const int cols = start_pos == 0 ? (s < window ? s : window) : window;
+    const int rows = start_pos == 0 ? s : 1;
+    if (ld < cols) return DS_EINVAL;
+    if (cols_out) *cols_out = cols;
+    return launch_window_idx(idx, ld, b, rows, cols, start_pos, window, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ds_kv_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b, int s,
+                           int d, int64_t start_pos, int window, ds_stream_t stream) {
+    if (!kv || b < 0 || s < 0 || d <= 0 || d % 32 != 0 || window < 1 || start_pos < 0) return DS_EINVAL;
+    if (kv_bstride < (int64_t)s * d || kv_bstride % 8 != 0 || !aligned16(kv)) return DS_EINVAL;
+    if (ring && (ring_bstride < (int64_t)window * d || ring_bstride % 8 != 0 || !aligned16(ring))) return DS_EINVAL;
+    return launch_kv_quant_ring(kv, kv_bstride, ring, ring_bstride, b, s, d, start_pos, window,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t ds_sparse_attn_workspace_bytes(int b, int m, int h, int d, int topk) {
+    if (b < 0 || m < 0 || h < 1 || h > 128 || topk < 0 || !supported_head_dim(d)) return 0;
+    return 0;
+}
+
+int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink, const int32_t *idx,
+                   int topk, float scale, uint16_t *o, int b, int m, int h, int d, void *workspace,
+                   size_t workspace_bytes, ds_stream_t stream) {
+    if (b < 0 || m < 0 || n < 0 || topk < 0 || h < 1) return DS_EINVAL;
+    if (!supported_head_dim(d) || h > 128) return DS_EUNSUPPORTED;
+    if ((int64_t)b * m == 0) return DS_OK;
+    if (!q || !o || !sink || (topk > 0 && (!idx || !kv))) return DS_EINVAL;
+    if (!aligned16(q) || !aligned16(o) || (kv && !aligned16(kv))) return DS_EINVAL;
+    const size_t need = ds_sparse_attn_workspace_bytes(b, m, h, d, topk);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return DS_EWORKSPACE;
+    AttnArgs a{q, kv, n, sink, idx, topk, scale, o, b, m, h, d, workspace, workspace_bytes, status_word()};
+    if (!a.status) return DS_ECUDA;
+    return launch_sparse_attn_simt(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ds_device_status(ds_stream_t stream, unsigned int *bits_out) {
+    unsigned int *p = status_word();
+    if (!p) return DS_ECUDA;
+    unsigned int bits = 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DS_ECUDA;
+    if (cudaMemcpy(&bits, p, sizeof bits, cudaMemcpyDeviceToHost) != cudaSuccess) return DS_ECUDA;
+    if (bits) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return DS_ECUDA;
+    }
+    if (bits_out) *bits_out = bits;
+    return bits ? DS_EDEVICE : DS_OK;
+}
+
+const char *ds_status_string(int status) {
+    switch (status) {
+        case DS_OK: return "ok";
+        case DS_EINVAL: return "invalid argument";
+        case DS_EUNSUPPORTED: return "unsupported shape";
+        case DS_EWORKSPACE: return "workspace too small";
+        case DS_ECUDA: return "CUDA error";
+        case DS_EDEVICE: return "a kernel flagged a device-side problem";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

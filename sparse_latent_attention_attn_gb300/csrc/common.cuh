@@ -1,0 +1,47 @@
+// common.cuh -- shared device helpers of libdsattn (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsattn.h"
+
+namespace dsattn {
+
+// Launch helpers return DS_OK / DS_ECUDA.
+inline int launch_status() { return cudaGetLastError() == cudaSuccess ? DS_OK : DS_ECUDA; }
+
+__device__ __forceinline__ void flag_status(unsigned int *status, unsigned int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// ------------------------------------------------------------------------------------------
+// Kernel entry points (defined in the per-kernel translation units).
+// ------------------------------------------------------------------------------------------
+int launch_window_idx(int32_t *idx, int64_t ld, int b, int rows, int cols, int64_t start_pos, int window,
+                      cudaStream_t stream);
+int launch_kv_quant_ring(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b, int s,
+                         int d, int64_t start_pos, int window, cudaStream_t stream);
+
+struct AttnArgs {
+    const uint16_t *q;
+    const uint16_t *kv;
+    int64_t n;
+    const float *sink;
+    const int32_t *idx;
+    int topk;
+    float scale;
+    uint16_t *o;
+    int b, m, h, d;
+    void *workspace;
+    size_t workspace_bytes;
+    unsigned int *status;
+};
+
+int launch_sparse_attn_simt(const AttnArgs &a, cudaStream_t stream);
+
+}  // namespace dsattn

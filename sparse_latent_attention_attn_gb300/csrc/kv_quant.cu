@@ -1,0 +1,108 @@
+// kv_quant.cu -- fp8 round trip of new KV rows in place, fused with the ring-slot store.
+//
+// "Module attn": FP8_BLOCK (32 values per scale), pow2_ceil (power-of-two ceiling from the IEEE
+// fields of an f32), act_quant_inplace (amax floored at 1e-4, scale = pow2_ceil(amax / 448),
+// e4m3 with round-to-nearest-even and clamping, dequantised and rounded to bf16), the Precision
+// paragraph (the round trip is bf16-exact) and the ring-cache paragraph (token at position p
+// lives in slot p % window; a prefill keeps the last `window` tokens of the chunk).
+//
+// One thread owns one 32-value block (64 contiguous bytes): it loads the block once, decides
+// the scale in f32 exactly as defined, converts pairs with the documented PTX conversion
+// cvt.rn.satfinite.e4m3x2.f32 (round to nearest even, saturating at +-448) and widens back with
+// cvt.rn.f16x2.e4m3x2 (exact), then stores the block in place and, when the token is among the
+// last `window` of the chunk, into its ring slot.  Memory-bound: 64 B read, 64-128 B written.
+#include "common.cuh"
+
+namespace dsattn {
+namespace {
+
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+    return __half2float(__ushort_as_half((unsigned short)h));
+}
+
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__global__ void __launch_bounds__(256) kv_quant_ring_kernel(uint16_t *__restrict__ kv, int64_t kv_bstride,
+                                                            uint16_t *__restrict__ ring, int64_t ring_bstride,
+                                                            int b, int s, int d, int64_t start_pos, int window) {
+    const int nblk = d / 32;
+    const int64_t total = (int64_t)b * s * nblk;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(e % nblk);
+        const int64_t r = e / nblk;
+        const int t = (int)(r % s);
+        const int64_t bi = r / s;
+        uint4 *src = reinterpret_cast<uint4 *>(kv + bi * kv_bstride + (int64_t)t * d + c * 32);
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint4 v = src[k];
+            w[4 * k + 0] = v.x;
+            w[4 * k + 1] = v.y;
+            w[4 * k + 2] = v.z;
+            w[4 * k + 3] = v.w;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        amax = fmaxf(amax, 1e-4f);
+        // power-of-two ceiling of amax / 448 from its IEEE fields (positive, normal)
+        const uint32_t rb = __float_as_uint(__fdiv_rn(amax, 448.0f));
+        const uint32_t se = (rb >> 23) + ((rb & 0x7fffffu) ? 1u : 0u);   // biased exponent of scale
+        const float scale = __uint_as_float(se << 23);
+        const float inv_scale = __uint_as_float((254u - se) << 23);     // exact reciprocal
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float y0 = fminf(fmaxf(bf16_lo(w[i]) * inv_scale, -448.0f), 448.0f);
+            const float y1 = fminf(fmaxf(bf16_hi(w[i]) * inv_scale, -448.0f), 448.0f);
+            const uint32_t h2 = f16x2_from_e4m3x2(e4m3x2_from_f32(y1, y0));
+            const float q0 = f16_bits_to_f32(h2 & 0xffffu) * scale;
+            const float q1 = f16_bits_to_f32(h2 >> 16) * scale;
+            w[i] = f32_to_bf16_bits(q0) | (f32_to_bf16_bits(q1) << 16);
+        }
+        const uint4 o0 = make_uint4(w[0], w[1], w[2], w[3]), o1 = make_uint4(w[4], w[5], w[6], w[7]);
+        const uint4 o2 = make_uint4(w[8], w[9], w[10], w[11]), o3 = make_uint4(w[12], w[13], w[14], w[15]);
+        src[0] = o0;
+        src[1] = o1;
+        src[2] = o2;
+        src[3] = o3;
+        if (ring != nullptr && t >= s - window) {
+            const int64_t slot = (start_pos + t) % window;
+            uint4 *dst = reinterpret_cast<uint4 *>(ring + bi * ring_bstride + slot * d + c * 32);
+            dst[0] = o0;
+            dst[1] = o1;
+            dst[2] = o2;
+            dst[3] = o3;
+        }
+    }
+}
+
+}  // namespace
+
+int launch_kv_quant_ring(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b, int s,
+                         int d, int64_t start_pos, int window, cudaStream_t stream) {
+    const int64_t total = (int64_t)b * s * (d / 32);
+    if (total == 0) return DS_OK;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    kv_quant_ring_kernel<<<(unsigned)blocks, 256, 0, stream>>>(kv, kv_bstride, ring, ring_bstride, b, s, d,
+                                                                start_pos, window);
+    return launch_status();
+}
+
+}  // namespace dsattn

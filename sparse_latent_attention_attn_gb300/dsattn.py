@@ -1,0 +1,163 @@
+"""Python binding of libdsattn (include/dsattn.h): argument marshalling only.
+
+Every function here takes torch tensors that already live on the current CUDA device, checks
+dtypes and shapes, and passes raw pointers, sizes and the current stream to the C ABI of the
+same name.  All computation happens in the library's CUDA kernels; there is no fallback of any
+kind: importing this module fails when ``libdsattn.so`` is missing.
+
+Sources, by page title and section: "DeepSeek V4.1", attention/attend (get_window_topk_idxs,
+sparse_attn_kernel, sparse_attn wrapper); attention/query-latent (Attention.__init__ ring buffer,
+Attention.forward concatenation); "Module attn" (act_quant_inplace, pow2_ceil, FP8_BLOCK,
+sparse_attn, window_topk_idxs, the ring-cache and Precision paragraphs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsattn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_latent_attention_attn_gb300.build`"
+                      " (or __graft_entry__.build())")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+DS_OK = 0
+DS_EINVAL = -1
+DS_EUNSUPPORTED = -2
+DS_EWORKSPACE = -3
+DS_ECUDA = -4
+DS_EDEVICE = -5
+DS_DEV_TIMEOUT = 1
+DS_DEV_BAD_INDEX = 2
+
+_P = ctypes.c_void_p
+_i32, _i64, _f32, _sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+_lib.ds_window_topk_idxs.argtypes = [_P, _i64, _i32, _i32, _i64, _i32, ctypes.POINTER(_i32), _P]
+_lib.ds_window_topk_idxs.restype = _i32
+_lib.ds_kv_quant_ring_write.argtypes = [_P, _i64, _P, _i64, _i32, _i32, _i32, _i64, _i32, _P]
+_lib.ds_kv_quant_ring_write.restype = _i32
+_lib.ds_sparse_attn_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
+_lib.ds_sparse_attn_workspace_bytes.restype = _sz
+_lib.ds_sparse_attn.argtypes = [_P, _P, _i64, _P, _P, _i32, _f32, _P, _i32, _i32, _i32, _i32, _P, _sz, _P]
+_lib.ds_sparse_attn.restype = _i32
+_lib.ds_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint)]
+_lib.ds_device_status.restype = _i32
+_lib.ds_status_string.argtypes = [_i32]
+_lib.ds_status_string.restype = ctypes.c_char_p
+
+
+class DsError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {_lib.ds_status_string(status).decode()} ({status})")
+        self.status = status
+
+
+def _check(fn: str, status: int) -> None:
+    if status != DS_OK:
+        raise DsError(fn, status)
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, dtype, name: str) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+
+
+def window_topk_idxs(idx: torch.Tensor, b: int, s: int, start_pos: int, window: int, stream=None) -> int:
+    """Write window index rows into ``idx`` (int32, last dim = row stride ``ld``); returns cols.
+
+    ``idx`` is viewed as rows of length ``idx.shape[-1]``: row (bi, q) is ``idx.view(-1, ld)[bi*rows+q]``.
+    """
+    _need(idx, torch.int32, "idx")
+    ld = idx.shape[-1]
+    if idx.stride(-1) != 1 or not idx.is_contiguous():
+        raise ValueError("idx must be contiguous")
+    cols = _i32(0)
+    _check("ds_window_topk_idxs",
+           _lib.ds_window_topk_idxs(_ptr(idx), ld, b, s, start_pos, window, ctypes.byref(cols), _stream(stream)))
+    return cols.value
+
+
+def kv_quant_ring_write(kv: torch.Tensor, ring: torch.Tensor | None, start_pos: int, window: int,
+                        stream=None) -> None:
+    """fp8 round trip of ``kv`` [b][s][d] (bf16, rows contiguous) in place, then the ring store.
+
+    ``ring`` is a bf16 view [b][>=window][d] whose rows are contiguous (it may be the leading
+    ``window`` rows of a larger per-sequence kv tensor).
+    """
+    _need(kv, torch.bfloat16, "kv")
+    b, s, d = kv.shape
+    if kv.stride(2) != 1 or kv.stride(1) != d:
+        raise ValueError("kv rows must be contiguous")
+    ring_bstride = 0
+    if ring is not None:
+        _need(ring, torch.bfloat16, "ring")
+        if ring.shape[0] != b or ring.shape[2] != d or ring.shape[1] < window or ring.stride(2) != 1 \
+                or ring.stride(1) != d:
+            raise ValueError("ring must be [b][>=window][d] with contiguous rows")
+        ring_bstride = ring.stride(0)
+    _check("ds_kv_quant_ring_write",
+           _lib.ds_kv_quant_ring_write(_ptr(kv), kv.stride(0), _ptr(ring), ring_bstride, b, s, d, start_pos, window,
+                                       _stream(stream)))
+
+
+def sparse_attn_workspace_bytes(b: int, m: int, h: int, d: int, topk: int) -> int:
+    return int(_lib.ds_sparse_attn_workspace_bytes(b, m, h, d, topk))
+
+
+def sparse_attn(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor, idx: torch.Tensor, scale: float,
+                o: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """o[b][m][h][d] = sparse_attn(q[b][m][h][d], kv[b][n][d], sink[h], idx[b][m][topk], scale)."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv, torch.bfloat16, "kv")
+    _need(sink, torch.float32, "sink")
+    _need(idx, torch.int32, "idx")
+    b, m, h, d = q.shape
+    n = kv.shape[1]
+    topk = idx.shape[2]
+    if kv.shape != (b, n, d) or idx.shape[:2] != (b, m) or sink.shape != (h,):
+        raise ValueError("shape mismatch")
+    for t, name in ((q, "q"), (kv, "kv"), (idx, "idx"), (sink, "sink")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if o is None:
+        o = torch.empty_like(q)
+    elif o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous bf16 tensor shaped like q")
+    need = sparse_attn_workspace_bytes(b, m, h, d, topk)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("ds_sparse_attn",
+           _lib.ds_sparse_attn(_ptr(q), _ptr(kv), n, _ptr(sink), _ptr(idx), topk, float(scale), _ptr(o), b, m, h, d,
+                               _ptr(workspace), ws_bytes, _stream(stream)))
+    return o
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status bits (0 = clean)."""
+    bits = ctypes.c_uint(0)
+    st = _lib.ds_device_status(_stream(stream), ctypes.byref(bits))
+    if st not in (DS_OK, DS_EDEVICE):
+        raise DsError("ds_device_status", st)
+    return bits.value
+
+
+def status_string(status: int) -> str:
+    return _lib.ds_status_string(status).decode()

@@ -1,0 +1,320 @@
+"""GPU-vs-oracle parity through the C ABI.
+
+Index rows and the fp8 round trip / ring contents must match the oracle bit for bit; attention
+outputs must satisfy |gpu - oracle| <= 1e-2 + 1.6e-2 * |oracle| elementwise ("Module attn",
+Precision paragraph: f32 arithmetic, bf16 result, compared at bf16 tolerance, window indices
+exactly).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from pathcheck import GpuStep, OracleStep, assert_close_bf16, bits
+from sparse_latent_attention_attn_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ds():
+    from sparse_latent_attention_attn_gb300 import dsattn
+    dsattn.device_status()      # clear anything left over
+    return dsattn
+
+
+def _bf16_from_bits(b: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+
+
+# ----------------------------------------------------------------------------------------------
+# window_topk_idxs
+# ----------------------------------------------------------------------------------------------
+
+WINDOW_CASES = [(s, 0, W) for s, W in [(1, 8), (5, 8), (12, 8), (37, 16), (300, 128), (4096, 128), (7, 1)]] + \
+               [(1, p, W) for p, W in [(1, 8), (3, 8), (7, 8), (8, 8), (12, 8), (13, 8), (127, 128), (128, 128),
+                                        (10000, 128), (16384, 128), (131072, 128), (5, 1), (9, 3)]]
+
+
+@pytest.mark.parametrize("s,start_pos,W", WINDOW_CASES)
+def test_window_idx_exact(ds, s, start_pos, W):
+    b, pad = 3, 5
+    rows = s if start_pos == 0 else 1
+    ref = oracle.window_topk_idxs(s, start_pos, W)
+    cols = ref.shape[1]
+    idx = torch.full((b, rows, cols + pad), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    got_cols = ds.window_topk_idxs(idx, b, s, start_pos, W)
+    assert got_cols == cols
+    got = idx.cpu().numpy()
+    for bi in range(b):
+        assert np.array_equal(got[bi, :, :cols], ref)
+    assert (got[:, :, cols:] == 0x5A5A5A5A).all()          # columns past cols untouched
+
+
+def test_window_idx_rejects_chunked_prefill(ds):
+    idx = torch.zeros((1, 4, 8), dtype=torch.int32, device="cuda")
+    with pytest.raises(ds.DsError) as e:
+        ds.window_topk_idxs(idx, 1, 4, 5, 8)
+    assert e.value.status == ds.DS_EUNSUPPORTED
+
+
+# ----------------------------------------------------------------------------------------------
+# fp8 round trip and ring
+# ----------------------------------------------------------------------------------------------
+
+def _all_finite_bf16_patterns() -> np.ndarray:
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    exp = (pats >> 7) & 0xFF
+    return np.where(exp == 0xFF, np.uint16(0), pats)
+
+
+@pytest.mark.parametrize("d", [512, 64])
+def test_quant_exhaustive_bit_exact(ds, d):
+    pats = _all_finite_bf16_patterns()
+    rng = np.random.default_rng(d)
+    for order in ("sorted", "shuffled"):
+        x = pats.copy() if order == "sorted" else rng.permutation(pats)
+        kv = _bf16_from_bits(x).view(1, -1, d).cuda()
+        ds.kv_quant_ring_write(kv, None, 0, 1)
+        want = oracle.act_quant_inplace(x.copy())
+        assert np.array_equal(bits(kv).reshape(-1), want), order
+
+
+@pytest.mark.parametrize("anchor_exp", [-20, -9, -6, 0, 7, 40])
+def test_quant_every_value_at_fixed_scale(ds, anchor_exp):
+    anchor = 448.0 * 2.0 ** anchor_exp
+    pats = _all_finite_bf16_patterns()
+    vals = _bf16_from_bits(pats).to(torch.float64)
+    vals = vals[vals.abs() <= anchor].to(torch.bfloat16)
+    nb = (vals.numel() + 30) // 31
+    nb += (-nb) % 16                                  # whole rows of d = 512
+    flat = torch.zeros(nb * 31, dtype=torch.bfloat16)
+    flat[: vals.numel()] = vals
+    blocks = torch.empty((nb, 32), dtype=torch.bfloat16)
+    blocks[:, :31] = flat.view(nb, 31)
+    blocks[:, 31] = anchor
+    x = bits(blocks).reshape(-1)
+    kv = blocks.view(1, -1, 512).cuda()
+    ds.kv_quant_ring_write(kv, None, 0, 1)
+    assert np.array_equal(bits(kv).reshape(-1), oracle.act_quant_inplace(x.copy()))
+
+
+@pytest.mark.parametrize("b,s,d,W,p0", [(1, 12, 64, 8, 0), (3, 20, 64, 8, 37), (2, 5, 512, 8, 0),
+                                        (4, 1, 512, 128, 10000), (2, 300, 512, 128, 0), (1, 7, 256, 16, 3)])
+def test_ring_write_bit_exact(ds, b, s, d, W, p0):
+    g = torch.Generator().manual_seed(b * 1000 + s)
+    raw = (torch.randn((b, s, d), generator=g) * torch.exp(torch.randn((b, s, 1), generator=g) * 3)).to(
+        torch.bfloat16)
+    extra = 9                                         # the ring sits inside a wider kv tensor
+    canary = 0x7F7F
+    big = torch.full((b, W + extra, d), canary, dtype=torch.int16).view(torch.bfloat16).cuda()
+    kv = raw.cuda()
+    ds.kv_quant_ring_write(kv, big[:, :W], p0, W)
+    want_kv = bits(raw).copy()
+    want_ring = np.full((b, W, d), canary, dtype=np.uint16)
+    oracle.kv_quant_ring_write(want_kv, want_ring, p0, W)
+    assert np.array_equal(bits(kv), want_kv)
+    got_big = bits(big)
+    assert np.array_equal(got_big[:, :W], want_ring)
+    assert (got_big[:, W:] == canary).all()
+
+
+def test_ring_worked_example_gpu(ds):
+    # "Module attn", ring-cache paragraph: rows valued t+1 are on the fp8 grid and name their token
+    W, d = 8, 64
+    ring = torch.zeros((1, W, d), dtype=torch.bfloat16, device="cuda")
+    chunk = torch.tensor([[float(t + 1)] * d for t in range(12)]).to(torch.bfloat16).view(1, 12, d).cuda()
+    ds.kv_quant_ring_write(chunk, ring, 0, W)
+    assert (ring[0, :, 0].float().cpu().numpy().astype(int) - 1).tolist() == [8, 9, 10, 11, 4, 5, 6, 7]
+    for step, ring_after in ((12, [8, 9, 10, 11, 12, 5, 6, 7]), (13, [8, 9, 10, 11, 12, 13, 6, 7])):
+        new = torch.full((1, 1, d), float(step + 1)).to(torch.bfloat16).cuda()
+        ds.kv_quant_ring_write(new, ring, step, W)
+        assert (ring[0, :, 0].float().cpu().numpy().astype(int) - 1).tolist() == ring_after
+
+
+# ----------------------------------------------------------------------------------------------
+# the ratio-0 fixture: prefill 12 tokens, then decode 12 and 13 through one cache
+# ----------------------------------------------------------------------------------------------
+
+def test_fixture_sequence(ds):
+    fx = wl.fixture_inputs(device="cuda")
+    w = fx["w"]
+    W, d, h = w.window, w.d, w.h
+    sink = fx["sink"]
+    # --- GPU ---------------------------------------------------------------------------------
+    from sparse_latent_attention_attn_gb300 import path
+    ring = torch.zeros((w.b, W, d), dtype=torch.bfloat16, device="cuda")
+    kv = fx["prefill_kv"].clone()
+    idx = torch.empty((w.b, w.s, min(w.s, W)), dtype=torch.int32, device="cuda")
+    o_pre = path.prefill_step(fx["prefill_q"], kv, ring, sink, idx, W, w.scale)
+    # --- oracle --------------------------------------------------------------------------------
+    ring_o = np.zeros((w.b, W, d), dtype=np.uint16)
+    chunk_o = bits(fx["prefill_kv"])
+    oracle.kv_quant_ring_write(chunk_o, ring_o, 0, W)
+    win = oracle.window_topk_idxs(w.s, 0, W)
+    idx_o = np.ascontiguousarray(win[None])
+    o_pre_o = oracle.sparse_attn(bits(fx["prefill_q"]), chunk_o, sink.cpu().numpy(), idx_o, w.scale)
+    assert np.array_equal(idx.cpu().numpy(), idx_o)
+    assert np.array_equal(bits(kv), chunk_o)
+    assert np.array_equal(bits(ring), ring_o)
+    assert_close_bf16(bits(o_pre), o_pre_o, "prefill o")
+    for step in fx["decode"]:
+        p = step["start_pos"]
+        new = step["new_kv"].clone()
+        idx_d = torch.empty((w.b, 1, W), dtype=torch.int32, device="cuda")
+        o_d = path.decode_step(step["q"], ring, new, sink, idx_d, p, W, w.scale)
+        oracle.kv_quant_ring_write(bits(step["new_kv"]), ring_o, p, W)
+        win_d = oracle.window_topk_idxs(1, p, W)
+        o_d_o = oracle.sparse_attn(bits(step["q"]), ring_o, sink.cpu().numpy(), np.ascontiguousarray(win_d[None]),
+                                   w.scale)
+        assert np.array_equal(idx_d.cpu().numpy()[0], win_d)
+        assert np.array_equal(bits(ring), ring_o), f"ring after decode {p}"
+        assert_close_bf16(bits(o_d), o_d_o, f"decode {p} o")
+    assert ds.device_status() == 0
+
+
+# ----------------------------------------------------------------------------------------------
+# the four model-scale workloads, at full size, sampled where the oracle would be slow
+# ----------------------------------------------------------------------------------------------
+
+SAMPLE_SEQS = {1: [0, 17, 63], 2: [0], 3: [0, 5, 31], 4: [0, 101, 255]}
+SAMPLE_TOKENS_PREFILL = [0, 1, 2, 3, 7, 127, 128, 129, 511, 1000, 2047, 2048, 2049, 3333, 4094, 4095]
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_workload_parity(ds, cfg):
+    w = wl.WORKLOADS[cfg]
+    gs = GpuStep(w)
+    gs.run()
+    torch.cuda.synchronize()
+    orc = OracleStep(gs, seqs=SAMPLE_SEQS[cfg])
+    sel = torch.tensor(orc.seqs, device="cuda")
+    # index rows and ring: exact
+    assert np.array_equal(gs.idx.index_select(0, sel).cpu().numpy(), orc.idx)
+    ring_gpu = bits(gs.ring.index_select(0, sel))
+    assert np.array_equal(ring_gpu, orc.ring)
+    if not w.decode:
+        assert np.array_equal(bits(gs.kv.index_select(0, sel)[:, : w.s]), orc.chunk)
+    # attention: tolerance, on sampled tokens
+    if w.decode:
+        got = bits(gs.o.index_select(0, sel)).reshape(len(orc.seqs), w.h, w.d)
+        ref = orc.attend()
+        assert_close_bf16(got, ref.reshape(len(orc.seqs), w.h, w.d), f"cfg{cfg} o")
+    else:
+        toks = np.array(SAMPLE_TOKENS_PREFILL, dtype=np.int64)
+        got = bits(gs.o[0, torch.from_numpy(toks).cuda()])
+        ref = orc.attend(tokens=toks)
+        assert_close_bf16(got, ref, f"cfg{cfg} o")
+    # every output is finite, and the step is repeatable bit for bit
+    assert torch.isfinite(gs.o.float()).all()
+    first = gs.o.clone()
+    gs.reset()
+    gs.run()
+    assert torch.equal(first, gs.o)
+    assert ds.device_status() == 0
+
+
+# ----------------------------------------------------------------------------------------------
+# sparse_attn edge cases on small shapes (every output element checked)
+# ----------------------------------------------------------------------------------------------
+
+def _case(seed, b, m, h, d, n, topk, neg=0.1, dup=False, sink_val=None, tail_pad=0):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((b, m, h, d), generator=g).to(torch.bfloat16)
+    kv = torch.randn((b, n, d), generator=g).to(torch.bfloat16)
+    sink = torch.randn((h,), generator=g) if sink_val is None else torch.full((h,), float(sink_val))
+    if dup or topk > n:
+        idx = torch.randint(0, n, (b, m, topk), generator=g)
+    else:
+        idx = torch.stack([torch.randperm(n, generator=g)[:topk] for _ in range(b * m)]).view(b, m, topk) \
+            if topk else torch.zeros((b, m, 0), dtype=torch.long)
+    idx = torch.where(torch.rand((b, m, topk), generator=g) < neg, -1, idx).to(torch.int32)
+    if tail_pad:
+        idx[..., -tail_pad:] = -1
+    return q, kv, sink, idx
+
+
+def _check_case(ds, q, kv, sink, idx, scale):
+    o = ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
+    ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), idx.numpy(), scale)
+    assert_close_bf16(bits(o), ref)
+    return o, ref
+
+
+EDGE = [
+    # seed, b, m, h, d, n, topk, neg, dup
+    (1, 2, 3, 4, 64, 40, 24, 0.1, False),
+    (2, 1, 5, 1, 64, 10, 8, 0.0, False),
+    (3, 3, 2, 16, 128, 300, 200, 0.2, False),
+    (4, 2, 2, 64, 512, 700, 640, 0.05, False),
+    (5, 1, 3, 128, 512, 2000, 1000, 0.02, False),
+    (6, 2, 2, 100, 256, 500, 65, 0.0, False),
+    (7, 2, 2, 128, 512, 300, 63, 0.0, False),
+    (8, 2, 2, 128, 512, 300, 64, 0.0, False),
+    (9, 2, 2, 33, 512, 300, 129, 0.3, False),
+    (10, 2, 2, 8, 64, 20, 50, 0.1, True),        # duplicates count as listed
+    (11, 1, 1, 128, 512, 100, 1, 0.0, False),
+    (12, 1, 4, 64, 512, 5000, 2176, 0.02, False),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[f"e{c[0]}" for c in EDGE])
+def test_attn_edge_shapes(ds, case):
+    seed, b, m, h, d, n, topk, neg, dup = case
+    q, kv, sink, idx = _case(seed, b, m, h, d, n, topk, neg, dup)
+    _check_case(ds, q, kv, sink, idx, d ** -0.5)
+    assert ds.device_status() == 0
+
+
+def test_attn_all_invalid_rows_give_zero(ds):
+    q, kv, sink, idx = _case(20, 2, 3, 64, 512, 300, 130)
+    idx[1, 2] = -1
+    idx[0, 0] = -1
+    o, _ = _check_case(ds, q, kv, sink, idx, 512 ** -0.5)
+    assert (o[1, 2].float() == 0).all() and (o[0, 0].float() == 0).all()
+
+
+def test_attn_empty_topk(ds):
+    q, kv, sink, idx = _case(21, 2, 2, 16, 64, 10, 0)
+    o, _ = _check_case(ds, q, kv, sink, idx, 0.125)
+    assert (o.float() == 0).all()
+
+
+@pytest.mark.parametrize("sink_val", [-1e30, -30.0, 30.0, 1e30])
+def test_attn_extreme_sinks(ds, sink_val):
+    q, kv, sink, idx = _case(22, 2, 2, 32, 512, 400, 256, sink_val=sink_val)
+    _check_case(ds, q, kv, sink, idx, 512 ** -0.5)
+
+
+def test_attn_tail_padding_and_permutation(ds):
+    q, kv, sink, idx = _case(23, 2, 2, 64, 512, 1000, 300, neg=0.0, tail_pad=37)
+    o1, _ = _check_case(ds, q, kv, sink, idx, 512 ** -0.5)
+    perm = torch.randperm(idx.shape[-1], generator=torch.Generator().manual_seed(1))
+    o2, _ = _check_case(ds, q, kv, sink, idx[..., perm].contiguous(), 512 ** -0.5)
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
+
+
+def test_attn_out_of_range_index_is_skipped_and_flagged(ds):
+    q, kv, sink, idx = _case(24, 1, 2, 16, 64, 50, 20, neg=0.0)
+    bad = idx.clone()
+    bad[0, 1, 3] = 50          # == n: out of range
+    o = ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), bad.cuda(), 0.125)
+    assert ds.device_status() & ds.DS_DEV_BAD_INDEX
+    skipped = bad.clone()
+    skipped[0, 1, 3] = -1
+    ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), skipped.numpy(), 0.125)
+    assert_close_bf16(bits(o), ref)
+    assert ds.device_status() == 0
+
+
+def test_attn_argument_errors(ds):
+    q, kv, sink, idx = _case(25, 1, 1, 4, 64, 10, 8)
+    q, kv, sink, idx = q.cuda(), kv.cuda(), sink.cuda(), idx.cuda()
+    with pytest.raises(ds.DsError) as e:
+        ds.sparse_attn(q.view(1, 1, 4, 64)[..., :48].contiguous().view(1, 1, 4, 48),
+                       kv[..., :48].contiguous(), sink, idx, 0.1)
+    assert e.value.status == ds.DS_EUNSUPPORTED
+    big_h = torch.zeros((1, 1, 129, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ds.DsError) as e:
+        ds.sparse_attn(big_h, kv, torch.zeros(129, device="cuda"), idx, 0.1)
+    assert e.value.status == ds.DS_EUNSUPPORTED
