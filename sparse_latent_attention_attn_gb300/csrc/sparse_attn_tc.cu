@@ -1,0 +1,809 @@
+// sparse_attn_tc.cu -- sparse_attn on the 5th-generation tensor cores (tcgen05 + TMEM + TMA gather).
+//
+// What it computes ("Module attn", sparse_attn and the Precision paragraph; "DeepSeek V4.1",
+// attention/attend, sparse_attn_kernel): for every query token and head, softmax over the
+// index-listed rows of one shared latent KV tensor plus an attention sink that counts in the
+// denominator only, the same rows reused as values, f32 arithmetic, bf16 output.
+//
+// How (GB300-first design; the pages' kernel is prior art only):
+//  * Every head of a token shares the same gathered rows, so Q[h x d] K^T and P V are dense bf16
+//    contractions with M = heads (padded to 128 = TMEM lanes).  S and O accumulate in TMEM.
+//  * Rows are gathered once per (token, tile of 64 valid rows) by TMA tile::gather4 straight into
+//    128-byte-swizzled shared memory and used by all heads, as the keys (K-major B operand of
+//    Q K^T) and as the values (MN-major B operand of P V).  -1 entries are compacted away first,
+//    so they cost neither bytes nor MMA work.
+//  * Q and P live in TMEM and are the A operands, so shared memory bandwidth is spent on the
+//    gathered rows only.
+//  * head_dim 512: O[128 x 512] f32 alone would fill TMEM, so a 2-CTA cluster splits the d columns:
+//    each CTA gathers and multiplies its own 256 columns, the two partial score tiles are summed
+//    through distributed shared memory, and both CTAs run the identical softmax.
+//  * Warp roles: warps 0-3 softmax and epilogue (thread = head = TMEM lane), warp 4 index
+//    compaction + TMA producer, warp 5 TMEM allocation + single-thread MMA issue.
+//  * Persistent clusters take contiguous ranges of the flattened (token, index entry) space, so
+//    the load is balanced whatever the batch; a token cut by a range boundary leaves f32 partials
+//    (running max, sum, unnormalised O) in the workspace and a combine kernel merges them with the
+//    sink.  Whole tokens are normalised with the sink in the epilogue and written as bf16.
+//  * Online softmax in the log2 domain with a lazy rescale: the running max is only moved (and O
+//    rescaled) when a tile's max exceeds it by more than 2^8, which keeps the rescale off the hot
+//    path while every exponent stays <= 2^8.
+//  * Every wait is bounded: past a time limit the kernel flags DS_DEV_TIMEOUT, drains its own
+//    copies and MMAs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dsattn {
+namespace tc {
+
+using namespace ptx;
+
+constexpr int BN = 64;            // gathered rows per tile: N of Q K^T, K of P V
+constexpr int NSTAGE = 4;         // tiles in flight
+constexpr int LMAX = 4096;        // largest index row handled (entries of one token)
+constexpr int NTHREADS = 192;     // warps 0-3 softmax, warp 4 producer, warp 5 MMA
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
+
+constexpr int SLOT_HEADS = 128;   // partial slots are laid out for 128 heads
+
+template <int D>
+struct Cfg {
+    static constexpr int CL = D == 512 ? 2 : 1;     // CTAs per cluster (d split)
+    static constexpr int DH = D / CL;               // columns per CTA
+    static constexpr int NCHUNK = DH / 64;          // 128-byte column chunks per row
+    static constexpr int CHUNK_BYTES = BN * 128;
+    static constexpr int TILE_BYTES = BN * DH * 2;
+    // TMEM columns (32-bit): O accumulator, two S buffers (P aliases the first BN/2 columns), Q
+    static constexpr int O_COL = 0;
+    static constexpr int S_COL = DH;
+    static constexpr int Q_COL = DH + 2 * BN;
+    static constexpr int TMEM_COLS = (Q_COL + DH / 2) <= 256 ? 256 : 512;
+    // shared memory, offsets from a 1024-aligned base
+    static constexpr int SM_KV = 0;
+    static constexpr int SM_X = SM_KV + NSTAGE * TILE_BYTES;
+    static constexpr int X_BYTES = CL == 2 ? 2 * 128 * BN * 4 : 0;
+    static constexpr int SM_LIST = SM_X + X_BYTES;
+    static constexpr int SM_BAR = SM_LIST + LMAX * 4;
+    static constexpr int SM_END = SM_BAR + 256;
+    static constexpr int SMEM_BYTES = SM_END + 1024;
+    static_assert(Q_COL + DH / 2 <= 512, "TMEM budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// barrier slots (8 bytes each) inside the SM_BAR block
+enum : int {
+    B_FULL = 0,                 // [NSTAGE] producer -> consumers: tile landed
+    B_EMPTY = B_FULL + NSTAGE,  // [NSTAGE] consumers -> producer: stage free
+    B_SFULL = B_EMPTY + NSTAGE, // [2] MMA -> softmax: S ready
+    B_PFULL = B_SFULL + 2,      // [2] softmax -> MMA: P written
+    B_PVDONE = B_PFULL + 2,     // [2] MMA -> softmax: P V done
+    B_QREADY = B_PVDONE + 2,    // softmax -> MMA: Q of the segment in TMEM
+    B_OFREE = B_QREADY + 1,     // softmax -> MMA: epilogue has read O
+    B_XFULL = B_OFREE + 1,      // [2] peer -> me: peer's partial scores are in my exchange buffer
+    B_XFREE = B_XFULL + 2,      // [2] peer -> me: peer has read what I sent
+    B_DRAIN = B_XFREE + 2,      // MMA drain on abort
+    B_ZREAD = B_DRAIN + 1,      // softmax threads have read the meta of a tile without rows
+    B_COUNT = B_ZREAD + 1
+};
+constexpr int META_OFF = 8 * B_COUNT;      // [NSTAGE] int2 {count, last}
+constexpr int TMEM_ADDR_OFF = META_OFF + 8 * NSTAGE;
+constexpr int ABORT_OFF = TMEM_ADDR_OFF + 4;
+static_assert(ABORT_OFF + 4 <= 256, "barrier block");
+
+struct Params {
+    const uint16_t *q;
+    const float *sink;
+    const int32_t *idx;
+    uint16_t *o;
+    float *ws;
+    int64_t n;
+    int64_t E;        // b * m * topk entries
+    int topk;
+    int m;
+    int h;
+    int G;            // clusters
+    float scale_log2; // softmax scale * log2(e)
+    unsigned int *status;
+};
+
+// Start of cluster c's range of the flattened entry space.
+__host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t E, int64_t G) {
+    return (int64_t)(((__int128)c * E) / G);
+}
+
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// Every lane waits; the warp proceeds only if all lanes saw the phase (a timeout in any lane
+// aborts the whole warp, so warp-collective tcgen05 instructions never diverge).
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    const bool ok = mbar_wait<kCluster>(bar, parity, abort, kWaitLimitNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
+                                                                     const Params p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+    uint8_t *sbase = smem_raw + (base - raw_u32);
+    const uint32_t bars = base + C::SM_BAR;
+    auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+    int2 *meta = reinterpret_cast<int2 *>(sbase + C::SM_BAR + META_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + ABORT_OFF);
+    int32_t *list = reinterpret_cast<int32_t *>(sbase + C::SM_LIST);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = C::CL == 2 ? cluster_ctarank() : 0u;
+    const uint32_t peer = crank ^ 1u;
+    const int64_t cid = blockIdx.x / C::CL;
+    const int64_t e0 = range_start(cid, p.E, p.G), e1 = range_start(cid + 1, p.E, p.G);
+    const int T = p.topk;
+
+    // ---- set-up --------------------------------------------------------------------------------
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(BAR(B_FULL + s), 1);
+            mbar_init(BAR(B_EMPTY + s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(BAR(B_SFULL + i), 1);
+            mbar_init(BAR(B_PFULL + i), 128);
+            mbar_init(BAR(B_PVDONE + i), 1);
+            mbar_init(BAR(B_XFULL + i), 128);
+            mbar_init(BAR(B_XFREE + i), 128);
+        }
+        mbar_init(BAR(B_QREADY), 128);
+        mbar_init(BAR(B_OFREE), 128);
+        mbar_init(BAR(B_DRAIN), 1);
+        mbar_init(BAR(B_ZREAD), 128);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // rows a tile does not load keep finite values: zero every stage once
+    for (int i = threadIdx.x; i < NSTAGE * C::TILE_BYTES / 16; i += NTHREADS)
+        reinterpret_cast<uint4 *>(sbase + C::SM_KV)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 5) {
+        tmem_alloc(base + C::SM_BAR + TMEM_ADDR_OFF, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if constexpr (C::CL == 2) cluster_sync();
+    else __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sbase + C::SM_BAR + TMEM_ADDR_OFF);
+
+    const int64_t tok_begin = e0 / (T > 0 ? T : 1);
+    const bool has_work = e1 > e0 && T > 0;
+
+    if (warp == 4) {
+        // ============================ producer: compaction + TMA gather ============================
+        if (lane == 0) prefetch_tensormap(&kv_map);
+        int it = 0;
+        bool ok = true;
+        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
+            const int a = (int)((e0 > tok * T ? e0 : tok * T) - tok * T);
+            const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
+            const int32_t *irow = p.idx + tok * T;
+            // stage the entries [a, z) into shared memory with one round trip, then compact in place
+            for (int j = a + lane; j < z; j += 32) cp_async_4(smem_u32(list + (j - a)), irow + j);
+            cp_async_wait_all();
+            __syncwarp();
+            {   // warm L2 with the next token's index row
+                const int64_t nt = tok + 1;
+                if (nt * T < e1)
+                    for (int j = lane * 32; j < T; j += 32 * 32) prefetch_l2(p.idx + nt * T + j);
+            }
+            int nvalid = 0;
+            bool bad = false;
+            for (int j0 = 0; j0 < z - a; j0 += 32) {
+                const int j = j0 + lane;
+                const int v = j < z - a ? list[j] : -1;
+                const bool valid = v >= 0 && (int64_t)v < p.n;
+                bad |= (int64_t)v >= p.n;
+                const uint32_t bal = __ballot_sync(0xffffffffu, valid);
+                __syncwarp();
+                if (valid) list[nvalid + __popc(bal & lanemask_lt())] = v;
+                nvalid += __popc(bal);
+                __syncwarp();
+            }
+            if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DS_DEV_BAD_INDEX);
+            const int ntiles = nvalid > 0 ? (nvalid + BN - 1) / BN : 1;
+            const int64_t rowbase = (tok / p.m) * p.n;
+            for (int t = 0; t < ntiles; ++t, ++it) {
+                const int stage = it % NSTAGE;
+                if (!warp_wait(BAR(B_EMPTY + stage), ((it / NSTAGE) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int cnt = nvalid - t * BN < BN ? nvalid - t * BN : BN;
+                if (lane == 0) {
+                    meta[stage] = make_int2(cnt, t == ntiles - 1 ? 1 : 0);
+                    if (cnt > 0) {
+                        const int rows4 = (cnt + 3) & ~3;
+                        mbar_arrive_expect_tx(BAR(B_FULL + stage), (uint32_t)(rows4 * C::DH * 2));
+                        const int first = t * BN, lastv = t * BN + cnt - 1;
+                        const uint32_t dst0 = base + C::SM_KV + stage * C::TILE_BYTES;
+                        for (int g = 0; g < rows4; g += 4) {
+                            int r[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int k = first + g + u;
+                                r[u] = (int)(rowbase + list[k <= lastv ? k : lastv]);
+                            }
+#pragma unroll
+                            for (int c = 0; c < C::NCHUNK; ++c)
+                                tma_gather4(dst0 + c * C::CHUNK_BYTES + g * 128, &kv_map,
+                                            (int)crank * C::DH + c * 64, r[0], r[1], r[2], r[3], BAR(B_FULL + stage));
+                        }
+                    } else {
+                        mbar_arrive(BAR(B_FULL + stage));
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        // on abort: let every copy already issued land before the CTA can exit
+        if (*abort_flag && lane == 0) {
+            for (int k = 1; k <= NSTAGE && it - k >= 0; ++k) {
+                const int i2 = it - k;
+                mbar_wait_drain(BAR(B_FULL + i2 % NSTAGE), (i2 / NSTAGE) & 1, 100000000ull);
+            }
+        }
+    } else if (warp == 5) {
+        // ================================= MMA issue (lane 0) =================================
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false);
+            constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, C::DH, true);
+            int it = 0, J = 0, seg = 0;
+            bool ok = true;
+            bool pend = false, pend_first = false;
+            int pend_stage = 0, pend_J = 0, pend_seg = 0;
+            // O += P V for the pending tile (P from TMEM, V = the same gathered rows)
+            auto issue_pv = [&]() -> bool {
+                const int sb = pend_J & 1;
+                if (!mbar_wait(BAR(B_PFULL + sb), (pend_J >> 1) & 1, abort_flag, kWaitLimitNs)) return false;
+                if (pend_first && pend_seg > 0 &&
+                    !mbar_wait(BAR(B_OFREE), (pend_seg - 1) & 1, abort_flag, kWaitLimitNs))
+                    return false;
+                tc_fence_after();
+                const uint32_t vbase = base + C::SM_KV + pend_stage * C::TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    // V rows 16k..16k+15 as the MN-major B operand (d contiguous): 8-row groups
+                    // 1024 B apart, 64-column chunks CHUNK_BYTES apart
+                    const uint64_t bdesc = smem_desc_sw128(vbase + k * 2048, C::CHUNK_BYTES, 1024);
+                    mma_bf16_ts(tmem + C::O_COL, tmem + C::S_COL + sb * BN + k * 8, bdesc, IDESC_PV,
+                                (pend_first && k == 0) ? 0u : 1u);
+                }
+                mma_commit(BAR(B_EMPTY + pend_stage));
+                mma_commit(BAR(B_PVDONE + sb));
+                pend = false;
+                return true;
+            };
+            for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok, ++seg) {
+                bool first = true;
+                for (;;) {
+                    const int stage = it % NSTAGE;
+                    if (!mbar_wait(BAR(B_FULL + stage), (it / NSTAGE) & 1, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const int2 mt = meta[stage];
+                    if (first && !mbar_wait(BAR(B_QREADY), seg & 1, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (mt.x > 0) {
+                        // S = Q K^T: K rows as the K-major B operand; 16 columns = 32 bytes inside
+                        // the 128-byte swizzle atom of chunk k/4; 8-row groups 1024 B apart
+                        const int sb = J & 1;
+                        const uint32_t kbase = base + C::SM_KV + stage * C::TILE_BYTES;
+#pragma unroll
+                        for (int k = 0; k < C::DH / 16; ++k) {
+                            const uint64_t bdesc =
+                                smem_desc_sw128(kbase + (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32, 16, 1024);
+                            mma_bf16_ts(tmem + C::S_COL + sb * BN, tmem + C::Q_COL + k * 8, bdesc, IDESC_S,
+                                        k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(BAR(B_SFULL + sb));
+                    }
+                    if (pend && !issue_pv()) {
+                        ok = false;
+                        break;
+                    }
+                    if (mt.x > 0) {
+                        pend = true;
+                        pend_first = first;
+                        pend_stage = stage;
+                        pend_J = J;
+                        pend_seg = seg;
+                        ++J;
+                    }
+                    ++it;
+                    first = false;
+                    if (mt.y) break;
+                }
+            }
+            if (ok && pend) ok = issue_pv();
+            if (*abort_flag) {   // let issued MMAs finish before TMEM is freed
+                mma_commit(BAR(B_DRAIN));
+                mbar_wait_drain(BAR(B_DRAIN), 0, 100000000ull);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ============================ softmax + epilogue (warps 0-3) ============================
+        const int t = threadIdx.x;                       // head row = TMEM lane
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const bool live = t < p.h;
+        const float sink2 = live ? p.sink[t] * kLog2e : 0.0f;
+        uint32_t xpeer = 0, xfull_peer = 0, xfree_peer = 0;
+        if constexpr (C::CL == 2) {
+            xpeer = mapa(base + C::SM_X, peer);
+            xfull_peer = mapa(BAR(B_XFULL), peer);
+            xfree_peer = mapa(BAR(B_XFREE), peer);
+        }
+        auto load_q = [&](int64_t tok) {
+            // this CTA's DH columns of q[tok][t] into TMEM columns [Q_COL, Q_COL + DH/2) of lane t
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (tok * p.h + t) * (int64_t)D + crank * C::DH);
+#pragma unroll 1
+            for (int c = 0; c < C::DH / 64; ++c) {
+                uint32_t r[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 v = live ? __ldg(src + c * 8 + k) : make_uint4(0, 0, 0, 0);
+                    r[4 * k] = v.x;
+                    r[4 * k + 1] = v.y;
+                    r[4 * k + 2] = v.z;
+                    r[4 * k + 3] = v.w;
+                }
+                tmem_st32(tmem + lane_off + C::Q_COL + c * 32, r);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(BAR(B_QREADY));
+        };
+        int it = 0, J = 0, nzero = 0;
+        bool ok = true;
+        if (has_work) load_q(tok_begin);
+        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
+            const int a = (int)((e0 > tok * T ? e0 : tok * T) - tok * T);
+            const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
+            float m_used = -INFINITY, l = 0.0f;
+            bool any = false;
+            for (;;) {
+                const int stage = it % NSTAGE;
+                if (!warp_wait(BAR(B_FULL + stage), (it / NSTAGE) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int2 mt = meta[stage];
+                const int cnt = mt.x;
+                if (cnt > 0) {
+                    const int sb = J & 1;
+                    const uint32_t ph = (J >> 1) & 1;
+                    if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tmem + lane_off + C::S_COL + sb * BN, r0);
+                    tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + 32, r1);
+                    tmem_ld_wait(r0);
+                    tmem_ld_wait(r1);
+                    float s[BN];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        s[j] = __uint_as_float(r0[j]);
+                        s[32 + j] = __uint_as_float(r1[j]);
+                    }
+                    if constexpr (C::CL == 2) {
+                        // partial scores of the two column halves: send mine, add the peer's
+                        const uint32_t xbuf = base + C::SM_X + sb * (128 * BN * 4);
+                        if (!warp_wait<true>(BAR(B_XFREE + sb), ph ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t rbuf = xpeer + sb * (128 * BN * 4);
+#pragma unroll
+                        for (int k = 0; k < BN / 4; ++k)
+                            st_cluster_v4(rbuf + (k * 128 + t) * 16, s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
+                        mbar_arrive_cluster(xfull_peer + 8u * sb);
+                        if (!warp_wait<true>(BAR(B_XFULL + sb), ph, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+#pragma unroll
+                        for (int k = 0; k < BN / 4; ++k) {
+                            const float4 v = ld_shared_v4(xbuf + (k * 128 + t) * 16);
+                            s[4 * k] += v.x;
+                            s[4 * k + 1] += v.y;
+                            s[4 * k + 2] += v.z;
+                            s[4 * k + 3] += v.w;
+                        }
+                        mbar_arrive_cluster(xfree_peer + 8u * sb);
+                    }
+                    float tmax = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < BN; ++j) {
+                        s[j] = j < cnt ? s[j] * p.scale_log2 : -INFINITY;
+                        tmax = fmaxf(tmax, s[j]);
+                    }
+                    if (!any) {
+                        m_used = tmax;
+                    } else if (__any_sync(0xffffffffu, tmax > m_used + kRescaleThreshold)) {
+                        // move the running max: wait for the P V in flight, rescale O and l
+                        const int Jp = J - 1;
+                        if (!warp_wait(BAR(B_PVDONE + (Jp & 1)), (Jp >> 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const float m_new = fmaxf(m_used, tmax);
+                        const float f = exp2f(m_used - m_new);
+                        l *= f;
+#pragma unroll 1
+                        for (int c = 0; c < C::DH / 32; ++c) {
+                            uint32_t r[32];
+                            tmem_ld32(tmem + lane_off + C::O_COL + c * 32, r);
+                            tmem_ld_wait(r);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+                            tmem_st32(tmem + lane_off + C::O_COL + c * 32, r);
+                        }
+                        tmem_st_wait();
+                        m_used = m_new;
+                    }
+                    any = true;
+                    uint32_t pk[32];
+                    float lsum = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float p0 = bf16_round(exp2f(s[2 * j] - m_used));
+                        const float p1 = bf16_round(exp2f(s[2 * j + 1] - m_used));
+                        lsum += p0 + p1;
+                        pk[j] = pack_bf16x2(p0, p1);
+                    }
+                    l += lsum;
+                    tmem_st32(tmem + lane_off + C::S_COL + sb * BN, pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(BAR(B_PFULL + sb));
+                    ++J;
+                } else {
+                    // a segment without a single valid row: its only tile loads nothing; once all
+                    // 128 threads have read its meta, thread 0 hands the stage back
+                    mbar_arrive(BAR(B_ZREAD));
+                    if (t == 0) {
+                        if (!mbar_wait(BAR(B_ZREAD), nzero & 1, abort_flag, kWaitLimitNs)) ok = false;
+                        else mbar_arrive(BAR(B_EMPTY + stage));
+                    }
+                    ++nzero;
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
+                ++it;
+                if (mt.y) break;
+            }
+            if (!ok) break;
+            // every S of this segment has been read, so the next token's Q may replace this one
+            if ((tok + 1) * T < e1) load_q(tok + 1);
+            if (any) {
+                const int Jl = J - 1;
+                if (!warp_wait(BAR(B_PVDONE + (Jl & 1)), (Jl >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            const bool whole = a == 0 && z == T;
+            if (whole) {
+                const float top = fmaxf(m_used, sink2);
+                const float w = any ? exp2f(m_used - top) : 0.0f;
+                const float inv = w / (l * w + exp2f(sink2 - top));
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + (tok * p.h + t) * (int64_t)D + crank * C::DH);
+#pragma unroll 1
+                for (int c = 0; c < C::DH / 32; ++c) {
+                    uint32_t r[32];
+                    if (any) {
+                        tmem_ld32(tmem + lane_off + C::O_COL + c * 32, r);
+                        tmem_ld_wait(r);
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float x0 = any ? __uint_as_float(r[8 * k + 2 * i]) * inv : 0.0f;
+                                const float x1 = any ? __uint_as_float(r[8 * k + 2 * i + 1]) * inv : 0.0f;
+                                w4[i] = pack_bf16x2(x0, x1);
+                            }
+                            dst[c * 4 + k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                }
+            } else {
+                // partial: unnormalised O, running max and sum (log2 domain) for the combine kernel
+                const int slot = tok == tok_begin ? 0 : 1;
+                float *ws = p.ws + ((size_t)cid * 2 + slot) * (size_t)(SLOT_HEADS * D + 2 * SLOT_HEADS);
+                if (live && crank == 0) {
+                    ws[SLOT_HEADS * D + t] = any ? m_used : -INFINITY;
+                    ws[SLOT_HEADS * D + SLOT_HEADS + t] = l;
+                }
+                float4 *dst = reinterpret_cast<float4 *>(ws + (size_t)t * D + crank * C::DH);
+#pragma unroll 1
+                for (int c = 0; c < C::DH / 32; ++c) {
+                    uint32_t r[32];
+                    if (any) {
+                        tmem_ld32(tmem + lane_off + C::O_COL + c * 32, r);
+                        tmem_ld_wait(r);
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            dst[c * 8 + k] = any ? make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                                               __uint_as_float(r[4 * k + 2]),
+                                                               __uint_as_float(r[4 * k + 3]))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(BAR(B_OFREE));
+        }
+    }
+
+    // ---- teardown --------------------------------------------------------------------------------
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, DS_DEV_TIMEOUT);
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    if constexpr (C::CL == 2) cluster_sync();
+}
+
+// Merge the partials of every token that a range boundary cut, add the sink once, write bf16.
+// Block c (1 <= c < G) owns the token holding boundary e(c) when that boundary falls inside a
+// token and no earlier boundary falls inside the same token.
+template <int D>
+__global__ void __launch_bounds__(256) sparse_attn_combine_kernel(const Params p) {
+    const int c = blockIdx.x + 1;
+    const int64_t T = p.topk;
+    const int64_t eb = range_start(c, p.E, p.G);
+    if (eb % T == 0 || eb >= p.E) return;
+    const int64_t tok = eb / T;
+    const int64_t ts = tok * T, te = ts + T;
+    // the earlier boundary inside this token (if any) owns it
+    const int64_t ep = range_start(c - 1, p.E, p.G);
+    if (c > 1 && ep > ts && ep % T != 0) return;
+    // clusters whose ranges meet the token: first = the one containing ts
+    int64_t cf = c - 1;
+    while (cf > 0 && range_start(cf, p.E, p.G) > ts) --cf;
+    constexpr size_t SLOT = (size_t)SLOT_HEADS * D + 2 * SLOT_HEADS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int hh = warp; hh < p.h; hh += 8) {
+        const float sink2 = p.sink[hh] * kLog2e;
+        float top = sink2;
+        for (int64_t k = cf; k < p.G; ++k) {
+            const int64_t r0 = range_start(k, p.E, p.G), r1 = range_start(k + 1, p.E, p.G);
+            if (r0 >= te) break;
+            if (r1 <= r0 || r1 <= ts) continue;
+            const int slot = (r0 / T == tok) ? 0 : 1;
+            const float *ws = p.ws + ((size_t)k * 2 + slot) * SLOT;
+            top = fmaxf(top, ws[SLOT_HEADS * D + hh]);
+        }
+        float den = exp2f(sink2 - top);
+        float acc[D / 32];
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) acc[i] = 0.0f;
+        for (int64_t k = cf; k < p.G; ++k) {
+            const int64_t r0 = range_start(k, p.E, p.G), r1 = range_start(k + 1, p.E, p.G);
+            if (r0 >= te) break;
+            if (r1 <= r0 || r1 <= ts) continue;
+            const int slot = (r0 / T == tok) ? 0 : 1;
+            const float *ws = p.ws + ((size_t)k * 2 + slot) * SLOT;
+            const float mk = ws[SLOT_HEADS * D + hh];
+            if (mk == -INFINITY) continue;
+            const float w = exp2f(mk - top);
+            den += w * ws[SLOT_HEADS * D + SLOT_HEADS + hh];
+            const float *orow = ws + (size_t)hh * D;
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) acc[i] += w * orow[i * 32 + lane];
+        }
+        const float inv = 1.0f / den;
+        uint16_t *dst = p.o + (tok * p.h + hh) * (int64_t)D;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) dst[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i] * inv));
+    }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int max_clusters[4] = {0, 0, 0, 0};   // per head_dim variant, co-resident clusters
+    bool ready[4] = {false, false, false, false};
+};
+constexpr int kMaxDev = 64;
+DeviceInfo g_dev[kMaxDev];
+std::mutex g_dev_mutex;
+
+template <int D>
+constexpr int dvar() { return D == 64 ? 0 : D == 128 ? 1 : D == 256 ? 2 : 3; }
+
+template <int D>
+int max_clusters(int dev) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &di = g_dev[dev];
+    if (di.ready[dvar<D>()]) return di.max_clusters[dvar<D>()];
+    using C = Cfg<D>;
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaFuncSetAttribute(sparse_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    int nclusters = di.sms;
+    if (C::CL > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(C::CL * di.sms, 1, 1);
+        cfg.blockDim = dim3(NTHREADS, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C::CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, sparse_attn_tc_kernel<D>, &cfg) != cudaSuccess ||
+            nclusters < 1)
+            return 0;
+    }
+    di.max_clusters[dvar<D>()] = nclusters;
+    di.ready[dvar<D>()] = true;
+    return nclusters;
+}
+
+// Cluster count for a problem: stream-K over all clusters when there are at least as many
+// tokens as clusters; otherwise each token gets the same number of clusters (split evenly),
+// but no split shorter than two tiles.
+int64_t choose_clusters(int64_t ntok, int topk, int gmax) {
+    if (ntok >= gmax) return gmax;
+    int64_t k = gmax / ntok;
+    const int64_t kmax = topk / (2 * BN) > 1 ? topk / (2 * BN) : 1;
+    if (k > kmax) k = kmax;
+    if (k < 1) k = 1;
+    return ntok * k;
+}
+
+bool splits_tokens(int64_t ntok, int topk, int64_t G) {
+    if (G <= 1 || topk == 0) return false;
+    const int64_t E = ntok * topk;
+    for (int64_t c = 1; c < G; ++c)
+        if (range_start(c, E, G) % topk != 0) return true;
+    return false;
+}
+
+template <int D>
+size_t workspace_bytes_for(int64_t ntok, int topk) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    const int gmax = max_clusters<D>(dev);
+    if (gmax <= 0 || ntok == 0 || topk == 0) return 0;
+    const int64_t G = choose_clusters(ntok, topk, gmax);
+    if (!splits_tokens(ntok, topk, G)) return 0;
+    return (size_t)G * 2 * ((size_t)SLOT_HEADS * D + 2 * SLOT_HEADS) * sizeof(float);
+}
+
+template <int D>
+int launch(const AttnArgs &a, cudaStream_t stream) {
+    using C = Cfg<D>;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return DS_ECUDA;
+    const int gmax = max_clusters<D>(dev);
+    if (gmax <= 0) return DS_ECUDA;
+    const int64_t ntok = (int64_t)a.b * a.m;
+    const int64_t G = choose_clusters(ntok, a.topk, gmax);
+    const bool split = splits_tokens(ntok, a.topk, G);
+    const size_t need = split ? (size_t)G * 2 * ((size_t)SLOT_HEADS * D + 2 * SLOT_HEADS) * sizeof(float) : 0;
+    if (a.workspace_bytes < need || (need && !a.workspace)) return DS_EWORKSPACE;
+
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return DS_ECUDA;
+    alignas(64) CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)a.b * (cuuint64_t)a.n};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.kv), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return DS_ECUDA;
+
+    Params p;
+    p.q = a.q;
+    p.sink = a.sink;
+    p.idx = a.idx;
+    p.o = a.o;
+    p.ws = static_cast<float *>(a.workspace);
+    p.n = a.n;
+    p.E = ntok * a.topk;
+    p.topk = a.topk;
+    p.m = a.m;
+    p.h = a.h;
+    p.G = (int)G;
+    p.scale_log2 = a.scale * kLog2e;
+    p.status = a.status;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(C::CL * G), 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C::CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D>, map, p) != cudaSuccess) return DS_ECUDA;
+    if (split) {
+        sparse_attn_combine_kernel<D><<<(unsigned)(G - 1), 256, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return DS_ECUDA;
+    }
+    return DS_OK;
+}
+
+}  // namespace tc
+
+size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk) {
+    (void)h;
+    const int64_t ntok = (int64_t)b * m;
+    switch (d) {
+        case 64: return tc::workspace_bytes_for<64>(ntok, topk);
+        case 128: return tc::workspace_bytes_for<128>(ntok, topk);
+        case 256: return tc::workspace_bytes_for<256>(ntok, topk);
+        case 512: return tc::workspace_bytes_for<512>(ntok, topk);
+        default: return 0;
+    }
+}
+
+int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream) {
+    switch (a.d) {
+        case 64: return tc::launch<64>(a, stream);
+        case 128: return tc::launch<128>(a, stream);
+        case 256: return tc::launch<256>(a, stream);
+        case 512: return tc::launch<512>(a, stream);
+        default: return DS_EUNSUPPORTED;
+    }
+}
+
+}  // namespace dsattn
