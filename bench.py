@@ -14,6 +14,7 @@ same workload; under torchrun only rank 0 runs it.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -323,6 +324,8 @@ def run_ours(args):
     dist_init(world, "nccl")
     from sparse_latent_attention_attn_gb300 import dsattn
     w = wl.WORKLOADS[args.config]
+    if args.batch:   # smaller batch of the same workload (profiling captures)
+        w = dataclasses.replace(w, b=args.batch, name=f"{w.name}[b={args.batch}]")
     peaks = load_peaks()
 
     # enough independent input sets that the gathered rows of consecutive steps miss in L2
@@ -433,6 +436,7 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate through (0 = automatic)")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -28,8 +28,6 @@
 //    path while every exponent stays <= 2^8.
 //  * Every wait is bounded: past a time limit the kernel flags DS_DEV_TIMEOUT, drains its own
 //    copies and MMAs, frees TMEM and returns.
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "common.cuh"
@@ -41,9 +39,18 @@ namespace tc {
 using namespace ptx;
 
 constexpr int BN = 64;            // gathered rows per tile: N of Q K^T, K of P V
-constexpr int NSTAGE = 4;         // tiles in flight
+constexpr int NSTAGE = 4;         // tiles in flight in shared memory
+constexpr int PREFETCH = 4;       // tiles further ahead whose rows are pulled into L2
 constexpr int LMAX = 4096;        // largest index row handled (entries of one token)
-constexpr int NTHREADS = 192;     // warps 0-3 softmax, warp 4 producer, warp 5 MMA
+// warp roles (16 warps = 4 warpgroups)
+constexpr int NTHREADS = 512;
+constexpr int W_PROD0 = 4;        // warps 4-11: row gather (cp.async), 256 threads
+constexpr int NPROD_WARPS = 8;
+constexpr int NPROD = NPROD_WARPS * 32;
+constexpr int W_LIST = 12;        // index compaction
+constexpr int W_MMA = 13;         // TMEM allocation + MMA issue (warps 14-15 idle)
+// register split: softmax warpgroup 232, the other three 88 (128 * (232 + 3 * 88) = 63488 <= 65536)
+constexpr uint32_t REG_SOFTMAX = 232, REG_OTHER = 88;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
@@ -87,15 +94,19 @@ enum : int {
     B_XFREE = B_XFULL + 2,      // [2] peer -> me: peer has read what I sent
     B_DRAIN = B_XFREE + 2,      // MMA drain on abort
     B_ZREAD = B_DRAIN + 1,      // softmax threads have read the meta of a tile without rows
-    B_COUNT = B_ZREAD + 1
+    B_LFULL = B_ZREAD + 1,      // compaction -> producers: the segment's index list is ready
+    B_LFREE = B_LFULL + 1,      // producers -> compaction: the list may be overwritten
+    B_COUNT = B_LFREE + 1
 };
 constexpr int META_OFF = 8 * B_COUNT;      // [NSTAGE] int2 {count, last}
 constexpr int TMEM_ADDR_OFF = META_OFF + 8 * NSTAGE;
 constexpr int ABORT_OFF = TMEM_ADDR_OFF + 4;
+constexpr int NVALID_OFF = ABORT_OFF + 4;
 static_assert(ABORT_OFF + 4 <= 256, "barrier block");
 
 struct Params {
     const uint16_t *q;
+    const uint16_t *kv;
     const float *sink;
     const int32_t *idx;
     uint16_t *o;
@@ -117,17 +128,19 @@ __host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t E, in
 
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-// Every lane waits; the warp proceeds only if all lanes saw the phase (a timeout in any lane
-// aborts the whole warp, so warp-collective tcgen05 instructions never diverge).
-template <bool kCluster = false>
+// Lane 0 polls the barrier for the whole warp (one poller per warp keeps the barrier hardware
+// free for the arrivals), then the other lanes acquire the completed phase themselves; the warp
+// proceeds together or not at all, so warp-collective tcgen05 instructions never diverge.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
-    const bool ok = mbar_wait<kCluster>(bar, parity, abort, kWaitLimitNs);
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, kWaitLimitNs);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) ok = mbar_try_wait(bar, parity);   // completed: returns at once, with acquire semantics
     return __all_sync(0xffffffffu, ok);
 }
 
 template <int D>
-__global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
-                                                                     const Params p) {
+__global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Params p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -149,20 +162,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
     // ---- set-up --------------------------------------------------------------------------------
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(BAR(B_FULL + s), 1);
+            mbar_init(BAR(B_FULL + s), NPROD + 1);   // every gather thread's copies + the meta writer
             mbar_init(BAR(B_EMPTY + s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(B_SFULL + i), 1);
             mbar_init(BAR(B_PFULL + i), 128);
             mbar_init(BAR(B_PVDONE + i), 1);
-            mbar_init(BAR(B_XFULL + i), 128);
-            mbar_init(BAR(B_XFREE + i), 128);
+            mbar_init(BAR(B_XFULL + i), 4);     // one arrival per softmax warp of the peer
+            mbar_init(BAR(B_XFREE + i), 4);     // one arrival per softmax warp of the peer
         }
         mbar_init(BAR(B_QREADY), 128);
         mbar_init(BAR(B_OFREE), 128);
         mbar_init(BAR(B_DRAIN), 1);
         mbar_init(BAR(B_ZREAD), 128);
+        mbar_init(BAR(B_LFULL), 32);
+        mbar_init(BAR(B_LFREE), NPROD_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -170,7 +185,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
     for (int i = threadIdx.x; i < NSTAGE * C::TILE_BYTES / 16; i += NTHREADS)
         reinterpret_cast<uint4 *>(sbase + C::SM_KV)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
-    if (warp == 5) {
+    if (warp == W_MMA) {
         tmem_alloc(base + C::SM_BAR + TMEM_ADDR_OFF, C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -178,18 +193,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sbase + C::SM_BAR + TMEM_ADDR_OFF);
+    volatile int *seg_nvalid = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + NVALID_OFF);
+    // warpgroup 3 (compaction, MMA, two idle warps) gives registers back before it branches
+    if (warp >= 12) setmaxnreg_dec<REG_OTHER>();
 
     const int64_t tok_begin = e0 / (T > 0 ? T : 1);
     const bool has_work = e1 > e0 && T > 0;
 
-    if (warp == 4) {
-        // ============================ producer: compaction + TMA gather ============================
-        if (lane == 0) prefetch_tensormap(&kv_map);
-        int it = 0;
-        bool ok = true;
-        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
+    if (warp == W_LIST) {
+        // ======================== index compaction: one list per segment ========================
+        int seg = 0;
+        for (int64_t tok = tok_begin; has_work && tok * T < e1; ++tok, ++seg) {
             const int a = (int)((e0 > tok * T ? e0 : tok * T) - tok * T);
             const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
+            if (!warp_wait(BAR(B_LFREE), (seg & 1) ^ 1, abort_flag)) break;
             const int32_t *irow = p.idx + tok * T;
             // stage the entries [a, z) into shared memory with one round trip, then compact in place
             for (int j = a + lane; j < z; j += 32) cp_async_4(smem_u32(list + (j - a)), irow + j);
@@ -214,49 +231,66 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
                 __syncwarp();
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DS_DEV_BAD_INDEX);
+            if (lane == 0) *seg_nvalid = nvalid;
+            mbar_arrive(BAR(B_LFULL));          // every lane releases its own list stores
+        }
+    } else if (warp >= W_PROD0 && warp < W_PROD0 + NPROD_WARPS) {
+        // ================== row gather: cp.async into the 128-byte-swizzled ring ==================
+        // A row half of DH columns is U = DH / 8 units of 16 bytes; each warp instruction copies
+        // 32 / U whole rows, so every global access is a contiguous row piece.
+        setmaxnreg_dec<REG_OTHER>();
+        constexpr int U = C::DH / 8;
+        constexpr int RPW = 32 / U;                      // rows per warp instruction
+        const int pw = warp - W_PROD0;                   // producer warp 0..7
+        const int rsub = lane / U, unit = lane % U;
+        const int chunk = unit / 8, u8 = unit % 8;
+        const bool writer = pw == 0 && lane == 0;
+        int it = 0, seg = 0;
+        bool ok = true;
+        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok, ++seg) {
+            if (!warp_wait(BAR(B_LFULL), seg & 1, abort_flag)) break;
+            const int nvalid = *seg_nvalid;
             const int ntiles = nvalid > 0 ? (nvalid + BN - 1) / BN : 1;
-            const int64_t rowbase = (tok / p.m) * p.n;
+            const uint16_t *kvb = p.kv + ((tok / p.m) * p.n) * (int64_t)D + crank * C::DH + unit * 8;
+            // L2 prefetch: producer thread i pulls 128-byte line i % (DH/64) of row i / (DH/64) of a
+            // tile PREFETCH tiles ahead, so the shared-memory copies below mostly hit L2
+            constexpr int LINES = C::DH / 64;                   // 128-byte lines per row half
+            const int pf_row = (threadIdx.x - W_PROD0 * 32) / LINES, pf_line = (threadIdx.x - W_PROD0 * 32) % LINES;
+            const uint16_t *kvl = p.kv + ((tok / p.m) * p.n) * (int64_t)D + crank * C::DH + pf_line * 64;
+            auto prefetch_tile = [&](int tt) {
+                for (int r = pf_row; r < BN; r += NPROD / LINES) {
+                    const int k = tt * BN + r;
+                    if (k < nvalid) prefetch_l2(kvl + (int64_t)list[k] * D);
+                }
+            };
+            for (int tt = 0; tt < PREFETCH && tt < ntiles; ++tt) prefetch_tile(tt);
             for (int t = 0; t < ntiles; ++t, ++it) {
+                if (t + PREFETCH < ntiles) prefetch_tile(t + PREFETCH);
                 const int stage = it % NSTAGE;
                 if (!warp_wait(BAR(B_EMPTY + stage), ((it / NSTAGE) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 const int cnt = nvalid - t * BN < BN ? nvalid - t * BN : BN;
-                if (lane == 0) {
-                    meta[stage] = make_int2(cnt, t == ntiles - 1 ? 1 : 0);
-                    if (cnt > 0) {
-                        const int rows4 = (cnt + 3) & ~3;
-                        mbar_arrive_expect_tx(BAR(B_FULL + stage), (uint32_t)(rows4 * C::DH * 2));
-                        const int first = t * BN, lastv = t * BN + cnt - 1;
-                        const uint32_t dst0 = base + C::SM_KV + stage * C::TILE_BYTES;
-                        for (int g = 0; g < rows4; g += 4) {
-                            int r[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int k = first + g + u;
-                                r[u] = (int)(rowbase + list[k <= lastv ? k : lastv]);
-                            }
-#pragma unroll
-                            for (int c = 0; c < C::NCHUNK; ++c)
-                                tma_gather4(dst0 + c * C::CHUNK_BYTES + g * 128, &kv_map,
-                                            (int)crank * C::DH + c * 64, r[0], r[1], r[2], r[3], BAR(B_FULL + stage));
-                        }
-                    } else {
-                        mbar_arrive(BAR(B_FULL + stage));
-                    }
+                const uint32_t dst0 = base + C::SM_KV + stage * C::TILE_BYTES + chunk * C::CHUNK_BYTES;
+#pragma unroll 4
+                for (int r = pw * RPW + rsub; r < cnt; r += NPROD_WARPS * RPW) {
+                    // row r, 16-byte unit u8 of its 128-byte chunk: swizzled to unit u8 ^ (r % 8)
+                    const int v = list[t * BN + r];
+                    cp_async_16(dst0 + r * 128 + ((u8 ^ (r & 7)) << 4), kvb + (int64_t)v * D);
                 }
-                __syncwarp();
+                cp_async_arrive_noinc(BAR(B_FULL + stage));
+                if (writer) {
+                    meta[stage] = make_int2(cnt, t == ntiles - 1 ? 1 : 0);
+                    mbar_arrive(BAR(B_FULL + stage));
+                }
             }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_LFREE));   // this warp is done with the list
         }
-        // on abort: let every copy already issued land before the CTA can exit
-        if (*abort_flag && lane == 0) {
-            for (int k = 1; k <= NSTAGE && it - k >= 0; ++k) {
-                const int i2 = it - k;
-                mbar_wait_drain(BAR(B_FULL + i2 % NSTAGE), (i2 / NSTAGE) & 1, 100000000ull);
-            }
-        }
-    } else if (warp == 5) {
+        cp_async_wait_all();                              // nothing may land after the CTA exits
+    } else if (warp == W_MMA) {
         // ================================= MMA issue (lane 0) =================================
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false);
@@ -300,6 +334,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
                         ok = false;
                         break;
                     }
+                    // the rows were written by cp.async (generic proxy); the MMA reads them through
+                    // the async proxy
+                    fence_proxy_async_smem();
                     tc_fence_after();
                     if (mt.x > 0) {
                         // S = Q K^T: K rows as the K-major B operand; 16 columns = 32 bytes inside
@@ -339,12 +376,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < 4) {
         // ============================ softmax + epilogue (warps 0-3) ============================
+        setmaxnreg_inc<REG_SOFTMAX>();
         const int t = threadIdx.x;                       // head row = TMEM lane
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const bool live = t < p.h;
         const float sink2 = live ? p.sink[t] * kLog2e : 0.0f;
+        constexpr uint32_t XSTRIDE = 128 * BN * 4;       // one exchange buffer
         uint32_t xpeer = 0, xfull_peer = 0, xfree_peer = 0;
         if constexpr (C::CL == 2) {
             xpeer = mapa(base + C::SM_X, peer);
@@ -371,6 +410,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
             tc_fence_before();
             mbar_arrive(BAR(B_QREADY));
         };
+        // Stage A of tile Jx: its scores are in TMEM; with a column split, send this CTA's partial
+        // scores to the peer right away (asynchronous stores counted on the peer's barrier).
+        auto stage_a = [&](int Jx) -> bool {
+            const int sb = Jx & 1;
+            const uint32_t ph = (Jx >> 1) & 1;
+            if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) return false;
+            tc_fence_after();
+            if constexpr (C::CL == 2) {
+                if (!warp_wait(BAR(B_XFREE + sb), ph ^ 1, abort_flag)) return false;
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem + lane_off + C::S_COL + sb * BN, r0);
+                tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + 32, r1);
+                tmem_ld_wait(r0);
+                tmem_ld_wait(r1);
+                // plain stores into the peer's exchange buffer, then one release-arrive per warp
+                const uint32_t rbuf = xpeer + sb * XSTRIDE;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_cluster_v4(rbuf + (k * 128 + t) * 16, __uint_as_float(r0[4 * k]), __uint_as_float(r0[4 * k + 1]),
+                                  __uint_as_float(r0[4 * k + 2]), __uint_as_float(r0[4 * k + 3]));
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_cluster_v4(rbuf + ((8 + k) * 128 + t) * 16, __uint_as_float(r1[4 * k]),
+                                  __uint_as_float(r1[4 * k + 1]), __uint_as_float(r1[4 * k + 2]),
+                                  __uint_as_float(r1[4 * k + 3]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(xfull_peer + 8u * sb);
+            }
+            return true;
+        };
         int it = 0, J = 0, nzero = 0;
         bool ok = true;
         if (has_work) load_q(tok_begin);
@@ -379,22 +448,52 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
             const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
             float m_used = -INFINITY, l = 0.0f;
             bool any = false;
-            for (;;) {
-                const int stage = it % NSTAGE;
-                if (!warp_wait(BAR(B_FULL + stage), (it / NSTAGE) & 1, abort_flag)) {
+            if (!warp_wait(BAR(B_FULL + it % NSTAGE), (it / NSTAGE) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            int2 cur = meta[it % NSTAGE];
+            if (cur.x == 0) {
+                // a segment without a single valid row: its only tile loads nothing; once all
+                // 128 threads have read its meta, thread 0 hands the stage back
+                mbar_arrive(BAR(B_ZREAD));
+                if (t == 0) {
+                    if (!mbar_wait(BAR(B_ZREAD), nzero & 1, abort_flag, kWaitLimitNs)) ok = false;
+                    else mbar_arrive(BAR(B_EMPTY + it % NSTAGE));
+                }
+                ++nzero;
+                ++it;
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            } else {
+                if (!stage_a(J)) {
                     ok = false;
                     break;
                 }
-                const int2 mt = meta[stage];
-                const int cnt = mt.x;
-                if (cnt > 0) {
+                bool next_sent = false;        // stage A of tile J+1 already done
+                for (;;) {
+                    // stage A of the next tile first when its scores are already there, so its
+                    // exchange is in flight while tile J is finished; never wait for it here
+                    int2 nxt = make_int2(0, 1);
+                    if (!cur.y) {
+                        const int in = it + 1;
+                        bool ready = false;
+                        if (lane == 0)
+                            ready = mbar_try_wait(BAR(B_FULL + in % NSTAGE), (in / NSTAGE) & 1) &&
+                                    mbar_try_wait(BAR(B_SFULL + ((J + 1) & 1)), ((J + 1) >> 1) & 1);
+                        ready = __shfl_sync(0xffffffffu, ready, 0);
+                        if (ready) {
+                            nxt = meta[in % NSTAGE];
+                            if (!stage_a(J + 1)) {
+                                ok = false;
+                                break;
+                            }
+                            next_sent = true;
+                        }
+                    }
+                    // stage B of tile J: full scores -> online softmax -> P (bf16) into TMEM
                     const int sb = J & 1;
                     const uint32_t ph = (J >> 1) & 1;
-                    if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
                     uint32_t r0[32], r1[32];
                     tmem_ld32(tmem + lane_off + C::S_COL + sb * BN, r0);
                     tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + 32, r1);
@@ -407,21 +506,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
                         s[32 + j] = __uint_as_float(r1[j]);
                     }
                     if constexpr (C::CL == 2) {
-                        // partial scores of the two column halves: send mine, add the peer's
-                        const uint32_t xbuf = base + C::SM_X + sb * (128 * BN * 4);
-                        if (!warp_wait<true>(BAR(B_XFREE + sb), ph ^ 1, abort_flag)) {
+                        if (!warp_wait(BAR(B_XFULL + sb), ph, abort_flag)) {
                             ok = false;
                             break;
                         }
-                        const uint32_t rbuf = xpeer + sb * (128 * BN * 4);
-#pragma unroll
-                        for (int k = 0; k < BN / 4; ++k)
-                            st_cluster_v4(rbuf + (k * 128 + t) * 16, s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
-                        mbar_arrive_cluster(xfull_peer + 8u * sb);
-                        if (!warp_wait<true>(BAR(B_XFULL + sb), ph, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
+                        const uint32_t xbuf = base + C::SM_X + sb * XSTRIDE;
 #pragma unroll
                         for (int k = 0; k < BN / 4; ++k) {
                             const float4 v = ld_shared_v4(xbuf + (k * 128 + t) * 16);
@@ -430,14 +519,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
                             s[4 * k + 2] += v.z;
                             s[4 * k + 3] += v.w;
                         }
-                        mbar_arrive_cluster(xfree_peer + 8u * sb);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(xfree_peer + 8u * sb);
                     }
-                    float tmax = -INFINITY;
+                    const int cnt = cur.x;
+                    if (cnt < BN) {
 #pragma unroll
-                    for (int j = 0; j < BN; ++j) {
-                        s[j] = j < cnt ? s[j] * p.scale_log2 : -INFINITY;
-                        tmax = fmaxf(tmax, s[j]);
+                        for (int j = 0; j < BN; ++j)
+                            if (j >= cnt) s[j] = -INFINITY;
                     }
+                    // row max of the raw scores (the scale is positive), as a tree
+                    float mx[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+                    for (int j = 16; j < BN; j += 8)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[j + i]);
+                    const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
                     if (!any) {
                         m_used = tmax;
                     } else if (__any_sync(0xffffffffu, tmax > m_used + kRescaleThreshold)) {
@@ -449,7 +549,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
                         }
                         tc_fence_after();
                         const float m_new = fmaxf(m_used, tmax);
-                        const float f = exp2f(m_used - m_new);
+                        const float f = ex2(m_used - m_new);
                         l *= f;
 #pragma unroll 1
                         for (int c = 0; c < C::DH / 32; ++c) {
@@ -464,37 +564,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
                         m_used = m_new;
                     }
                     any = true;
+                    // p = 2^(s * scale_log2 - m); P goes to the MMA in bf16, the row sum stays f32
                     uint32_t pk[32];
-                    float lsum = 0.0f;
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                    const float neg_m = -m_used;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float p0 = bf16_round(exp2f(s[2 * j] - m_used));
-                        const float p1 = bf16_round(exp2f(s[2 * j + 1] - m_used));
-                        lsum += p0 + p1;
+                        const float p0 = ex2(fmaf(s[2 * j], p.scale_log2, neg_m));
+                        const float p1 = ex2(fmaf(s[2 * j + 1], p.scale_log2, neg_m));
+                        ls[j & 3] += p0 + p1;
                         pk[j] = pack_bf16x2(p0, p1);
                     }
-                    l += lsum;
+                    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                     tmem_st32(tmem + lane_off + C::S_COL + sb * BN, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(BAR(B_PFULL + sb));
                     ++J;
-                } else {
-                    // a segment without a single valid row: its only tile loads nothing; once all
-                    // 128 threads have read its meta, thread 0 hands the stage back
-                    mbar_arrive(BAR(B_ZREAD));
-                    if (t == 0) {
-                        if (!mbar_wait(BAR(B_ZREAD), nzero & 1, abort_flag, kWaitLimitNs)) ok = false;
-                        else mbar_arrive(BAR(B_EMPTY + stage));
+                    ++it;
+                    if (cur.y) break;
+                    // stage A of the next tile if it was not ready before
+                    if (!next_sent) {
+                        const int in = it;
+                        if (!warp_wait(BAR(B_FULL + in % NSTAGE), (in / NSTAGE) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        nxt = meta[in % NSTAGE];
+                        if (!stage_a(J)) {
+                            ok = false;
+                            break;
+                        }
                     }
-                    ++nzero;
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
+                    next_sent = false;
+                    cur = nxt;
                 }
-                ++it;
-                if (mt.y) break;
+                if (!ok) break;
             }
-            if (!ok) break;
             // every S of this segment has been read, so the next token's Q may replace this one
             if ((tok + 1) * T < e1) load_q(tok + 1);
             if (any) {
@@ -508,8 +614,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
             const bool whole = a == 0 && z == T;
             if (whole) {
                 const float top = fmaxf(m_used, sink2);
-                const float w = any ? exp2f(m_used - top) : 0.0f;
-                const float inv = w / (l * w + exp2f(sink2 - top));
+                const float w = any ? ex2(m_used - top) : 0.0f;
+                const float inv = w / (l * w + ex2(sink2 - top));
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (tok * p.h + t) * (int64_t)D + crank * C::DH);
 #pragma unroll 1
                 for (int c = 0; c < C::DH / 32; ++c) {
@@ -567,7 +673,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const __gri
     // ---- teardown --------------------------------------------------------------------------------
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, DS_DEV_TIMEOUT);
-    if (warp == 5) {
+    if (warp == W_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
@@ -632,20 +738,6 @@ __global__ void __launch_bounds__(256) sparse_attn_combine_kernel(const Params p
 // ---------------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
 
 struct DeviceInfo {
     int sms = 0;
@@ -735,20 +827,9 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     const size_t need = split ? (size_t)G * 2 * ((size_t)SLOT_HEADS * D + 2 * SLOT_HEADS) * sizeof(float) : 0;
     if (a.workspace_bytes < need || (need && !a.workspace)) return DS_EWORKSPACE;
 
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return DS_ECUDA;
-    alignas(64) CUtensorMap map;
-    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)a.b * (cuuint64_t)a.n};
-    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {64, 1};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.kv), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return DS_ECUDA;
-
     Params p;
     p.q = a.q;
+    p.kv = a.kv;
     p.sink = a.sink;
     p.idx = a.idx;
     p.o = a.o;
@@ -773,8 +854,8 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D>, map, p) != cudaSuccess) return DS_ECUDA;
+    cfg.numAttrs = C::CL > 1 ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D>, p) != cudaSuccess) return DS_ECUDA;
     if (split) {
         sparse_attn_combine_kernel<D><<<(unsigned)(G - 1), 256, 0, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return DS_ECUDA;
