@@ -133,6 +133,31 @@ int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float
                    void *workspace, size_t workspace_bytes, ds_stream_t stream);
 
 /*
+ * ds_sparse_attn_static_scratch -- ds_sparse_attn for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists for integration.  Some callers cannot
+ * call cudaMalloc where they run attention (a runtime or memory manager that owns every device
+ * allocation, a plugin handed only its input and output buffers, a hot path where allocation is
+ * forbidden).  This call takes no workspace: the scratch that ds_sparse_attn would take from the
+ * caller lives in a fixed device array of ds_sparse_attn_static_scratch_capacity() bytes
+ * (32 MiB) compiled into the library, which every device that loads the library keeps reserved
+ * until the process exits.  Nothing is allocated by the call.
+ *
+ * Arguments, layouts, results and errors are those of ds_sparse_attn, except that a shape whose
+ * scratch need (ds_sparse_attn_workspace_bytes) exceeds the capacity is refused with
+ * DS_EWORKSPACE before anything is launched.
+ * The first call on each device looks up that device's copy of the array (cudaGetSymbolAddress)
+ * and so should happen before any stream capture on that device.  Every call on a device shares
+ * the one array, and it keeps whatever the last call left there (no call needs it cleared):
+ * calls whose work overlaps on the GPU (different streams, no ordering) race on it.
+ */
+int ds_sparse_attn_static_scratch(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink,
+                                  const int32_t *idx, int topk, float scale, uint16_t *o, int b, int m, int h,
+                                  int d, ds_stream_t stream);
+
+/* Bytes of the fixed scratch array behind ds_sparse_attn_static_scratch (pure host function). */
+size_t ds_sparse_attn_static_scratch_capacity(void);
+
+/*
  * ds_device_status -- synchronise `stream`, then read and clear the current device's status word
  * (DS_DEV_* bits set by kernels since the last read).  Returns DS_OK when the word was 0,
  * DS_EDEVICE when a bit was set (the bits are stored to *bits_out when it is not NULL), or

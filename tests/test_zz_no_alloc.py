@@ -1,0 +1,80 @@
+"""ds_sparse_attn_static_scratch: sparse_attn without a caller-provided workspace.
+
+Some callers cannot allocate device memory where they run attention (an owning runtime or memory
+manager, a plugin handed only its buffers), so this entry point keeps its scratch in a fixed
+device array inside the library.  The test calls it through the C ABI on a shape that needs
+scratch (tokens split across CTAs), twice in a row, and checks every output against
+ds_sparse_attn with an allocated workspace.  It lives in its own file, collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-2, 1.6e-2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_latent_attention_attn_gb300 import dsattn
+    L = dsattn._lib
+    P = ctypes.c_void_p
+    L.ds_sparse_attn_static_scratch.argtypes = [P, P, ctypes.c_int64, P, P, ctypes.c_int, ctypes.c_float, P,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+    L.ds_sparse_attn_static_scratch.restype = ctypes.c_int
+    L.ds_sparse_attn_static_scratch_capacity.argtypes = []
+    L.ds_sparse_attn_static_scratch_capacity.restype = ctypes.c_size_t
+    return L
+
+
+def _inputs(b, m, h, d, n, topk, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    q = torch.randn((b, m, h, d), generator=g, device="cuda").to(torch.bfloat16)
+    kv = torch.randn((b, n, d), generator=g, device="cuda").to(torch.bfloat16)
+    sink = torch.randn((h,), generator=g, device="cuda")
+    idx = torch.rand((b * m, n), generator=g, device="cuda").topk(topk, dim=-1).indices.to(torch.int32)
+    idx = idx.view(b, m, topk).contiguous()
+    idx[..., -13:] = -1
+    return q, kv, sink, idx
+
+
+def _call_static(lib, q, kv, sink, idx, scale, o):
+    b, m, h, d = q.shape
+    return lib.ds_sparse_attn_static_scratch(q.data_ptr(), kv.data_ptr(), kv.shape[1], sink.data_ptr(),
+                                             idx.data_ptr(), idx.shape[2], scale, o.data_ptr(), b, m, h, d,
+                                             torch.cuda.current_stream().cuda_stream)
+
+
+def test_static_scratch_matches_workspace_path(lib):
+    from sparse_latent_attention_attn_gb300 import dsattn
+    b, m, h, d, n, topk = 4, 1, 64, 512, 900, 700
+    scale = d ** -0.5
+    assert dsattn.sparse_attn_workspace_bytes(b, m, h, d, topk) > 0          # the shape really uses scratch
+    assert dsattn.sparse_attn_workspace_bytes(b, m, h, d, topk) <= lib.ds_sparse_attn_static_scratch_capacity()
+    for call, seed in enumerate((11, 12)):                                 # two calls in a row
+        q, kv, sink, idx = _inputs(b, m, h, d, n, topk, seed)
+        ref = dsattn.sparse_attn(q, kv, sink, idx, scale)
+        o = torch.full_like(q, float("nan"))
+        assert _call_static(lib, q, kv, sink, idx, scale, o) == 0
+        torch.cuda.synchronize()
+        got, want = o.float().cpu().numpy(), ref.float().cpu().numpy()
+        assert np.isfinite(got).all(), f"call {call}: non-finite output"
+        assert (np.abs(got - want) <= ATOL + RTOL * np.abs(want)).all(), f"call {call}: mismatch"
+    assert dsattn.device_status() == 0
+
+
+def test_static_scratch_refuses_shapes_beyond_capacity(lib):
+    from sparse_latent_attention_attn_gb300 import dsattn
+    b, m, h, d, n, topk = 128, 1, 8, 512, 300, 256
+    need = dsattn.sparse_attn_workspace_bytes(b, m, h, d, topk)
+    if need <= lib.ds_sparse_attn_static_scratch_capacity():
+        pytest.skip("on this device the shape fits the static scratch")
+    q, kv, sink, idx = _inputs(b, m, h, d, n, topk, 13)
+    o = torch.zeros_like(q)
+    assert _call_static(lib, q, kv, sink, idx, d ** -0.5, o) == dsattn.DS_EWORKSPACE
+    torch.cuda.synchronize()
+    assert (o.float() == 0).all()                                          # nothing was launched
