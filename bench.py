@@ -38,7 +38,9 @@ UNIT = "(token·head·row)/s"
 DEFAULT_CONFIG = 4
 L2_BYTES = 129 * 1024 * 1024
 SLEEP_CYCLES = 40_000_000      # ~20 ms of device time: long enough for the host to enqueue a run
-ATTN_KERNEL_SOURCES = ["sparse_latent_attention_attn_gb300/csrc/sparse_attn_simt.cu"]
+ATTN_KERNEL_SOURCES = ["sparse_latent_attention_attn_gb300/csrc/sparse_attn_tc.cu",
+                       "sparse_latent_attention_attn_gb300/csrc/ptx.cuh",
+                       "sparse_latent_attention_attn_gb300/csrc/common.cuh"]
 PROFILE_SUMMARY = "profiles/sparse_attn_{workload}.txt"
 
 
@@ -445,7 +447,8 @@ def run_ours(args):
         roof["frac"] = roof["achieved"] / roof["peak"]
         roof["traffic"] = profiled_traffic(w.name, 1)
         roof["peak_source"] = peaks["source"]
-        roof["kernel"] = "sparse_attn"
+        roof["kernel"] = "sparse_attn (tcgen05 kernel + combine)"
+        roof["kernel_source_sha256_16"] = kernel_source_hash()
         roof["kernel_ms"] = attn_s * 1e3
         roof["roofline_ms"] = max(t_hbm, t_tc) * 1e3
         roof["algorithmic_bytes"] = alg_bytes
