@@ -121,9 +121,10 @@ struct Params {
     unsigned int *status;
 };
 
-// Start of cluster c's range of the flattened entry space.
+// Start of cluster c's range of the flattened entry space.  The host guarantees G * E < 2^63,
+// so the product is exact in 64 bits (a 128-bit division is a long software routine on the GPU).
 __host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t E, int64_t G) {
-    return (int64_t)(((__int128)c * E) / G);
+    return (int64_t)(((uint64_t)c * (uint64_t)E) / (uint64_t)G);
 }
 
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
@@ -425,16 +426,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 tmem_ld_wait(r0);
                 tmem_ld_wait(r1);
                 // plain stores into the peer's exchange buffer, then one release-arrive per warp
+                // rows of heads >= h are never read, so only live rows cross the cluster
                 const uint32_t rbuf = xpeer + sb * XSTRIDE;
+                if (live) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    st_cluster_v4(rbuf + (k * 128 + t) * 16, __uint_as_float(r0[4 * k]), __uint_as_float(r0[4 * k + 1]),
-                                  __uint_as_float(r0[4 * k + 2]), __uint_as_float(r0[4 * k + 3]));
+                    for (int k = 0; k < 8; ++k)
+                        st_cluster_v4(rbuf + (k * 128 + t) * 16, __uint_as_float(r0[4 * k]),
+                                      __uint_as_float(r0[4 * k + 1]), __uint_as_float(r0[4 * k + 2]),
+                                      __uint_as_float(r0[4 * k + 3]));
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    st_cluster_v4(rbuf + ((8 + k) * 128 + t) * 16, __uint_as_float(r1[4 * k]),
-                                  __uint_as_float(r1[4 * k + 1]), __uint_as_float(r1[4 * k + 2]),
-                                  __uint_as_float(r1[4 * k + 3]));
+                    for (int k = 0; k < 8; ++k)
+                        st_cluster_v4(rbuf + ((8 + k) * 128 + t) * 16, __uint_as_float(r1[4 * k]),
+                                      __uint_as_float(r1[4 * k + 1]), __uint_as_float(r1[4 * k + 2]),
+                                      __uint_as_float(r1[4 * k + 3]));
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(xfull_peer + 8u * sb);
             }
@@ -511,13 +516,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                             break;
                         }
                         const uint32_t xbuf = base + C::SM_X + sb * XSTRIDE;
+                        if (live) {
 #pragma unroll
-                        for (int k = 0; k < BN / 4; ++k) {
-                            const float4 v = ld_shared_v4(xbuf + (k * 128 + t) * 16);
-                            s[4 * k] += v.x;
-                            s[4 * k + 1] += v.y;
-                            s[4 * k + 2] += v.z;
-                            s[4 * k + 3] += v.w;
+                            for (int k = 0; k < BN / 4; ++k) {
+                                const float4 v = ld_shared_v4(xbuf + (k * 128 + t) * 16);
+                                s[4 * k] += v.x;
+                                s[4 * k + 1] += v.y;
+                                s[4 * k + 2] += v.z;
+                                s[4 * k + 3] += v.w;
+                            }
                         }
                         __syncwarp();
                         if (lane == 0) mbar_arrive_cluster(xfree_peer + 8u * sb);
@@ -681,11 +688,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
 }
 
 // Merge the partials of every token that a range boundary cut, add the sink once, write bf16.
-// Block c (1 <= c < G) owns the token holding boundary e(c) when that boundary falls inside a
-// token and no earlier boundary falls inside the same token.
+// Block (c - 1, y) owns heads 8y..8y+7 of the token holding boundary e(c) when that boundary
+// falls inside a token and no earlier boundary falls inside the same token; one warp per head,
+// each lane holding D/32 consecutive-by-vector elements of the row.
+constexpr int kCombineHeadsPerBlock = 8;
+
 template <int D>
-__global__ void __launch_bounds__(256) sparse_attn_combine_kernel(const Params p) {
+__global__ void __launch_bounds__(32 * kCombineHeadsPerBlock) sparse_attn_combine_kernel(const Params p) {
     const int c = blockIdx.x + 1;
+    const int hh = blockIdx.y * kCombineHeadsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (hh >= p.h) return;
     const int64_t T = p.topk;
     const int64_t eb = range_start(c, p.E, p.G);
     if (eb % T == 0 || eb >= p.E) return;
@@ -698,40 +711,61 @@ __global__ void __launch_bounds__(256) sparse_attn_combine_kernel(const Params p
     int64_t cf = c - 1;
     while (cf > 0 && range_start(cf, p.E, p.G) > ts) --cf;
     constexpr size_t SLOT = (size_t)SLOT_HEADS * D + 2 * SLOT_HEADS;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int hh = warp; hh < p.h; hh += 8) {
-        const float sink2 = p.sink[hh] * kLog2e;
-        float top = sink2;
-        for (int64_t k = cf; k < p.G; ++k) {
-            const int64_t r0 = range_start(k, p.E, p.G), r1 = range_start(k + 1, p.E, p.G);
-            if (r0 >= te) break;
-            if (r1 <= r0 || r1 <= ts) continue;
-            const int slot = (r0 / T == tok) ? 0 : 1;
-            const float *ws = p.ws + ((size_t)k * 2 + slot) * SLOT;
-            top = fmaxf(top, ws[SLOT_HEADS * D + hh]);
+    constexpr int PER = D / 32;                 // elements per lane
+    constexpr int VW = PER >= 4 ? 4 : PER;      // floats per vector load
+    constexpr int NV = PER / VW;                // vector loads per lane per partial
+    static_assert(PER % VW == 0 && (VW == 2 || VW == 4), "combine vector width");
+
+    const float sink2 = p.sink[hh] * kLog2e;
+    float top = sink2;
+    for (int64_t k = cf; k < p.G; ++k) {
+        const int64_t r0 = range_start(k, p.E, p.G), r1 = range_start(k + 1, p.E, p.G);
+        if (r0 >= te) break;
+        if (r1 <= r0 || r1 <= ts) continue;
+        const int slot = (r0 / T == tok) ? 0 : 1;
+        top = fmaxf(top, p.ws[((size_t)k * 2 + slot) * SLOT + SLOT_HEADS * D + hh]);
+    }
+    float den = exp2f(sink2 - top);
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.0f;
+    for (int64_t k = cf; k < p.G; ++k) {
+        const int64_t r0 = range_start(k, p.E, p.G), r1 = range_start(k + 1, p.E, p.G);
+        if (r0 >= te) break;
+        if (r1 <= r0 || r1 <= ts) continue;
+        const int slot = (r0 / T == tok) ? 0 : 1;
+        const float *ws = p.ws + ((size_t)k * 2 + slot) * SLOT;
+        const float mk = ws[SLOT_HEADS * D + hh];
+        if (mk == -INFINITY) continue;
+        const float w = exp2f(mk - top);
+        den += w * ws[SLOT_HEADS * D + SLOT_HEADS + hh];
+        const float *orow = ws + (size_t)hh * D;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            if constexpr (VW == 4) {
+                const float4 x = reinterpret_cast<const float4 *>(orow)[v * 32 + lane];
+                acc[4 * v] += w * x.x;
+                acc[4 * v + 1] += w * x.y;
+                acc[4 * v + 2] += w * x.z;
+                acc[4 * v + 3] += w * x.w;
+            } else {
+                const float2 x = reinterpret_cast<const float2 *>(orow)[v * 32 + lane];
+                acc[2 * v] += w * x.x;
+                acc[2 * v + 1] += w * x.y;
+            }
         }
-        float den = exp2f(sink2 - top);
-        float acc[D / 32];
+    }
+    const float inv = 1.0f / den;
+    uint16_t *dst = p.o + (tok * p.h + hh) * (int64_t)D;
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) acc[i] = 0.0f;
-        for (int64_t k = cf; k < p.G; ++k) {
-            const int64_t r0 = range_start(k, p.E, p.G), r1 = range_start(k + 1, p.E, p.G);
-            if (r0 >= te) break;
-            if (r1 <= r0 || r1 <= ts) continue;
-            const int slot = (r0 / T == tok) ? 0 : 1;
-            const float *ws = p.ws + ((size_t)k * 2 + slot) * SLOT;
-            const float mk = ws[SLOT_HEADS * D + hh];
-            if (mk == -INFINITY) continue;
-            const float w = exp2f(mk - top);
-            den += w * ws[SLOT_HEADS * D + SLOT_HEADS + hh];
-            const float *orow = ws + (size_t)hh * D;
-#pragma unroll
-            for (int i = 0; i < D / 32; ++i) acc[i] += w * orow[i * 32 + lane];
+    for (int v = 0; v < NV; ++v) {
+        if constexpr (VW == 4) {
+            reinterpret_cast<uint2 *>(dst)[v * 32 + lane] =
+                make_uint2(pack_bf16x2(acc[4 * v] * inv, acc[4 * v + 1] * inv),
+                           pack_bf16x2(acc[4 * v + 2] * inv, acc[4 * v + 3] * inv));
+        } else {
+            reinterpret_cast<uint32_t *>(dst)[v * 32 + lane] = pack_bf16x2(acc[2 * v] * inv, acc[2 * v + 1] * inv);
         }
-        const float inv = 1.0f / den;
-        uint16_t *dst = p.o + (tok * p.h + hh) * (int64_t)D;
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) dst[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i] * inv));
     }
 }
 
@@ -823,6 +857,7 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     if (gmax <= 0) return DS_ECUDA;
     const int64_t ntok = (int64_t)a.b * a.m;
     const int64_t G = choose_clusters(ntok, a.topk, gmax);
+    if (a.topk > 0 && ntok > (INT64_MAX / (G + 1)) / a.topk) return DS_EUNSUPPORTED;   // G * E < 2^63
     const bool split = splits_tokens(ntok, a.topk, G);
     const size_t need = split ? (size_t)G * 2 * ((size_t)SLOT_HEADS * D + 2 * SLOT_HEADS) * sizeof(float) : 0;
     if (a.workspace_bytes < need || (need && !a.workspace)) return DS_EWORKSPACE;
@@ -857,7 +892,8 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     cfg.numAttrs = C::CL > 1 ? 1 : 0;
     if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D>, p) != cudaSuccess) return DS_ECUDA;
     if (split) {
-        sparse_attn_combine_kernel<D><<<(unsigned)(G - 1), 256, 0, stream>>>(p);
+        const dim3 grid((unsigned)(G - 1), (unsigned)((a.h + kCombineHeadsPerBlock - 1) / kCombineHeadsPerBlock));
+        sparse_attn_combine_kernel<D><<<grid, 32 * kCombineHeadsPerBlock, 0, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return DS_ECUDA;
     }
     return DS_OK;
