@@ -1,4 +1,4 @@
-// sparse_attn_tc.cu -- sparse_attn on the 5th-generation tensor cores (tcgen05 + TMEM + TMA gather).
+// sparse_attn_tc.cu -- sparse_attn on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
 // What it computes ("Module attn", sparse_attn and the Precision paragraph; "DeepSeek V4.1",
 // attention/attend, sparse_attn_kernel): for every query token and head, softmax over the
@@ -8,17 +8,22 @@
 // How (GB300-first design; the pages' kernel is prior art only):
 //  * Every head of a token shares the same gathered rows, so Q[h x d] K^T and P V are dense bf16
 //    contractions with M = heads (padded to 128 = TMEM lanes).  S and O accumulate in TMEM.
-//  * Rows are gathered once per (token, tile of 64 valid rows) by TMA tile::gather4 straight into
-//    128-byte-swizzled shared memory and used by all heads, as the keys (K-major B operand of
-//    Q K^T) and as the values (MN-major B operand of P V).  -1 entries are compacted away first,
-//    so they cost neither bytes nor MMA work.
-//  * Q and P live in TMEM and are the A operands, so shared memory bandwidth is spent on the
-//    gathered rows only.
+//  * Rows are gathered once per (token, tile of 64 valid rows) by cp.async into 128-byte-swizzled
+//    shared memory and used by all heads, as the keys (K-major B operand of Q K^T) and as the
+//    values (MN-major B operand of P V).  -1 entries are compacted away first, so they cost
+//    neither bytes nor MMA work; rows of later tiles are pulled into L2 ahead of the copies.
+//  * Q lives in TMEM (A operand of Q K^T); P is written to shared memory in the swizzled K-major
+//    layout (A operand of P V), so a score buffer is free again as soon as it has been read and the
+//    MMA can run two tiles ahead of the softmax.
 //  * head_dim 512: O[128 x 512] f32 alone would fill TMEM, so a 2-CTA cluster splits the d columns:
-//    each CTA gathers and multiplies its own 256 columns, the two partial score tiles are summed
-//    through distributed shared memory, and both CTAs run the identical softmax.
-//  * Warp roles: warps 0-3 softmax and epilogue (thread = head = TMEM lane), warp 4 index
-//    compaction + TMA producer, warp 5 TMEM allocation + single-thread MMA issue.
+//    each CTA gathers and multiplies its own 256 columns and the two partial score tiles are summed
+//    through distributed shared memory.  Dedicated exchange warps send this CTA's partial scores
+//    to the peer while the softmax warps work on the previous tile; both CTAs then run the
+//    identical softmax.
+//  * Warp roles (16 warps): 0-3 softmax and epilogue (thread = head = TMEM lane); 4-7 and 14-15
+//    row gather, plus 8-11 when d is not split; 8-11 score exchange when it is; 12 index
+//    compaction; 13 TMEM allocation + single-thread MMA issue, in whatever order its inputs
+//    become ready.
 //  * Persistent clusters take contiguous ranges of the flattened (token, index entry) space, so
 //    the load is balanced whatever the batch; a token cut by a range boundary leaves f32 partials
 //    (running max, sum, unnormalised O) in the workspace and a combine kernel merges them with the
@@ -39,16 +44,12 @@ namespace tc {
 using namespace ptx;
 
 constexpr int BN = 64;            // gathered rows per tile: N of Q K^T, K of P V
-constexpr int NSTAGE = 4;         // tiles in flight in shared memory
 constexpr int PREFETCH = 4;       // tiles further ahead whose rows are pulled into L2
 constexpr int LMAX = 4096;        // largest index row handled (entries of one token)
-// warp roles (16 warps = 4 warpgroups)
-constexpr int NTHREADS = 512;
-constexpr int W_PROD0 = 4;        // warps 4-11: row gather (cp.async), 256 threads
-constexpr int NPROD_WARPS = 8;
-constexpr int NPROD = NPROD_WARPS * 32;
+constexpr int NTHREADS = 512;     // 16 warps = 4 warpgroups
+constexpr int W_XCH0 = 8;         // warps 8-11: score exchange (split d) or row gather
 constexpr int W_LIST = 12;        // index compaction
-constexpr int W_MMA = 13;         // TMEM allocation + MMA issue (warps 14-15 idle)
+constexpr int W_MMA = 13;         // TMEM allocation + MMA issue
 // register split: softmax warpgroup 232, the other three 88 (128 * (232 + 3 * 88) = 63488 <= 65536)
 constexpr uint32_t REG_SOFTMAX = 232, REG_OTHER = 88;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
@@ -64,30 +65,47 @@ struct Cfg {
     static constexpr int NCHUNK = DH / 64;          // 128-byte column chunks per row
     static constexpr int CHUNK_BYTES = BN * 128;
     static constexpr int TILE_BYTES = BN * DH * 2;
-    // TMEM columns (32-bit): O accumulator, two S buffers (P aliases the first BN/2 columns), Q
+    static constexpr int NSTAGE = CL == 2 ? 3 : 4;  // tiles in flight in shared memory
+    static constexpr int NPROD_WARPS = CL == 2 ? 6 : 10;
+    static constexpr int NPROD = NPROD_WARPS * 32;
+    // TMEM columns (32-bit): O accumulator, two S buffers, Q (bf16 pairs)
     static constexpr int O_COL = 0;
     static constexpr int S_COL = DH;
     static constexpr int Q_COL = DH + 2 * BN;
     static constexpr int TMEM_COLS = (Q_COL + DH / 2) <= 256 ? 256 : 512;
     // shared memory, offsets from a 1024-aligned base
+    static constexpr int P_BYTES = 128 * BN * 2;    // one P tile, bf16, 128-byte rows
     static constexpr int SM_KV = 0;
-    static constexpr int SM_X = SM_KV + NSTAGE * TILE_BYTES;
+    static constexpr int SM_P = SM_KV + NSTAGE * TILE_BYTES;
+    static constexpr int SM_X = SM_P + 2 * P_BYTES;
     static constexpr int X_BYTES = CL == 2 ? 2 * 128 * BN * 4 : 0;
     static constexpr int SM_LIST = SM_X + X_BYTES;
-    static constexpr int SM_BAR = SM_LIST + LMAX * 4;
-    static constexpr int SM_END = SM_BAR + 256;
+    static constexpr int LIST_BYTES = (LMAX + 16) * 4;
+    static constexpr int SM_BAR = SM_LIST + LIST_BYTES;
+    static constexpr int SM_END = SM_BAR + 512;
     static constexpr int SMEM_BYTES = SM_END + 1024;
     static_assert(Q_COL + DH / 2 <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(SM_P % 1024 == 0 && P_BYTES % 1024 == 0, "swizzled operands are 1024-byte aligned");
 };
+
+// Producer index (0..NPROD_WARPS-1) of a gather warp, -1 for other warps.
+template <int D>
+__device__ __forceinline__ int prod_warp(int warp) {
+    if (warp >= 4 && warp < 8) return warp - 4;
+    if (Cfg<D>::CL == 1 && warp >= 8 && warp < 12) return warp - 4;
+    if (warp >= 14) return Cfg<D>::NPROD_WARPS - 2 + (warp - 14);
+    return -1;
+}
 
 // barrier slots (8 bytes each) inside the SM_BAR block
 enum : int {
     B_FULL = 0,                 // [NSTAGE] producer -> consumers: tile landed
-    B_EMPTY = B_FULL + NSTAGE,  // [NSTAGE] consumers -> producer: stage free
-    B_SFULL = B_EMPTY + NSTAGE, // [2] MMA -> softmax: S ready
-    B_PFULL = B_SFULL + 2,      // [2] softmax -> MMA: P written
-    B_PVDONE = B_PFULL + 2,     // [2] MMA -> softmax: P V done
+    B_EMPTY = B_FULL + 4,       // [NSTAGE] MMA -> producer: stage free
+    B_SFULL = B_EMPTY + 4,      // [2] MMA -> softmax, exchange: S ready (or the end marker)
+    B_SFREE = B_SFULL + 2,      // [2] softmax, exchange -> MMA: S buffer read
+    B_PFULL = B_SFREE + 2,      // [2] softmax -> MMA: P written to shared memory
+    B_PVDONE = B_PFULL + 2,     // [2] MMA -> softmax: P V done (P buffer and O free)
     B_QREADY = B_PVDONE + 2,    // softmax -> MMA: Q of the segment in TMEM
     B_OFREE = B_QREADY + 1,     // softmax -> MMA: epilogue has read O
     B_XFULL = B_OFREE + 1,      // [2] peer -> me: peer's partial scores are in my exchange buffer
@@ -98,11 +116,13 @@ enum : int {
     B_LFREE = B_LFULL + 1,      // producers -> compaction: the list may be overwritten
     B_COUNT = B_LFREE + 1
 };
-constexpr int META_OFF = 8 * B_COUNT;      // [NSTAGE] int2 {count, last}
-constexpr int TMEM_ADDR_OFF = META_OFF + 8 * NSTAGE;
+constexpr int META_OFF = 8 * B_COUNT;      // [4] int2 {count, last}
+constexpr int TMEM_ADDR_OFF = META_OFF + 8 * 4;
 constexpr int ABORT_OFF = TMEM_ADDR_OFF + 4;
 constexpr int NVALID_OFF = ABORT_OFF + 4;
-static_assert(ABORT_OFF + 4 <= 256, "barrier block");
+constexpr int LOFF_OFF = NVALID_OFF + 4;
+constexpr int SEND_OFF = LOFF_OFF + 4;
+static_assert(SEND_OFF + 4 <= 512, "barrier block");
 
 struct Params {
     const uint16_t *q;
@@ -127,22 +147,23 @@ __host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t E, in
     return (int64_t)(((uint64_t)c * (uint64_t)E) / (uint64_t)G);
 }
 
-__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-
-// Lane 0 polls the barrier for the whole warp (one poller per warp keeps the barrier hardware
-// free for the arrivals), then the other lanes acquire the completed phase themselves; the warp
-// proceeds together or not at all, so warp-collective tcgen05 instructions never diverge.
+// Lane 0 waits for the whole warp (acquire) and broadcasts the outcome; every other lane's
+// accesses to the guarded data come after it receives that value.  Having every lane re-check the
+// barrier, or adding a warp barrier, costs about a microsecond or a quarter of one per tile on
+// this path (measured).  The warp proceeds together or not at all, so warp-collective tcgen05
+// instructions never diverge.
+// kCluster: the phase was completed from the other CTA of the cluster (acquire at cluster scope).
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
     bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, kWaitLimitNs);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) ok = mbar_try_wait(bar, parity);   // completed: returns at once, with acquire semantics
-    return __all_sync(0xffffffffu, ok);
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait<kCluster>(bar, parity, abort, kWaitLimitNs);
+    return __shfl_sync(0xffffffffu, ok, 0);
 }
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Params p) {
     using C = Cfg<D>;
+    constexpr int NSTAGE = C::NSTAGE;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -151,6 +172,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
     int2 *meta = reinterpret_cast<int2 *>(sbase + C::SM_BAR + META_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + ABORT_OFF);
+    volatile int *seg_nvalid = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + NVALID_OFF);
+    volatile int *seg_loff = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + LOFF_OFF);
+    volatile int *s_end = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + SEND_OFF);
     int32_t *list = reinterpret_cast<int32_t *>(sbase + C::SM_LIST);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -163,24 +187,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     // ---- set-up --------------------------------------------------------------------------------
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(BAR(B_FULL + s), NPROD + 1);   // every gather thread's copies + the meta writer
+            mbar_init(BAR(B_FULL + s), C::NPROD + 1);   // every gather thread's copies + the meta writer
             mbar_init(BAR(B_EMPTY + s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(B_SFULL + i), 1);
+            mbar_init(BAR(B_SFREE + i), C::CL == 2 ? 8 : 4);   // one arrival per reading warp
             mbar_init(BAR(B_PFULL + i), 128);
             mbar_init(BAR(B_PVDONE + i), 1);
-            mbar_init(BAR(B_XFULL + i), 4);     // one arrival per softmax warp of the peer
+            mbar_init(BAR(B_XFULL + i), 1);     // armed by the receiver; the peer's bytes complete it
             mbar_init(BAR(B_XFREE + i), 4);     // one arrival per softmax warp of the peer
         }
         mbar_init(BAR(B_QREADY), 128);
         mbar_init(BAR(B_OFREE), 128);
         mbar_init(BAR(B_DRAIN), 1);
-        mbar_init(BAR(B_ZREAD), 128);
+        mbar_init(BAR(B_ZREAD), 128 + 1);     // softmax threads + the MMA thread
         mbar_init(BAR(B_LFULL), 32);
-        mbar_init(BAR(B_LFREE), NPROD_WARPS);
+        mbar_init(BAR(B_LFREE), C::NPROD_WARPS);
         *abort_flag = 0;
+        *s_end = -1;
         fence_mbar_init();
+        if constexpr (C::CL == 2) {
+            // the exchange buffers expect the peer's live score rows of tiles 0 and 1
+            const uint32_t xbytes = (uint32_t)(p.h < 128 ? p.h : 128) * BN * 4;
+            mbar_arrive_expect_tx(BAR(B_XFULL + 0), xbytes);
+            mbar_arrive_expect_tx(BAR(B_XFULL + 1), xbytes);
+        }
     }
     // rows a tile does not load keep finite values: zero every stage once
     for (int i = threadIdx.x; i < NSTAGE * C::TILE_BYTES / 16; i += NTHREADS)
@@ -194,12 +226,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sbase + C::SM_BAR + TMEM_ADDR_OFF);
-    volatile int *seg_nvalid = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + NVALID_OFF);
-    // warpgroup 3 (compaction, MMA, two idle warps) gives registers back before it branches
-    if (warp >= 12) setmaxnreg_dec<REG_OTHER>();
+    // warpgroups 1-3 give registers back to the softmax warpgroup before they branch
+    if (warp >= 4) setmaxnreg_dec<REG_OTHER>();
 
     const int64_t tok_begin = e0 / (T > 0 ? T : 1);
     const bool has_work = e1 > e0 && T > 0;
+    const int pw = prod_warp<D>(warp);
 
     if (warp == W_LIST) {
         // ======================== index compaction: one list per segment ========================
@@ -208,9 +240,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             const int a = (int)((e0 > tok * T ? e0 : tok * T) - tok * T);
             const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
             if (!warp_wait(BAR(B_LFREE), (seg & 1) ^ 1, abort_flag)) break;
-            const int32_t *irow = p.idx + tok * T;
-            // stage the entries [a, z) into shared memory with one round trip, then compact in place
-            for (int j = a + lane; j < z; j += 32) cp_async_4(smem_u32(list + (j - a)), irow + j);
+            // stage entries [a, z) with one round trip: entry g of the flattened index tensor goes
+            // to list[g - g0], g0 = g_a rounded down to 4 entries, so 16-byte pieces stay aligned
+            const int64_t g_a = tok * T + a, g_z = tok * T + z;
+            const int off = (int)(g_a & 3);
+            const int64_t g0 = g_a - off;
+            const int64_t ga4 = (g_a + 3) & ~(int64_t)3, gz4 = g_z & ~(int64_t)3;
+            if (ga4 >= gz4) {
+                for (int64_t g = g_a + lane; g < g_z; g += 32) cp_async_4(smem_u32(list + (g - g0)), p.idx + g);
+            } else {
+                for (int64_t g = g_a + lane; g < ga4; g += 32) cp_async_4(smem_u32(list + (g - g0)), p.idx + g);
+                for (int64_t g = ga4 + 4 * lane; g < gz4; g += 128) cp_async_16(smem_u32(list + (g - g0)), p.idx + g);
+                for (int64_t g = gz4 + lane; g < g_z; g += 32) cp_async_4(smem_u32(list + (g - g0)), p.idx + g);
+            }
             cp_async_wait_all();
             __syncwarp();
             {   // warm L2 with the next token's index row
@@ -218,11 +260,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 if (nt * T < e1)
                     for (int j = lane * 32; j < T; j += 32 * 32) prefetch_l2(p.idx + nt * T + j);
             }
+            // compact in place: valid entries move to the front (writes never pass the reads)
             int nvalid = 0;
             bool bad = false;
             for (int j0 = 0; j0 < z - a; j0 += 32) {
                 const int j = j0 + lane;
-                const int v = j < z - a ? list[j] : -1;
+                const int v = j < z - a ? list[off + j] : -1;
                 const bool valid = v >= 0 && (int64_t)v < p.n;
                 bad |= (int64_t)v >= p.n;
                 const uint32_t bal = __ballot_sync(0xffffffffu, valid);
@@ -235,17 +278,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             if (lane == 0) *seg_nvalid = nvalid;
             mbar_arrive(BAR(B_LFULL));          // every lane releases its own list stores
         }
-    } else if (warp >= W_PROD0 && warp < W_PROD0 + NPROD_WARPS) {
+    } else if (pw >= 0) {
         // ================== row gather: cp.async into the 128-byte-swizzled ring ==================
         // A row half of DH columns is U = DH / 8 units of 16 bytes; each warp instruction copies
         // 32 / U whole rows, so every global access is a contiguous row piece.
-        setmaxnreg_dec<REG_OTHER>();
         constexpr int U = C::DH / 8;
         constexpr int RPW = 32 / U;                      // rows per warp instruction
-        const int pw = warp - W_PROD0;                   // producer warp 0..7
         const int rsub = lane / U, unit = lane % U;
         const int chunk = unit / 8, u8 = unit % 8;
         const bool writer = pw == 0 && lane == 0;
+        const int ptid = pw * 32 + lane;
         int it = 0, seg = 0;
         bool ok = true;
         for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok, ++seg) {
@@ -256,10 +298,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             // L2 prefetch: producer thread i pulls 128-byte line i % (DH/64) of row i / (DH/64) of a
             // tile PREFETCH tiles ahead, so the shared-memory copies below mostly hit L2
             constexpr int LINES = C::DH / 64;                   // 128-byte lines per row half
-            const int pf_row = (threadIdx.x - W_PROD0 * 32) / LINES, pf_line = (threadIdx.x - W_PROD0 * 32) % LINES;
+            const int pf_row = ptid / LINES, pf_line = ptid % LINES;
             const uint16_t *kvl = p.kv + ((tok / p.m) * p.n) * (int64_t)D + crank * C::DH + pf_line * 64;
             auto prefetch_tile = [&](int tt) {
-                for (int r = pf_row; r < BN; r += NPROD / LINES) {
+                for (int r = pf_row; r < BN; r += C::NPROD / LINES) {
                     const int k = tt * BN + r;
                     if (k < nvalid) prefetch_l2(kvl + (int64_t)list[k] * D);
                 }
@@ -275,7 +317,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 const int cnt = nvalid - t * BN < BN ? nvalid - t * BN : BN;
                 const uint32_t dst0 = base + C::SM_KV + stage * C::TILE_BYTES + chunk * C::CHUNK_BYTES;
 #pragma unroll 4
-                for (int r = pw * RPW + rsub; r < cnt; r += NPROD_WARPS * RPW) {
+                for (int r = pw * RPW + rsub; r < cnt; r += C::NPROD_WARPS * RPW) {
                     // row r, 16-byte unit u8 of its 128-byte chunk: swizzled to unit u8 ^ (r % 8)
                     const int v = list[t * BN + r];
                     cp_async_16(dst0 + r * 128 + ((u8 ^ (r & 7)) << 4), kvb + (int64_t)v * D);
@@ -293,90 +335,177 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         cp_async_wait_all();                              // nothing may land after the CTA exits
     } else if (warp == W_MMA) {
         // ================================= MMA issue (lane 0) =================================
+        // Two independent streams, each in tile order: S = Q K^T for the next tile whose rows have
+        // landed (once its score buffer has been read), and O += P V for the oldest tile whose P is
+        // written.  Whichever is ready goes first, so a slow softmax never holds back the scores
+        // of the tiles behind it.
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false);
             constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, C::DH, true);
+            int64_t tok = tok_begin;
             int it = 0, J = 0, seg = 0;
+            bool first = true, s_more = has_work;
+            // pending P V, oldest at pq_head; at most three can be outstanding
+            int pq_J[4], pq_stage[4], pq_seg[4];
+            bool pq_first[4];
+            int pq_head = 0, pq_tail = 0;
+            uint64_t idle_since = 0;
+            uint32_t idle = 0;
             bool ok = true;
-            bool pend = false, pend_first = false;
-            int pend_stage = 0, pend_J = 0, pend_seg = 0;
-            // O += P V for the pending tile (P from TMEM, V = the same gathered rows)
-            auto issue_pv = [&]() -> bool {
-                const int sb = pend_J & 1;
-                if (!mbar_wait(BAR(B_PFULL + sb), (pend_J >> 1) & 1, abort_flag, kWaitLimitNs)) return false;
-                if (pend_first && pend_seg > 0 &&
-                    !mbar_wait(BAR(B_OFREE), (pend_seg - 1) & 1, abort_flag, kWaitLimitNs))
-                    return false;
-                tc_fence_after();
-                const uint32_t vbase = base + C::SM_KV + pend_stage * C::TILE_BYTES;
-#pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    // V rows 16k..16k+15 as the MN-major B operand (d contiguous): 8-row groups
-                    // 1024 B apart, 64-column chunks CHUNK_BYTES apart
-                    const uint64_t bdesc = smem_desc_sw128(vbase + k * 2048, C::CHUNK_BYTES, 1024);
-                    mma_bf16_ts(tmem + C::O_COL, tmem + C::S_COL + sb * BN + k * 8, bdesc, IDESC_PV,
-                                (pend_first && k == 0) ? 0u : 1u);
-                }
-                mma_commit(BAR(B_EMPTY + pend_stage));
-                mma_commit(BAR(B_PVDONE + sb));
-                pend = false;
-                return true;
-            };
-            for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok, ++seg) {
-                bool first = true;
-                for (;;) {
+            for (;;) {
+                bool progressed = false;
+                if (s_more) {
                     const int stage = it % NSTAGE;
-                    if (!mbar_wait(BAR(B_FULL + stage), (it / NSTAGE) & 1, abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    const int2 mt = meta[stage];
-                    if (first && !mbar_wait(BAR(B_QREADY), seg & 1, abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    // the rows were written by cp.async (generic proxy); the MMA reads them through
-                    // the async proxy
-                    fence_proxy_async_smem();
-                    tc_fence_after();
-                    if (mt.x > 0) {
-                        // S = Q K^T: K rows as the K-major B operand; 16 columns = 32 bytes inside
-                        // the 128-byte swizzle atom of chunk k/4; 8-row groups 1024 B apart
-                        const int sb = J & 1;
-                        const uint32_t kbase = base + C::SM_KV + stage * C::TILE_BYTES;
+                    if (mbar_test_wait(BAR(B_FULL + stage), (it / NSTAGE) & 1)) {
+                        const int2 mt = meta[stage];
+                        if (mt.x == 0) {
+                            // a segment without a single valid row: nothing to multiply; the softmax
+                            // warps hand the stage back once this thread has read the meta too
+                            mbar_arrive(BAR(B_ZREAD));
+                            ++it;
+                            ++seg;
+                            ++tok;
+                            first = true;
+                            s_more = tok * T < e1;
+                            progressed = true;
+                        } else if (mbar_test_wait(BAR(B_SFREE + (J & 1)), ((J >> 1) & 1) ^ 1) &&
+                                   (!first || mbar_test_wait(BAR(B_QREADY), seg & 1))) {
+                            // the rows were written by cp.async (generic proxy); the MMA reads them
+                            // through the async proxy
+                            fence_proxy_async_smem();
+                            tc_fence_after();
+                            // S = Q K^T: K rows as the K-major B operand; 16 columns = 32 bytes inside
+                            // the 128-byte swizzle atom of chunk k/4; 8-row groups 1024 B apart
+                            const uint32_t kbase = base + C::SM_KV + stage * C::TILE_BYTES;
 #pragma unroll
-                        for (int k = 0; k < C::DH / 16; ++k) {
-                            const uint64_t bdesc =
-                                smem_desc_sw128(kbase + (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32, 16, 1024);
-                            mma_bf16_ts(tmem + C::S_COL + sb * BN, tmem + C::Q_COL + k * 8, bdesc, IDESC_S,
-                                        k > 0 ? 1u : 0u);
+                            for (int k = 0; k < C::DH / 16; ++k) {
+                                const uint64_t bdesc =
+                                    smem_desc_sw128(kbase + (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32, 16, 1024);
+                                mma_bf16_ts(tmem + C::S_COL + (J & 1) * BN, tmem + C::Q_COL + k * 8, bdesc, IDESC_S,
+                                            k > 0 ? 1u : 0u);
+                            }
+                            mma_commit(BAR(B_SFULL + (J & 1)));
+                            const int q = pq_tail & 3;
+                            pq_J[q] = J;
+                            pq_stage[q] = stage;
+                            pq_seg[q] = seg;
+                            pq_first[q] = first;
+                            ++pq_tail;
+                            ++J;
+                            ++it;
+                            first = false;
+                            if (mt.y) {
+                                ++seg;
+                                ++tok;
+                                first = true;
+                                s_more = tok * T < e1;
+                            }
+                            progressed = true;
                         }
-                        mma_commit(BAR(B_SFULL + sb));
                     }
-                    if (pend && !issue_pv()) {
+                }
+                if (pq_head != pq_tail) {
+                    const int q = pq_head & 3;
+                    const int Jp = pq_J[q];
+                    if (mbar_test_wait(BAR(B_PFULL + (Jp & 1)), (Jp >> 1) & 1) &&
+                        (!pq_first[q] || pq_seg[q] == 0 || mbar_test_wait(BAR(B_OFREE), (pq_seg[q] - 1) & 1))) {
+                        // P was written by st.shared (generic proxy) and fenced by its writers
+                        tc_fence_after();
+                        const uint32_t pbase = base + C::SM_P + (Jp & 1) * C::P_BYTES;
+                        const uint32_t vbase = base + C::SM_KV + pq_stage[q] * C::TILE_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BN / 16; ++k) {
+                            // P: K-major A operand, 16 columns = 32 bytes of each 128-byte row.
+                            // V rows 16k..16k+15 as the MN-major B operand (d contiguous): 8-row
+                            // groups 1024 B apart, 64-column chunks CHUNK_BYTES apart
+                            const uint64_t adesc = smem_desc_sw128(pbase + k * 32, 16, 1024);
+                            const uint64_t bdesc = smem_desc_sw128(vbase + k * 2048, C::CHUNK_BYTES, 1024);
+                            mma_bf16_ss(tmem + C::O_COL, adesc, bdesc, IDESC_PV, (pq_first[q] && k == 0) ? 0u : 1u);
+                        }
+                        mma_commit(BAR(B_EMPTY + pq_stage[q]));
+                        mma_commit(BAR(B_PVDONE + (Jp & 1)));
+                        ++pq_head;
+                        progressed = true;
+                    }
+                }
+                if (!s_more && pq_head == pq_tail) break;
+                if (progressed) {
+                    idle = 0;
+                    idle_since = 0;
+                    continue;
+                }
+                // nothing ready: sleep briefly so the polling does not take issue slots from the
+                // softmax warp that shares this warp's scheduler
+                __nanosleep(32);
+                if ((++idle & 63u) == 0u) {
+                    if (*abort_flag) {
                         ok = false;
                         break;
                     }
-                    if (mt.x > 0) {
-                        pend = true;
-                        pend_first = first;
-                        pend_stage = stage;
-                        pend_J = J;
-                        pend_seg = seg;
-                        ++J;
+                    const uint64_t now = globaltimer_ns();
+                    if (idle_since == 0) {
+                        idle_since = now;
+                    } else if (now - idle_since > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
                     }
-                    ++it;
-                    first = false;
-                    if (mt.y) break;
                 }
             }
-            if (ok && pend) ok = issue_pv();
+            (void)ok;
+            if constexpr (C::CL == 2) {
+                // end marker for the exchange warps: no score tile J follows
+                *s_end = J;
+                mbar_arrive(BAR(B_SFULL + (J & 1)));
+            }
             if (*abort_flag) {   // let issued MMAs finish before TMEM is freed
                 mma_commit(BAR(B_DRAIN));
                 mbar_wait_drain(BAR(B_DRAIN), 0, 100000000ull);
             }
         }
         __syncwarp();
+    } else if (C::CL == 2 && warp >= W_XCH0 && warp < W_XCH0 + 4) {
+        // ======================= score exchange (d split across the cluster) =======================
+        // Warp w reads TMEM lane quarter w % 4 of each finished score tile and stores it into the
+        // peer's exchange buffer, so the softmax warps never wait on the cluster network to send.
+        const int quarter = warp & 3;
+        const int t = quarter * 32 + lane;               // head row = TMEM lane
+        const bool live = t < p.h;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        constexpr uint32_t XSTRIDE = 128 * BN * 4;       // one exchange buffer
+        const uint32_t xpeer = mapa(base + C::SM_X, peer);
+        const uint32_t xfull_peer = mapa(BAR(B_XFULL), peer);   // counts the bytes of each store
+        for (int J = 0; has_work; ++J) {
+            const int sb = J & 1;
+            const uint32_t ph = (J >> 1) & 1;
+            if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) break;
+            if (*s_end == J) break;
+            // the peer has read what this warp sent into the same buffer two tiles ago
+            if (!warp_wait<true>(BAR(B_XFREE + sb), ph ^ 1, abort_flag)) break;
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tmem + lane_off + C::S_COL + sb * BN, r0);
+            tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + 32, r1);
+            tmem_ld_wait(r0);
+            tmem_ld_wait(r1);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
+            // rows of heads >= h are never read, so only live rows cross the cluster; each
+            // asynchronous store counts its bytes on the peer's barrier (no fence needed)
+            const uint32_t rbuf = xpeer + sb * XSTRIDE, rbar = xfull_peer + 8u * sb;
+            if (live) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_async_v4(rbuf + (k * 128 + t) * 16, __uint_as_float(r0[4 * k]), __uint_as_float(r0[4 * k + 1]),
+                                __uint_as_float(r0[4 * k + 2]), __uint_as_float(r0[4 * k + 3]), rbar);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_async_v4(rbuf + ((8 + k) * 128 + t) * 16, __uint_as_float(r1[4 * k]),
+                                __uint_as_float(r1[4 * k + 1]), __uint_as_float(r1[4 * k + 2]),
+                                __uint_as_float(r1[4 * k + 3]), rbar);
+            }
+        }
     } else if (warp < 4) {
         // ============================ softmax + epilogue (warps 0-3) ============================
         setmaxnreg_inc<REG_SOFTMAX>();
@@ -385,12 +514,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         const bool live = t < p.h;
         const float sink2 = live ? p.sink[t] * kLog2e : 0.0f;
         constexpr uint32_t XSTRIDE = 128 * BN * 4;       // one exchange buffer
-        uint32_t xpeer = 0, xfull_peer = 0, xfree_peer = 0;
-        if constexpr (C::CL == 2) {
-            xpeer = mapa(base + C::SM_X, peer);
-            xfull_peer = mapa(BAR(B_XFULL), peer);
-            xfree_peer = mapa(BAR(B_XFREE), peer);
-        }
+        uint32_t xfree_peer = 0;
+        if constexpr (C::CL == 2) xfree_peer = mapa(BAR(B_XFREE), peer);
         auto load_q = [&](int64_t tok) {
             // this CTA's DH columns of q[tok][t] into TMEM columns [Q_COL, Q_COL + DH/2) of lane t
             const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (tok * p.h + t) * (int64_t)D + crank * C::DH);
@@ -411,40 +536,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             tc_fence_before();
             mbar_arrive(BAR(B_QREADY));
         };
-        // Stage A of tile Jx: its scores are in TMEM; with a column split, send this CTA's partial
-        // scores to the peer right away (asynchronous stores counted on the peer's barrier).
-        auto stage_a = [&](int Jx) -> bool {
-            const int sb = Jx & 1;
-            const uint32_t ph = (Jx >> 1) & 1;
-            if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) return false;
-            tc_fence_after();
-            if constexpr (C::CL == 2) {
-                if (!warp_wait(BAR(B_XFREE + sb), ph ^ 1, abort_flag)) return false;
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tmem + lane_off + C::S_COL + sb * BN, r0);
-                tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + 32, r1);
-                tmem_ld_wait(r0);
-                tmem_ld_wait(r1);
-                // plain stores into the peer's exchange buffer, then one release-arrive per warp
-                // rows of heads >= h are never read, so only live rows cross the cluster
-                const uint32_t rbuf = xpeer + sb * XSTRIDE;
-                if (live) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_cluster_v4(rbuf + (k * 128 + t) * 16, __uint_as_float(r0[4 * k]),
-                                      __uint_as_float(r0[4 * k + 1]), __uint_as_float(r0[4 * k + 2]),
-                                      __uint_as_float(r0[4 * k + 3]));
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_cluster_v4(rbuf + ((8 + k) * 128 + t) * 16, __uint_as_float(r1[4 * k]),
-                                      __uint_as_float(r1[4 * k + 1]), __uint_as_float(r1[4 * k + 2]),
-                                      __uint_as_float(r1[4 * k + 3]));
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(xfull_peer + 8u * sb);
-            }
-            return true;
-        };
         int it = 0, J = 0, nzero = 0;
         bool ok = true;
         if (has_work) load_q(tok_begin);
@@ -460,7 +551,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             int2 cur = meta[it % NSTAGE];
             if (cur.x == 0) {
                 // a segment without a single valid row: its only tile loads nothing; once all
-                // 128 threads have read its meta, thread 0 hands the stage back
+                // 128 threads and the MMA thread have read its meta, thread 0 hands the stage back
                 mbar_arrive(BAR(B_ZREAD));
                 if (t == 0) {
                     if (!mbar_wait(BAR(B_ZREAD), nzero & 1, abort_flag, kWaitLimitNs)) ok = false;
@@ -471,39 +562,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
             } else {
-                if (!stage_a(J)) {
-                    ok = false;
-                    break;
-                }
-                bool next_sent = false;        // stage A of tile J+1 already done
                 for (;;) {
-                    // stage A of the next tile first when its scores are already there, so its
-                    // exchange is in flight while tile J is finished; never wait for it here
-                    int2 nxt = make_int2(0, 1);
-                    if (!cur.y) {
-                        const int in = it + 1;
-                        bool ready = false;
-                        if (lane == 0)
-                            ready = mbar_try_wait(BAR(B_FULL + in % NSTAGE), (in / NSTAGE) & 1) &&
-                                    mbar_try_wait(BAR(B_SFULL + ((J + 1) & 1)), ((J + 1) >> 1) & 1);
-                        ready = __shfl_sync(0xffffffffu, ready, 0);
-                        if (ready) {
-                            nxt = meta[in % NSTAGE];
-                            if (!stage_a(J + 1)) {
-                                ok = false;
-                                break;
-                            }
-                            next_sent = true;
-                        }
-                    }
-                    // stage B of tile J: full scores -> online softmax -> P (bf16) into TMEM
+                    // tile J: own scores from TMEM (+ the peer's partial scores) -> online softmax
+                    // -> P (bf16) into shared memory
                     const int sb = J & 1;
                     const uint32_t ph = (J >> 1) & 1;
+                    if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     uint32_t r0[32], r1[32];
                     tmem_ld32(tmem + lane_off + C::S_COL + sb * BN, r0);
                     tmem_ld32(tmem + lane_off + C::S_COL + sb * BN + 32, r1);
                     tmem_ld_wait(r0);
                     tmem_ld_wait(r1);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));   // the MMA may reuse the buffer
                     float s[BN];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -511,10 +587,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         s[32 + j] = __uint_as_float(r1[j]);
                     }
                     if constexpr (C::CL == 2) {
-                        if (!warp_wait(BAR(B_XFULL + sb), ph, abort_flag)) {
+                        if (!warp_wait<true>(BAR(B_XFULL + sb), ph, abort_flag)) {
                             ok = false;
                             break;
                         }
+                        // arm the buffer for tile J + 2 (its bytes cannot come before every softmax
+                        // warp has released tile J below)
+                        if (t == 0)
+                            mbar_arrive_expect_tx(BAR(B_XFULL + sb), (uint32_t)(p.h < 128 ? p.h : 128) * BN * 4);
                         const uint32_t xbuf = base + C::SM_X + sb * XSTRIDE;
                         if (live) {
 #pragma unroll
@@ -526,8 +606,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                                 s[4 * k + 3] += v.w;
                             }
                         }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(xfree_peer + 8u * sb);
+                        __syncwarp();   // every lane's loads have returned (their sums are taken)
+                        if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer + 8u * sb);
                     }
                     const int cnt = cur.x;
                     if (cnt < BN) {
@@ -583,28 +663,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         pk[j] = pack_bf16x2(p0, p1);
                     }
                     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    tmem_st32(tmem + lane_off + C::S_COL + sb * BN, pk);
-                    tmem_st_wait();
-                    tc_fence_before();
+                    // the P buffer is free once the P V of two tiles ago is done
+                    if (J >= 2 && !warp_wait(BAR(B_PVDONE + sb), ph ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    // row t of P, 16-byte unit u at unit u ^ (t % 8) of its 128-byte row
+                    const uint32_t prow = base + C::SM_P + sb * C::P_BYTES + t * 128;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(prow + ((u ^ (t & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                    fence_proxy_async_smem();
                     mbar_arrive(BAR(B_PFULL + sb));
                     ++J;
                     ++it;
                     if (cur.y) break;
-                    // stage A of the next tile if it was not ready before
-                    if (!next_sent) {
-                        const int in = it;
-                        if (!warp_wait(BAR(B_FULL + in % NSTAGE), (in / NSTAGE) & 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        nxt = meta[in % NSTAGE];
-                        if (!stage_a(J)) {
-                            ok = false;
-                            break;
-                        }
+                    if (!warp_wait(BAR(B_FULL + it % NSTAGE), (it / NSTAGE) & 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                    next_sent = false;
-                    cur = nxt;
+                    cur = meta[it % NSTAGE];
                 }
                 if (!ok) break;
             }
@@ -684,7 +762,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if constexpr (C::CL == 2) cluster_sync();
+    if constexpr (C::CL == 2) {
+        // after an abort the peer's score stores may still be on their way into this CTA's
+        // shared memory (a normal run has received every byte): give them time to land
+        if (*abort_flag) {
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 50000ull) {
+            }
+        }
+        cluster_sync();
+    }
 }
 
 // Merge the partials of every token that a range boundary cut, add the sink once, write bf16.
