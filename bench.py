@@ -233,55 +233,81 @@ class StepSet:
 # CPU oracle baseline (bounded sample)
 # ----------------------------------------------------------------------------------------------
 
-def oracle_sample_rate(w: wl.Workload, sset: StepSet | None, budget_s: float, device):
-    """Time the oracle (plain C, all host cores) on a bounded sample of the workload's tokens."""
-    import oracle
-    oracle.build()
-    cores = os.cpu_count() or 1
-    if sset is None:
-        inp = wl.make_step_inputs(w, device=device)
-        idx = torch.empty((w.b, w.m, w.topk), dtype=torch.int32, device=device)
-        idx[..., w.win_cols:] = inp.cidx
-        q, kv, sink = inp.q, inp.kv, inp.sink
-    else:
-        idx, q, kv, sink = sset.idx, sset.q, sset.kv, sset.sink
-    # window columns as the oracle computes them
-    win = oracle.window_topk_idxs(w.s if not w.decode else 1, w.start_pos, w.window)
-    idx_host = idx.cpu().numpy()
-    idx_host[..., : w.win_cols] = win[None] if w.decode else win[None]
-    sink_h = sink.cpu().numpy()
-    # sample whole sequences (decode) or query tokens of the one sequence (prefill)
-    tokens_per_seq = w.m
+class OracleSample:
+    """The oracle (plain C, all host cores) on the host copy of a workload's inputs.
 
-    def run(nseq_or_tok):
+    Inputs are generated and copied to the host once; `time(n)` runs the oracle on the first n
+    sequences (decode) or n evenly spaced query tokens (prefill) and returns (seconds, units)."""
+
+    def __init__(self, w: wl.Workload, sset: StepSet | None, device, max_items: int):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.w = w
+        self.cores = os.cpu_count() or 1
+        if sset is None:
+            inp = wl.make_step_inputs(w, device=device)
+            idx = torch.empty((w.b, w.m, w.topk), dtype=torch.int32, device=device)
+            idx[..., w.win_cols:] = inp.cidx
+            q, kv, sink = inp.q, inp.kv, inp.sink
+        else:
+            idx, q, kv, sink = sset.idx, sset.q, sset.kv, sset.sink
+        # window columns as the oracle computes them
+        win = oracle.window_topk_idxs(w.s if not w.decode else 1, w.start_pos, w.window)
+        self.limit = w.b if w.decode else w.m
+        keep = min(self.limit, max(1, max_items))
         if w.decode:
-            seqs = torch.arange(nseq_or_tok, device=q.device)
-            qb = wl.bits(q.index_select(0, seqs))
-            kvb = wl.bits(kv.index_select(0, seqs))
-            ib = np.ascontiguousarray(idx_host[:nseq_or_tok])
+            seqs = torch.arange(keep, device=q.device)
+            self.q = wl.bits(q.index_select(0, seqs))
+            self.kv = wl.bits(kv.index_select(0, seqs))
+            self.idx = idx[:keep].cpu().numpy()
+        else:
+            self.q, self.kv = wl.bits(q), wl.bits(kv)
+            self.idx = idx.cpu().numpy()
+        self.idx[..., : w.win_cols] = win[None]
+        self.sink = sink.cpu().numpy()
+        self.keep = keep
+
+    def time(self, n: int):
+        w, o = self.w, self.oracle
+        n = max(1, min(n, self.keep))
+        if w.decode:
+            ib = np.ascontiguousarray(self.idx[:n])
             t0 = time.perf_counter()
-            oracle.sparse_attn(qb, kvb, sink_h, ib, w.scale, nthreads=cores)
+            o.sparse_attn(np.ascontiguousarray(self.q[:n]), np.ascontiguousarray(self.kv[:n]), self.sink, ib,
+                          w.scale, nthreads=self.cores)
             dt = time.perf_counter() - t0
             units = int((ib >= 0).sum()) * w.h
         else:
-            toks = np.linspace(0, w.m - 1, nseq_or_tok).astype(np.int64)
-            qb, kvb = wl.bits(q), wl.bits(kv)
+            toks = np.linspace(0, w.m - 1, n).astype(np.int64)
             t0 = time.perf_counter()
-            oracle.sparse_attn(qb, kvb, sink_h, idx_host, w.scale, tokens=toks, nthreads=cores)
+            o.sparse_attn(self.q, self.kv, self.sink, self.idx, w.scale, tokens=toks, nthreads=self.cores)
             dt = time.perf_counter() - t0
-            units = int((idx_host[0, toks] >= 0).sum()) * w.h
+            units = int((self.idx[0, toks] >= 0).sum()) * w.h
         return dt, units
 
-    limit = w.b if w.decode else tokens_per_seq
-    n = min(limit, max(1, cores))
-    dt, units = run(n)
-    if dt < budget_s / 4 and n < limit:
-        n = int(min(limit, max(n + 1, n * budget_s / max(dt, 1e-3) * 0.8)))
-        dt, units = run(n)
-    what = "sequences" if w.decode else "query tokens"
-    return {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {limit} {what} of {w.name} ({units} units, {dt:.2f} s wall, plain C, {cores} threads)",
-            "_units": units, "_seconds": dt}
+    def size_for(self, budget_s: float) -> int:
+        """Items whose oracle run takes about budget_s (measured on a first small run)."""
+        n = min(self.keep, self.cores)
+        dt, _ = self.time(n)
+        if dt < budget_s / 4 and n < self.keep:
+            n = int(min(self.keep, max(n + 1, n * budget_s / max(dt, 1e-3) * 0.8)))
+        return n
+
+    def describe(self, n: int, units: int, dt: float) -> str:
+        what = "sequences" if self.w.decode else "query tokens"
+        return (f"{n} of {self.limit} {what} of {self.w.name} ({units} units, {dt:.2f} s wall, plain C, "
+                f"{self.cores} threads)")
+
+
+def oracle_sample_rate(w: wl.Workload, sset: StepSet | None, budget_s: float, device):
+    """cpu_baseline: the oracle timed on a bounded sample (about budget_s of host work)."""
+    cores = os.cpu_count() or 1
+    smp = OracleSample(w, sset, device, max_items=max(cores, 4 * cores))
+    n = smp.size_for(budget_s)
+    dt, units = smp.time(n)
+    return {"value": units / dt, "unit": UNIT, "cores": smp.cores, "kind": "oracle",
+            "sample": smp.describe(n, units, dt), "_units": units, "_seconds": dt}
 
 
 def public(d):
@@ -303,26 +329,33 @@ def workload_config(w: wl.Workload, nsets: int):
 
 
 def run_reference(args):
+    """The reference arm: the oracle, as it stands, on the host cores (rank 0 only).
+
+    Each of the warm-up and timed steps runs the oracle on the same bounded sample of the
+    workload, sized so that the whole run takes about --ref-budget seconds of host work."""
     rank, world, local = dist_env()
     if rank != 0:
         return 0
     w = wl.WORKLOADS[args.config]
     device = "cuda" if torch.cuda.is_available() else "cpu"
+    cores = os.cpu_count() or 1
+    nsteps = args.warmup + args.steps
+    smp = OracleSample(w, None, device, max_items=4 * cores)
+    n = smp.size_for(max(0.05, args.ref_budget / max(1, nsteps)))
     total_units, total_s = 0, 0.0
-    per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
-    cb = None
-    for k in range(args.warmup + args.steps):
-        cb = oracle_sample_rate(w, None, per_step_budget, device)
+    for k in range(nsteps):
+        dt, units = smp.time(n)
         if k >= args.warmup:
-            total_units += cb["_units"]
-            total_s += cb["_seconds"]
+            total_units += units
+            total_s += dt
     value = total_units / total_s if total_s else 0.0
+    per_step = total_units // max(1, args.steps)
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / max(1, args.steps), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, N(0,1))",
            "config": workload_config(w, 1),
-           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
-                            "sample": cb["sample"]},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": smp.cores, "kind": "oracle",
+                            "sample": "each step: " + smp.describe(n, per_step, total_s / max(1, args.steps))},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
     return 0
@@ -478,6 +511,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=60.0,
+                    help="seconds of host work for the whole --impl reference run")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
