@@ -65,7 +65,10 @@ struct Cfg {
     static constexpr int NCHUNK = DH / 64;          // 128-byte column chunks per row
     static constexpr int CHUNK_BYTES = BN * 128;
     static constexpr int TILE_BYTES = BN * DH * 2;
-    static constexpr int NSTAGE = CL == 2 ? 3 : 4;  // tiles in flight in shared memory
+    static constexpr int NSTAGE = 4;                // tiles in flight in shared memory
+    // exchange buffers (tiles of peer scores): one is enough, since the peer's next send overlaps
+    // this CTA's softmax, and the 32 KB it frees holds a fourth stage
+    static constexpr int NX = CL == 2 ? 1 : 0;
     static constexpr int NPROD_WARPS = CL == 2 ? 6 : 10;
     static constexpr int NPROD = NPROD_WARPS * 32;
     // TMEM columns (32-bit): O accumulator, two S buffers, Q (bf16 pairs)
@@ -78,7 +81,7 @@ struct Cfg {
     static constexpr int SM_KV = 0;
     static constexpr int SM_P = SM_KV + NSTAGE * TILE_BYTES;
     static constexpr int SM_X = SM_P + 2 * P_BYTES;
-    static constexpr int X_BYTES = CL == 2 ? 2 * 128 * BN * 4 : 0;
+    static constexpr int X_BYTES = NX * 128 * BN * 4;
     static constexpr int SM_LIST = SM_X + X_BYTES;
     static constexpr int LIST_BYTES = (LMAX + 16) * 4;
     static constexpr int SM_BAR = SM_LIST + LIST_BYTES;
@@ -87,6 +90,7 @@ struct Cfg {
     static_assert(Q_COL + DH / 2 <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SM_P % 1024 == 0 && P_BYTES % 1024 == 0, "swizzled operands are 1024-byte aligned");
+    static_assert(NSTAGE <= 6 && NX <= 2, "barrier slots");
 };
 
 // Producer index (0..NPROD_WARPS-1) of a gather warp, -1 for other warps.
@@ -101,23 +105,23 @@ __device__ __forceinline__ int prod_warp(int warp) {
 // barrier slots (8 bytes each) inside the SM_BAR block
 enum : int {
     B_FULL = 0,                 // [NSTAGE] producer -> consumers: tile landed
-    B_EMPTY = B_FULL + 4,       // [NSTAGE] MMA -> producer: stage free
-    B_SFULL = B_EMPTY + 4,      // [2] MMA -> softmax, exchange: S ready (or the end marker)
+    B_EMPTY = B_FULL + 6,       // [NSTAGE] MMA -> producer: stage free
+    B_SFULL = B_EMPTY + 6,      // [2] MMA -> softmax, exchange: S ready (or the end marker)
     B_SFREE = B_SFULL + 2,      // [2] softmax, exchange -> MMA: S buffer read
     B_PFULL = B_SFREE + 2,      // [2] softmax -> MMA: P written to shared memory
     B_PVDONE = B_PFULL + 2,     // [2] MMA -> softmax: P V done (P buffer and O free)
     B_QREADY = B_PVDONE + 2,    // softmax -> MMA: Q of the segment in TMEM
     B_OFREE = B_QREADY + 1,     // softmax -> MMA: epilogue has read O
-    B_XFULL = B_OFREE + 1,      // [2] peer -> me: peer's partial scores are in my exchange buffer
-    B_XFREE = B_XFULL + 2,      // [2] peer -> me: peer has read what I sent
+    B_XFULL = B_OFREE + 1,      // [NX] peer -> me: peer's partial scores are in my exchange buffer
+    B_XFREE = B_XFULL + 2,      // [NX] peer -> me: peer has read what I sent
     B_DRAIN = B_XFREE + 2,      // MMA drain on abort
     B_ZREAD = B_DRAIN + 1,      // softmax threads have read the meta of a tile without rows
     B_LFULL = B_ZREAD + 1,      // compaction -> producers: the segment's index list is ready
     B_LFREE = B_LFULL + 1,      // producers -> compaction: the list may be overwritten
     B_COUNT = B_LFREE + 1
 };
-constexpr int META_OFF = 8 * B_COUNT;      // [4] int2 {count, last}
-constexpr int TMEM_ADDR_OFF = META_OFF + 8 * 4;
+constexpr int META_OFF = 8 * B_COUNT;      // [NSTAGE] int2 {count, last}
+constexpr int TMEM_ADDR_OFF = META_OFF + 8 * 6;
 constexpr int ABORT_OFF = TMEM_ADDR_OFF + 4;
 constexpr int NVALID_OFF = ABORT_OFF + 4;
 constexpr int LOFF_OFF = NVALID_OFF + 4;
@@ -195,6 +199,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             mbar_init(BAR(B_SFREE + i), C::CL == 2 ? 8 : 4);   // one arrival per reading warp
             mbar_init(BAR(B_PFULL + i), 128);
             mbar_init(BAR(B_PVDONE + i), 1);
+        }
+        for (int i = 0; i < C::NX; ++i) {
             mbar_init(BAR(B_XFULL + i), 1);     // armed by the receiver; the peer's bytes complete it
             mbar_init(BAR(B_XFREE + i), 4);     // one arrival per softmax warp of the peer
         }
@@ -208,10 +214,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         *s_end = -1;
         fence_mbar_init();
         if constexpr (C::CL == 2) {
-            // the exchange buffers expect the peer's live score rows of tiles 0 and 1
+            // the exchange buffers expect the peer's live score rows of tiles 0 .. NX-1
             const uint32_t xbytes = (uint32_t)(p.h < 128 ? p.h : 128) * BN * 4;
-            mbar_arrive_expect_tx(BAR(B_XFULL + 0), xbytes);
-            mbar_arrive_expect_tx(BAR(B_XFULL + 1), xbytes);
+            for (int i = 0; i < C::NX; ++i) mbar_arrive_expect_tx(BAR(B_XFULL + i), xbytes);
         }
     }
     // rows a tile does not load keep finite values: zero every stage once
@@ -480,8 +485,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             const uint32_t ph = (J >> 1) & 1;
             if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) break;
             if (*s_end == J) break;
-            // the peer has read what this warp sent into the same buffer two tiles ago
-            if (!warp_wait<true>(BAR(B_XFREE + sb), ph ^ 1, abort_flag)) break;
+            // the peer has read what this warp sent into the same buffer NX tiles ago
+            const int xs = J % C::NX;
+            const uint32_t xph = (uint32_t)(J / C::NX) & 1u;
+            if (!warp_wait<true>(BAR(B_XFREE + xs), xph ^ 1, abort_flag)) break;
             tc_fence_after();
             uint32_t r0[32], r1[32];
             tmem_ld32(tmem + lane_off + C::S_COL + sb * BN, r0);
@@ -493,7 +500,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
             // rows of heads >= h are never read, so only live rows cross the cluster; each
             // asynchronous store counts its bytes on the peer's barrier (no fence needed)
-            const uint32_t rbuf = xpeer + sb * XSTRIDE, rbar = xfull_peer + 8u * sb;
+            const uint32_t rbuf = xpeer + xs * XSTRIDE, rbar = xfull_peer + 8u * xs;
             if (live) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
@@ -587,15 +594,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         s[32 + j] = __uint_as_float(r1[j]);
                     }
                     if constexpr (C::CL == 2) {
-                        if (!warp_wait<true>(BAR(B_XFULL + sb), ph, abort_flag)) {
+                        const int xs = J % C::NX;
+                        if (!warp_wait<true>(BAR(B_XFULL + xs), (uint32_t)(J / C::NX) & 1u, abort_flag)) {
                             ok = false;
                             break;
                         }
-                        // arm the buffer for tile J + 2 (its bytes cannot come before every softmax
-                        // warp has released tile J below)
+                        // arm the buffer for tile J + NX (its bytes cannot come before every
+                        // softmax warp has released tile J below)
                         if (t == 0)
-                            mbar_arrive_expect_tx(BAR(B_XFULL + sb), (uint32_t)(p.h < 128 ? p.h : 128) * BN * 4);
-                        const uint32_t xbuf = base + C::SM_X + sb * XSTRIDE;
+                            mbar_arrive_expect_tx(BAR(B_XFULL + xs), (uint32_t)(p.h < 128 ? p.h : 128) * BN * 4);
+                        const uint32_t xbuf = base + C::SM_X + xs * XSTRIDE;
                         if (live) {
 #pragma unroll
                             for (int k = 0; k < BN / 4; ++k) {
@@ -607,7 +615,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                             }
                         }
                         __syncwarp();   // every lane's loads have returned (their sums are taken)
-                        if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer + 8u * sb);
+                        if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer + 8u * xs);
                     }
                     const int cnt = cur.x;
                     if (cnt < BN) {
