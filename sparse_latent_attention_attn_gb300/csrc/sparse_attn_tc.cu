@@ -69,6 +69,10 @@ struct Cfg {
     // exchange buffers (tiles of peer scores): one is enough, since the peer's next send overlaps
     // this CTA's softmax, and the 32 KB it frees holds a fourth stage
     static constexpr int NX = CL == 2 ? 1 : 0;
+    static constexpr int NXD = NX > 0 ? NX : 1;     // divisor for buffer arithmetic
+    // P buffers: the softmax writes P of tile J into buffer J % NP without waiting, because the
+    // MMA thread issues S(J) only after P V of tile J - NP (so S(J)'s completion covers it)
+    static constexpr int NP = 3;
     static constexpr int NPROD_WARPS = CL == 2 ? 6 : 10;
     static constexpr int NPROD = NPROD_WARPS * 32;
     // TMEM columns (32-bit): O accumulator, two S buffers, Q (bf16 pairs)
@@ -80,7 +84,7 @@ struct Cfg {
     static constexpr int P_BYTES = 128 * BN * 2;    // one P tile, bf16, 128-byte rows
     static constexpr int SM_KV = 0;
     static constexpr int SM_P = SM_KV + NSTAGE * TILE_BYTES;
-    static constexpr int SM_X = SM_P + 2 * P_BYTES;
+    static constexpr int SM_X = SM_P + NP * P_BYTES;
     static constexpr int X_BYTES = NX * 128 * BN * 4;
     static constexpr int SM_LIST = SM_X + X_BYTES;
     static constexpr int LIST_BYTES = (LMAX + 16) * 4;
@@ -126,7 +130,8 @@ constexpr int ABORT_OFF = TMEM_ADDR_OFF + 4;
 constexpr int NVALID_OFF = ABORT_OFF + 4;
 constexpr int LOFF_OFF = NVALID_OFF + 4;
 constexpr int SEND_OFF = LOFF_OFF + 4;
-static_assert(SEND_OFF + 4 <= 512, "barrier block");
+constexpr int NVRING_OFF = SEND_OFF + 4;   // [8] valid entries of recent segments
+static_assert(NVRING_OFF + 32 <= 512, "barrier block");
 
 struct Params {
     const uint16_t *q;
@@ -179,6 +184,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     volatile int *seg_nvalid = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + NVALID_OFF);
     volatile int *seg_loff = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + LOFF_OFF);
     volatile int *s_end = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + SEND_OFF);
+    volatile int *nvring = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + NVRING_OFF);
     int32_t *list = reinterpret_cast<int32_t *>(sbase + C::SM_LIST);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -280,7 +286,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 __syncwarp();
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DS_DEV_BAD_INDEX);
-            if (lane == 0) *seg_nvalid = nvalid;
+            if (lane == 0) {
+                *seg_nvalid = nvalid;
+                nvring[seg & 7] = nvalid;   // for the softmax warps, which never read the list
+            }
             mbar_arrive(BAR(B_LFULL));          // every lane releases its own list stores
         }
     } else if (pw >= 0) {
@@ -373,7 +382,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                             first = true;
                             s_more = tok * T < e1;
                             progressed = true;
-                        } else if (mbar_test_wait(BAR(B_SFREE + (J & 1)), ((J >> 1) & 1) ^ 1) &&
+                        } else if (pq_head >= J - C::NP + 1 &&
+                                   mbar_test_wait(BAR(B_SFREE + (J & 1)), ((J >> 1) & 1) ^ 1) &&
                                    (!first || mbar_test_wait(BAR(B_QREADY), seg & 1))) {
                             // the rows were written by cp.async (generic proxy); the MMA reads them
                             // through the async proxy
@@ -416,7 +426,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         (!pq_first[q] || pq_seg[q] == 0 || mbar_test_wait(BAR(B_OFREE), (pq_seg[q] - 1) & 1))) {
                         // P was written by st.shared (generic proxy) and fenced by its writers
                         tc_fence_after();
-                        const uint32_t pbase = base + C::SM_P + (Jp & 1) * C::P_BYTES;
+                        const uint32_t pbase = base + C::SM_P + (Jp % C::NP) * C::P_BYTES;
                         const uint32_t vbase = base + C::SM_KV + pq_stage[q] * C::TILE_BYTES;
 #pragma unroll
                         for (int k = 0; k < BN / 16; ++k) {
@@ -486,8 +496,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) break;
             if (*s_end == J) break;
             // the peer has read what this warp sent into the same buffer NX tiles ago
-            const int xs = J % C::NX;
-            const uint32_t xph = (uint32_t)(J / C::NX) & 1u;
+            const int xs = J % C::NXD;
+            const uint32_t xph = (uint32_t)(J / C::NXD) & 1u;
             if (!warp_wait<true>(BAR(B_XFREE + xs), xph ^ 1, abort_flag)) break;
             tc_fence_after();
             uint32_t r0[32], r1[32];
@@ -543,22 +553,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             tc_fence_before();
             mbar_arrive(BAR(B_QREADY));
         };
-        int it = 0, J = 0, nzero = 0;
+        int it = 0, J = 0, nzero = 0, seg = 0;
         bool ok = true;
         if (has_work) load_q(tok_begin);
-        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
+        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok, ++seg) {
             const int a = (int)((e0 > tok * T ? e0 : tok * T) - tok * T);
             const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
             float m_used = -INFINITY, l = 0.0f;
             bool any = false;
+            // the segment's first tile has landed, so its valid-entry count is published; the
+            // later tiles need no wait here (their scores come after their rows)
             if (!warp_wait(BAR(B_FULL + it % NSTAGE), (it / NSTAGE) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
-            int2 cur = meta[it % NSTAGE];
-            if (cur.x == 0) {
+            const int nv = nvring[seg & 7];
+            if (nv == 0) {
                 // a segment without a single valid row: its only tile loads nothing; once all
-                // 128 threads and the MMA thread have read its meta, thread 0 hands the stage back
+                // 128 threads and the MMA thread have seen it, thread 0 hands the stage back
                 mbar_arrive(BAR(B_ZREAD));
                 if (t == 0) {
                     if (!mbar_wait(BAR(B_ZREAD), nzero & 1, abort_flag, kWaitLimitNs)) ok = false;
@@ -569,7 +581,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
             } else {
-                for (;;) {
+                for (int tile = 0;; ++tile) {
                     // tile J: own scores from TMEM (+ the peer's partial scores) -> online softmax
                     // -> P (bf16) into shared memory
                     const int sb = J & 1;
@@ -594,8 +606,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         s[32 + j] = __uint_as_float(r1[j]);
                     }
                     if constexpr (C::CL == 2) {
-                        const int xs = J % C::NX;
-                        if (!warp_wait<true>(BAR(B_XFULL + xs), (uint32_t)(J / C::NX) & 1u, abort_flag)) {
+                        const int xs = J % C::NXD;
+                        if (!warp_wait<true>(BAR(B_XFULL + xs), (uint32_t)(J / C::NXD) & 1u, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -617,7 +629,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         __syncwarp();   // every lane's loads have returned (their sums are taken)
                         if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer + 8u * xs);
                     }
-                    const int cnt = cur.x;
+                    const int cnt = nv - tile * BN < BN ? nv - tile * BN : BN;
                     if (cnt < BN) {
 #pragma unroll
                         for (int j = 0; j < BN; ++j)
@@ -671,13 +683,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         pk[j] = pack_bf16x2(p0, p1);
                     }
                     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    // the P buffer is free once the P V of two tiles ago is done
-                    if (J >= 2 && !warp_wait(BAR(B_PVDONE + sb), ph ^ 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    // row t of P, 16-byte unit u at unit u ^ (t % 8) of its 128-byte row
-                    const uint32_t prow = base + C::SM_P + sb * C::P_BYTES + t * 128;
+                    // row t of P, 16-byte unit u at unit u ^ (t % 8) of its 128-byte row; the buffer
+                    // is free: S(J) was issued after the P V of tile J - NP, and S(J) is complete
+                    const uint32_t prow = base + C::SM_P + (J % C::NP) * C::P_BYTES + t * 128;
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
                         st_shared_v4(prow + ((u ^ (t & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
@@ -685,19 +693,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     mbar_arrive(BAR(B_PFULL + sb));
                     ++J;
                     ++it;
-                    if (cur.y) break;
-                    if (!warp_wait(BAR(B_FULL + it % NSTAGE), (it / NSTAGE) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    cur = meta[it % NSTAGE];
+                    if ((tile + 1) * BN >= nv) break;
                 }
                 if (!ok) break;
             }
             // every S of this segment has been read, so the next token's Q may replace this one
             if ((tok + 1) * T < e1) load_q(tok + 1);
             if (any) {
+                // O is final once the segment's last P V is done.  A parity wait is only exact
+                // when the previous completion of the same barrier has happened, so wait for the
+                // P V before the last first (its own predecessor, three tiles back, is done:
+                // S of the current tile came after it), then for the last one.
                 const int Jl = J - 1;
+                if (Jl >= 1 && !warp_wait(BAR(B_PVDONE + ((Jl - 1) & 1)), ((Jl - 1) >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 if (!warp_wait(BAR(B_PVDONE + (Jl & 1)), (Jl >> 1) & 1, abort_flag)) {
                     ok = false;
                     break;
