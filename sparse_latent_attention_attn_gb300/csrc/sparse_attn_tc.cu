@@ -66,13 +66,16 @@ struct Cfg {
     static constexpr int CHUNK_BYTES = BN * 128;
     static constexpr int TILE_BYTES = BN * DH * 2;
     static constexpr int NSTAGE = 4;                // tiles in flight in shared memory
-    // exchange buffers (tiles of peer scores): one is enough, since the peer's next send overlaps
-    // this CTA's softmax, and the 32 KB it frees holds a fourth stage
-    static constexpr int NX = CL == 2 ? 1 : 0;
+    // exchange buffers (tiles of the peer's partial scores).  With the d split, P of tile J is
+    // written into exchange buffer J % NX once its scores have been read, and the peer may send
+    // tile J + NX there once this CTA's P V of tile J is done.
+    static constexpr int NX = CL == 2 ? 2 : 0;
     static constexpr int NXD = NX > 0 ? NX : 1;     // divisor for buffer arithmetic
-    // P buffers: the softmax writes P of tile J into buffer J % NP without waiting, because the
-    // MMA thread issues S(J) only after P V of tile J - NP (so S(J)'s completion covers it)
-    static constexpr int NP = 3;
+    // separate P buffers (no d split): the softmax writes P of tile J into buffer J % NP without
+    // waiting, because the MMA thread issues S(J) only after P V of tile J - NP (so S(J)'s
+    // completion covers it)
+    static constexpr int NP = CL == 2 ? 0 : 3;
+    static constexpr int NPD = NP > 0 ? NP : 1;
     static constexpr int NPROD_WARPS = CL == 2 ? 6 : 10;
     static constexpr int NPROD = NPROD_WARPS * 32;
     // TMEM columns (32-bit): O accumulator, two S buffers, Q (bf16 pairs)
@@ -85,7 +88,12 @@ struct Cfg {
     static constexpr int SM_KV = 0;
     static constexpr int SM_P = SM_KV + NSTAGE * TILE_BYTES;
     static constexpr int SM_X = SM_P + NP * P_BYTES;
-    static constexpr int X_BYTES = NX * 128 * BN * 4;
+    static constexpr int X_STRIDE = 128 * BN * 4;   // one exchange buffer
+    // shared address of P of tile J (relative to the 1024-aligned base)
+    __device__ static uint32_t p_off(int J) {
+        return NX > 0 ? (uint32_t)(SM_X + (J % NXD) * X_STRIDE) : (uint32_t)(SM_P + (J % NPD) * P_BYTES);
+    }
+    static constexpr int X_BYTES = NX * X_STRIDE;
     static constexpr int SM_LIST = SM_X + X_BYTES;
     static constexpr int LIST_BYTES = (LMAX + 16) * 4;
     static constexpr int SM_BAR = SM_LIST + LIST_BYTES;
@@ -94,7 +102,7 @@ struct Cfg {
     static_assert(Q_COL + DH / 2 <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SM_P % 1024 == 0 && P_BYTES % 1024 == 0, "swizzled operands are 1024-byte aligned");
-    static_assert(NSTAGE <= 6 && NX <= 2, "barrier slots");
+    static_assert(NSTAGE <= 6 && NX <= 3, "barrier slots");
 };
 
 // Producer index (0..NPROD_WARPS-1) of a gather warp, -1 for other warps.
@@ -113,12 +121,12 @@ enum : int {
     B_SFULL = B_EMPTY + 6,      // [2] MMA -> softmax, exchange: S ready (or the end marker)
     B_SFREE = B_SFULL + 2,      // [2] softmax, exchange -> MMA: S buffer read
     B_PFULL = B_SFREE + 2,      // [2] softmax -> MMA: P written to shared memory
-    B_PVDONE = B_PFULL + 2,     // [2] MMA -> softmax: P V done (P buffer and O free)
-    B_QREADY = B_PVDONE + 2,    // softmax -> MMA: Q of the segment in TMEM
+    B_PVDONE = B_PFULL + 2,     // [4] MMA -> softmax, exchange: P V of tile J done (slot J % 4)
+    B_QREADY = B_PVDONE + 4,    // softmax -> MMA: Q of the segment in TMEM
     B_OFREE = B_QREADY + 1,     // softmax -> MMA: epilogue has read O
     B_XFULL = B_OFREE + 1,      // [NX] peer -> me: peer's partial scores are in my exchange buffer
-    B_XFREE = B_XFULL + 2,      // [NX] peer -> me: peer has read what I sent
-    B_DRAIN = B_XFREE + 2,      // MMA drain on abort
+    B_XFREE = B_XFULL + 3,      // [NX] peer -> me: the peer's buffer for my next send is free
+    B_DRAIN = B_XFREE + 3,      // MMA drain on abort
     B_ZREAD = B_DRAIN + 1,      // softmax threads have read the meta of a tile without rows
     B_LFULL = B_ZREAD + 1,      // compaction -> producers: the segment's index list is ready
     B_LFREE = B_LFULL + 1,      // producers -> compaction: the list may be overwritten
@@ -204,12 +212,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             mbar_init(BAR(B_SFULL + i), 1);
             mbar_init(BAR(B_SFREE + i), C::CL == 2 ? 8 : 4);   // one arrival per reading warp
             mbar_init(BAR(B_PFULL + i), 128);
-            mbar_init(BAR(B_PVDONE + i), 1);
+
         }
         for (int i = 0; i < C::NX; ++i) {
             mbar_init(BAR(B_XFULL + i), 1);     // armed by the receiver; the peer's bytes complete it
-            mbar_init(BAR(B_XFREE + i), 4);     // one arrival per softmax warp of the peer
+            mbar_init(BAR(B_XFREE + i), 4);     // one arrival per exchange warp of the peer
         }
+        for (int i = 0; i < 4; ++i) mbar_init(BAR(B_PVDONE + i), 1);
         mbar_init(BAR(B_QREADY), 128);
         mbar_init(BAR(B_OFREE), 128);
         mbar_init(BAR(B_DRAIN), 1);
@@ -382,7 +391,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                             first = true;
                             s_more = tok * T < e1;
                             progressed = true;
-                        } else if (pq_head >= J - C::NP + 1 &&
+                        } else if ((C::NP == 0 || pq_head >= J - C::NP + 1) &&
                                    mbar_test_wait(BAR(B_SFREE + (J & 1)), ((J >> 1) & 1) ^ 1) &&
                                    (!first || mbar_test_wait(BAR(B_QREADY), seg & 1))) {
                             // the rows were written by cp.async (generic proxy); the MMA reads them
@@ -426,7 +435,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         (!pq_first[q] || pq_seg[q] == 0 || mbar_test_wait(BAR(B_OFREE), (pq_seg[q] - 1) & 1))) {
                         // P was written by st.shared (generic proxy) and fenced by its writers
                         tc_fence_after();
-                        const uint32_t pbase = base + C::SM_P + (Jp % C::NP) * C::P_BYTES;
+                        const uint32_t pbase = base + C::p_off(Jp);
                         const uint32_t vbase = base + C::SM_KV + pq_stage[q] * C::TILE_BYTES;
 #pragma unroll
                         for (int k = 0; k < BN / 16; ++k) {
@@ -438,7 +447,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                             mma_bf16_ss(tmem + C::O_COL, adesc, bdesc, IDESC_PV, (pq_first[q] && k == 0) ? 0u : 1u);
                         }
                         mma_commit(BAR(B_EMPTY + pq_stage[q]));
-                        mma_commit(BAR(B_PVDONE + (Jp & 1)));
+                        mma_commit(BAR(B_PVDONE + (Jp & 3)));
                         ++pq_head;
                         progressed = true;
                     }
@@ -487,17 +496,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         const int t = quarter * 32 + lane;               // head row = TMEM lane
         const bool live = t < p.h;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        constexpr uint32_t XSTRIDE = 128 * BN * 4;       // one exchange buffer
+        constexpr uint32_t XSTRIDE = C::X_STRIDE;
         const uint32_t xpeer = mapa(base + C::SM_X, peer);
         const uint32_t xfull_peer = mapa(BAR(B_XFULL), peer);   // counts the bytes of each store
+        const uint32_t xfree_peer = mapa(BAR(B_XFREE), peer);
         for (int J = 0; has_work; ++J) {
             const int sb = J & 1;
             const uint32_t ph = (J >> 1) & 1;
-            if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) break;
-            if (*s_end == J) break;
-            // the peer has read what this warp sent into the same buffer NX tiles ago
             const int xs = J % C::NXD;
             const uint32_t xph = (uint32_t)(J / C::NXD) & 1u;
+            if (J >= C::NX) {
+                // this CTA's P V of tile J - NX is done, so the exchange buffer that held its P may
+                // take the peer's scores of tile J (the P V four tiles earlier on the same barrier
+                // was waited for at tile J - 4, so this parity wait is exact)
+                const int Jo = J - C::NX;
+                if (!warp_wait(BAR(B_PVDONE + (Jo & 3)), (Jo >> 2) & 1, abort_flag)) break;
+                if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer + 8u * xs);
+            }
+            if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) break;
+            if (*s_end == J) break;
+            // the peer's exchange buffer for tile J is free (its P V of tile J - NX is done)
             if (!warp_wait<true>(BAR(B_XFREE + xs), xph ^ 1, abort_flag)) break;
             tc_fence_after();
             uint32_t r0[32], r1[32];
@@ -530,9 +548,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const bool live = t < p.h;
         const float sink2 = live ? p.sink[t] * kLog2e : 0.0f;
-        constexpr uint32_t XSTRIDE = 128 * BN * 4;       // one exchange buffer
-        uint32_t xfree_peer = 0;
-        if constexpr (C::CL == 2) xfree_peer = mapa(BAR(B_XFREE), peer);
+        constexpr uint32_t XSTRIDE = C::X_STRIDE;
         auto load_q = [&](int64_t tok) {
             // this CTA's DH columns of q[tok][t] into TMEM columns [Q_COL, Q_COL + DH/2) of lane t
             const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (tok * p.h + t) * (int64_t)D + crank * C::DH);
@@ -626,8 +642,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                                 s[4 * k + 3] += v.w;
                             }
                         }
-                        __syncwarp();   // every lane's loads have returned (their sums are taken)
-                        if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer + 8u * xs);
+                        // the exchange warps tell the peer when this buffer is free again (after
+                        // the P V of this tile, whose P is written here below)
                     }
                     const int cnt = nv - tile * BN < BN ? nv - tile * BN : BN;
                     if (cnt < BN) {
@@ -650,7 +666,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     } else if (__any_sync(0xffffffffu, tmax > m_used + kRescaleThreshold)) {
                         // move the running max: wait for the P V in flight, rescale O and l
                         const int Jp = J - 1;
-                        if (!warp_wait(BAR(B_PVDONE + (Jp & 1)), (Jp >> 1) & 1, abort_flag)) {
+                        if (!warp_wait(BAR(B_PVDONE + (Jp & 3)), (Jp >> 2) & 1, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -683,9 +699,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         pk[j] = pack_bf16x2(p0, p1);
                     }
                     l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    // row t of P, 16-byte unit u at unit u ^ (t % 8) of its 128-byte row; the buffer
-                    // is free: S(J) was issued after the P V of tile J - NP, and S(J) is complete
-                    const uint32_t prow = base + C::SM_P + (J % C::NP) * C::P_BYTES + t * 128;
+                    // row t of P, 16-byte unit u at unit u ^ (t % 8) of its 128-byte row.  With the d
+                    // split P goes into this tile's exchange buffer, once all four warps have read
+                    // the peer's scores from it; otherwise the buffer is free because S(J) was
+                    // issued after the P V of tile J - NP and S(J) is complete.
+                    if constexpr (C::CL == 2) named_bar_sync(1, 128);
+                    const uint32_t prow = base + C::p_off(J) + t * 128;
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
                         st_shared_v4(prow + ((u ^ (t & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
@@ -701,15 +720,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             if ((tok + 1) * T < e1) load_q(tok + 1);
             if (any) {
                 // O is final once the segment's last P V is done.  A parity wait is only exact
-                // when the previous completion of the same barrier has happened, so wait for the
-                // P V before the last first (its own predecessor, three tiles back, is done:
-                // S of the current tile came after it), then for the last one.
+                // when the previous completion of the same barrier (four tiles back) has happened,
+                // so wait for the P V before the last first (its predecessor is done: the scores
+                // or peer scores of the last tile came after it), then for the last one.
                 const int Jl = J - 1;
-                if (Jl >= 1 && !warp_wait(BAR(B_PVDONE + ((Jl - 1) & 1)), ((Jl - 1) >> 1) & 1, abort_flag)) {
+                if (Jl >= 1 && !warp_wait(BAR(B_PVDONE + ((Jl - 1) & 3)), ((Jl - 1) >> 2) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                if (!warp_wait(BAR(B_PVDONE + (Jl & 1)), (Jl >> 1) & 1, abort_flag)) {
+                if (!warp_wait(BAR(B_PVDONE + (Jl & 3)), (Jl >> 2) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
