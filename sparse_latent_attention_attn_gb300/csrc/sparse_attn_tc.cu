@@ -234,6 +234,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             for (int i = 0; i < C::NX; ++i) mbar_arrive_expect_tx(BAR(B_XFULL + i), xbytes);
         }
     }
+    // the combine kernel may be scheduled as soon as SMs free up (it waits for this grid itself)
+    if (threadIdx.x == 0) grid_launch_dependents();
     // rows a tile does not load keep finite values: zero every stage once
     for (int i = threadIdx.x; i < NSTAGE * C::TILE_BYTES / 16; i += NTHREADS)
         reinterpret_cast<uint4 *>(sbase + C::SM_KV)[i] = make_uint4(0, 0, 0, 0);
@@ -246,6 +248,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sbase + C::SM_BAR + TMEM_ADDR_OFF);
+    // everything above overlaps the previous kernel on the stream (launched as a programmatic
+    // dependent); from here on the inputs it may have written are read, and outputs written
+    grid_dependency_wait();
     // warpgroups 1-3 give registers back to the softmax warpgroup before they branch
     if (warp >= 4) setmaxnreg_dec<REG_OTHER>();
 
@@ -813,58 +818,64 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
 }
 
 // Merge the partials of every token that a range boundary cut, add the sink once, write bf16.
-// Block (c - 1, y) owns heads 8y..8y+7 of the token holding boundary e(c) when that boundary
-// falls inside a token and no earlier boundary falls inside the same token; one warp per head,
-// each lane holding D/32 consecutive-by-vector elements of the row.
+// The host lists the cut tokens: token, first part (cluster), number of parts and, per part, the
+// partial slot it wrote (0: the part's first segment, 1: its last).  Block (i, y) merges heads
+// 8y..8y+7 of cut token i, one warp per head: lane j first reads part j's running max and sum,
+// the warp reduces them, then every lane accumulates its D/32 elements over the parts.
 constexpr int kCombineHeadsPerBlock = 8;
+constexpr int kMaxCut = 160;      // cut tokens: at most one per range boundary, G <= SM count
+
+struct CombineParams {
+    const float *sink;
+    const float *ws;
+    uint16_t *o;
+    int h;
+    int ncut;
+    float pad_;
+    int4 cut[kMaxCut];            // {token, first part, parts, slot bits}
+};
 
 template <int D>
-__global__ void __launch_bounds__(32 * kCombineHeadsPerBlock) sparse_attn_combine_kernel(const Params p) {
-    const int c = blockIdx.x + 1;
+__global__ void __launch_bounds__(32 * kCombineHeadsPerBlock) sparse_attn_combine_kernel(const CombineParams cp) {
+    grid_dependency_wait();   // launched as a programmatic dependent of the attention kernel
     const int hh = blockIdx.y * kCombineHeadsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (hh >= p.h) return;
-    const int64_t T = p.topk;
-    const int64_t eb = range_start(c, p.E, p.G);
-    if (eb % T == 0 || eb >= p.E) return;
-    const int64_t tok = eb / T;
-    const int64_t ts = tok * T, te = ts + T;
-    // the earlier boundary inside this token (if any) owns it
-    const int64_t ep = range_start(c - 1, p.E, p.G);
-    if (c > 1 && ep > ts && ep % T != 0) return;
-    // clusters whose ranges meet the token: first = the one containing ts
-    int64_t cf = c - 1;
-    while (cf > 0 && range_start(cf, p.E, p.G) > ts) --cf;
+    if (hh >= cp.h || (int)blockIdx.x >= cp.ncut) return;
+    const int4 c = cp.cut[blockIdx.x];
+    const int64_t tok = c.x;
+    const int kf = c.y, np = c.z;
+    const uint32_t slots = (uint32_t)c.w;
     constexpr size_t SLOT = (size_t)SLOT_HEADS * D + 2 * SLOT_HEADS;
     constexpr int PER = D / 32;                 // elements per lane
     constexpr int VW = PER >= 4 ? 4 : PER;      // floats per vector load
     constexpr int NV = PER / VW;                // vector loads per lane per partial
     static_assert(PER % VW == 0 && (VW == 2 || VW == 4), "combine vector width");
-
-    const float sink2 = p.sink[hh] * kLog2e;
-    float top = sink2;
-    for (int64_t k = cf; k < p.G; ++k) {
-        const int64_t r0 = range_start(k, p.E, p.G), r1 = range_start(k + 1, p.E, p.G);
-        if (r0 >= te) break;
-        if (r1 <= r0 || r1 <= ts) continue;
-        const int slot = (r0 / T == tok) ? 0 : 1;
-        top = fmaxf(top, p.ws[((size_t)k * 2 + slot) * SLOT + SLOT_HEADS * D + hh]);
+    auto part = [&](int i) -> const float * {
+        return cp.ws + ((size_t)(kf + i) * 2 + ((slots >> i) & 1u)) * SLOT;
+    };
+    // running maxima and sums of the parts, one part per lane (np <= 32)
+    float mi = -INFINITY, li = 0.0f;
+    if (lane < np) {
+        const float *ws = part(lane);
+        mi = ws[SLOT_HEADS * D + hh];
+        li = ws[SLOT_HEADS * D + SLOT_HEADS + hh];
     }
-    float den = exp2f(sink2 - top);
+    const float sink2 = cp.sink[hh] * kLog2e;
+    float top = fmaxf(mi, sink2);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, off));
+    const float wi = (lane < np && mi != -INFINITY) ? exp2f(mi - top) : 0.0f;
+    float den = wi * li;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    den += exp2f(sink2 - top);
     float acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.0f;
-    for (int64_t k = cf; k < p.G; ++k) {
-        const int64_t r0 = range_start(k, p.E, p.G), r1 = range_start(k + 1, p.E, p.G);
-        if (r0 >= te) break;
-        if (r1 <= r0 || r1 <= ts) continue;
-        const int slot = (r0 / T == tok) ? 0 : 1;
-        const float *ws = p.ws + ((size_t)k * 2 + slot) * SLOT;
-        const float mk = ws[SLOT_HEADS * D + hh];
-        if (mk == -INFINITY) continue;
-        const float w = exp2f(mk - top);
-        den += w * ws[SLOT_HEADS * D + SLOT_HEADS + hh];
-        const float *orow = ws + (size_t)hh * D;
+    for (int i = 0; i < np; ++i) {
+        const float w = __shfl_sync(0xffffffffu, wi, i);
+        if (w == 0.0f) continue;
+        const float *orow = part(i) + (size_t)hh * D;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             if constexpr (VW == 4) {
@@ -881,7 +892,7 @@ __global__ void __launch_bounds__(32 * kCombineHeadsPerBlock) sparse_attn_combin
         }
     }
     const float inv = 1.0f / den;
-    uint16_t *dst = p.o + (tok * p.h + hh) * (int64_t)D;
+    uint16_t *dst = cp.o + (tok * cp.h + hh) * (int64_t)D;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         if constexpr (VW == 4) {
@@ -892,6 +903,36 @@ __global__ void __launch_bounds__(32 * kCombineHeadsPerBlock) sparse_attn_combin
             reinterpret_cast<uint32_t *>(dst)[v * 32 + lane] = pack_bf16x2(acc[2 * v] * inv, acc[2 * v + 1] * inv);
         }
     }
+}
+
+// The cut tokens of a launch (host): every token that some range boundary falls inside.
+// Returns the number of entries written to cut (at most kMaxCut), or -1 when a token has more
+// than 32 parts or there are too many cut tokens.
+int cut_tokens(int64_t E, int64_t T, int64_t G, int4 *cut) {
+    int n = 0;
+    int64_t last_tok = -1;
+    for (int64_t c = 1; c < G; ++c) {
+        const int64_t eb = range_start(c, E, G);
+        if (eb % T == 0 || eb >= E) continue;
+        const int64_t tok = eb / T;
+        if (tok == last_tok) continue;               // already listed through an earlier boundary
+        last_tok = tok;
+        // parts: clusters whose ranges meet [tok T, tok T + T)
+        int64_t kf = c - 1;
+        while (kf > 0 && range_start(kf, E, G) > tok * T) --kf;
+        int np = 0;
+        uint32_t slots = 0;
+        for (int64_t k = kf; k < G && range_start(k, E, G) < (tok + 1) * T; ++k) {
+            if (range_start(k + 1, E, G) <= range_start(k, E, G)) continue;   // empty range
+            if (np >= 32) return -1;
+            if (range_start(k, E, G) / T != tok) slots |= 1u << np;          // token is k's last segment
+            if (np == 0) kf = k;
+            ++np;
+        }
+        if (n >= kMaxCut) return -1;
+        cut[n++] = make_int4((int)tok, (int)kf, np, (int)slots);
+    }
+    return n;
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -1008,18 +1049,34 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     cfg.blockDim = dim3(NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C::CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the kernel's set-up overlaps the previous kernel on the
+    // stream; it waits for that kernel (griddepcontrol.wait) before touching global memory
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = C::CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = C::CL > 1 ? 1 : 0;
+    cfg.numAttrs = C::CL > 1 ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D>, p) != cudaSuccess) return DS_ECUDA;
     if (split) {
-        const dim3 grid((unsigned)(G - 1), (unsigned)((a.h + kCombineHeadsPerBlock - 1) / kCombineHeadsPerBlock));
-        sparse_attn_combine_kernel<D><<<grid, 32 * kCombineHeadsPerBlock, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return DS_ECUDA;
+        CombineParams cpar;
+        cpar.sink = a.sink;
+        cpar.ws = static_cast<const float *>(a.workspace);
+        cpar.o = a.o;
+        cpar.h = a.h;
+        cpar.pad_ = 0.0f;
+        cpar.ncut = cut_tokens(p.E, a.topk, G, cpar.cut);
+        if (cpar.ncut <= 0) return DS_EUNSUPPORTED;
+        cudaLaunchConfig_t ccfg = {};
+        ccfg.gridDim = dim3((unsigned)cpar.ncut, (unsigned)((a.h + kCombineHeadsPerBlock - 1) / kCombineHeadsPerBlock), 1);
+        ccfg.blockDim = dim3(32 * kCombineHeadsPerBlock, 1, 1);
+        ccfg.stream = stream;
+        ccfg.attrs = attr;   // programmatic serialization only
+        ccfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&ccfg, sparse_attn_combine_kernel<D>, cpar) != cudaSuccess) return DS_ECUDA;
     }
     return DS_OK;
 }
