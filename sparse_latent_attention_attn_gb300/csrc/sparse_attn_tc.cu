@@ -45,7 +45,10 @@ using namespace ptx;
 
 constexpr int BN = 64;            // gathered rows per tile: N of Q K^T, K of P V
 constexpr int PREFETCH = 4;       // tiles further ahead whose rows are pulled into L2
-constexpr int LMAX = 4096;        // largest index row handled (entries of one token)
+// compacted indices travel from the compaction warp to the gather warps through a ring of LR
+// tiles of BN entries: the tile being gathered, the PREFETCH tiles whose rows go to L2 ahead of
+// it, and one being filled
+constexpr int LR = PREFETCH + 2;
 constexpr int NTHREADS = 512;     // 16 warps = 4 warpgroups
 constexpr int W_XCH0 = 8;         // warps 8-11: score exchange (split d) or row gather
 constexpr int W_LIST = 12;        // index compaction
@@ -65,7 +68,7 @@ struct Cfg {
     static constexpr int NCHUNK = DH / 64;          // 128-byte column chunks per row
     static constexpr int CHUNK_BYTES = BN * 128;
     static constexpr int TILE_BYTES = BN * DH * 2;
-    static constexpr int NSTAGE = 4;                // tiles in flight in shared memory
+    static constexpr int NSTAGE = 5;                // tiles in flight in shared memory
     // exchange buffers (tiles of the peer's partial scores).  With the d split, P of tile J is
     // written into exchange buffer J % NX once its scores have been read, and the peer may send
     // tile J + NX there once this CTA's P V of tile J is done.
@@ -95,14 +98,14 @@ struct Cfg {
     }
     static constexpr int X_BYTES = NX * X_STRIDE;
     static constexpr int SM_LIST = SM_X + X_BYTES;
-    static constexpr int LIST_BYTES = (LMAX + 16) * 4;
+    static constexpr int LIST_BYTES = LR * BN * 4;  // the index ring
     static constexpr int SM_BAR = SM_LIST + LIST_BYTES;
     static constexpr int SM_END = SM_BAR + 512;
     static constexpr int SMEM_BYTES = SM_END + 1024;
     static_assert(Q_COL + DH / 2 <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SM_P % 1024 == 0 && P_BYTES % 1024 == 0, "swizzled operands are 1024-byte aligned");
-    static_assert(NSTAGE <= 6 && NX <= 3, "barrier slots");
+    static_assert(NSTAGE <= 5 && NX <= 3, "barrier slots");
 };
 
 // Producer index (0..NPROD_WARPS-1) of a gather warp, -1 for other warps.
@@ -117,8 +120,8 @@ __device__ __forceinline__ int prod_warp(int warp) {
 // barrier slots (8 bytes each) inside the SM_BAR block
 enum : int {
     B_FULL = 0,                 // [NSTAGE] producer -> consumers: tile landed
-    B_EMPTY = B_FULL + 6,       // [NSTAGE] MMA -> producer: stage free
-    B_SFULL = B_EMPTY + 6,      // [2] MMA -> softmax, exchange: S ready (or the end marker)
+    B_EMPTY = B_FULL + 5,       // [NSTAGE] MMA -> producer: stage free
+    B_SFULL = B_EMPTY + 5,      // [2] MMA -> softmax, exchange: S ready (or the end marker)
     B_SFREE = B_SFULL + 2,      // [2] softmax, exchange -> MMA: S buffer read
     B_PFULL = B_SFREE + 2,      // [2] softmax -> MMA: P written to shared memory
     B_PVDONE = B_PFULL + 2,     // [4] MMA -> softmax, exchange: P V of tile J done (slot J % 4)
@@ -128,18 +131,16 @@ enum : int {
     B_XFREE = B_XFULL + 3,      // [NX] peer -> me: the peer's buffer for my next send is free
     B_DRAIN = B_XFREE + 3,      // MMA drain on abort
     B_ZREAD = B_DRAIN + 1,      // softmax threads have read the meta of a tile without rows
-    B_LFULL = B_ZREAD + 1,      // compaction -> producers: the segment's index list is ready
-    B_LFREE = B_LFULL + 1,      // producers -> compaction: the list may be overwritten
-    B_COUNT = B_LFREE + 1
+    B_LTFULL = B_ZREAD + 1,     // [LR] compaction -> producers: index ring tile written
+    B_LTFREE = B_LTFULL + LR,   // [LR] producers -> compaction: index ring tile consumed
+    B_COUNT = B_LTFREE + LR
 };
 constexpr int META_OFF = 8 * B_COUNT;      // [NSTAGE] int2 {count, last}
-constexpr int TMEM_ADDR_OFF = META_OFF + 8 * 6;
+constexpr int LMETA_OFF = (META_OFF + 8 * 5 + 15) & ~15;   // [LR] int4 {count, last, sequence, 0}
+constexpr int TMEM_ADDR_OFF = LMETA_OFF + 16 * LR;
 constexpr int ABORT_OFF = TMEM_ADDR_OFF + 4;
-constexpr int NVALID_OFF = ABORT_OFF + 4;
-constexpr int LOFF_OFF = NVALID_OFF + 4;
-constexpr int SEND_OFF = LOFF_OFF + 4;
-constexpr int NVRING_OFF = SEND_OFF + 4;   // [8] valid entries of recent segments
-static_assert(NVRING_OFF + 32 <= 512, "barrier block");
+constexpr int SEND_OFF = ABORT_OFF + 4;
+static_assert(SEND_OFF + 4 <= 512, "barrier block");
 
 struct Params {
     const uint16_t *q;
@@ -189,10 +190,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
     int2 *meta = reinterpret_cast<int2 *>(sbase + C::SM_BAR + META_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + ABORT_OFF);
-    volatile int *seg_nvalid = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + NVALID_OFF);
-    volatile int *seg_loff = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + LOFF_OFF);
     volatile int *s_end = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + SEND_OFF);
-    volatile int *nvring = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + NVRING_OFF);
+    int4 *lmeta = reinterpret_cast<int4 *>(sbase + C::SM_BAR + LMETA_OFF);
     int32_t *list = reinterpret_cast<int32_t *>(sbase + C::SM_LIST);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -223,8 +222,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         mbar_init(BAR(B_OFREE), 128);
         mbar_init(BAR(B_DRAIN), 1);
         mbar_init(BAR(B_ZREAD), 128 + 1);     // softmax threads + the MMA thread
-        mbar_init(BAR(B_LFULL), 32);
-        mbar_init(BAR(B_LFREE), C::NPROD_WARPS);
+        for (int i = 0; i < LR; ++i) {
+            mbar_init(BAR(B_LTFULL + i), 32);                // every compaction lane's writes
+            mbar_init(BAR(B_LTFREE + i), C::NPROD_WARPS);    // one arrival per gather warp
+        }
         *abort_flag = 0;
         *s_end = -1;
         fence_mbar_init();
@@ -259,106 +260,145 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     const int pw = prod_warp<D>(warp);
 
     if (warp == W_LIST) {
-        // ======================== index compaction: one list per segment ========================
-        int seg = 0;
-        for (int64_t tok = tok_begin; has_work && tok * T < e1; ++tok, ++seg) {
+        // ======================= index compaction into the ring of tiles =======================
+        // The index row of each segment is read 256 entries at a time (8 per lane, coalesced, the
+        // next batch in flight while this one is compacted); valid entries go in order into ring
+        // tiles of BN.  A full tile is published only once the next valid entry (or the segment's
+        // end) shows whether it is the segment's last; a segment without valid entries publishes
+        // one empty tile.
+        int lt = 0;              // ring tiles published so far (= the gather warps' tile counter)
+        int fill = 0;            // entries in the tile being filled
+        bool ok = true;
+        auto acquire = [&]() -> bool {   // ring slot of tile lt is free again
+            return warp_wait(BAR(B_LTFREE + lt % LR), (uint32_t)((lt / LR) & 1) ^ 1u, abort_flag);
+        };
+        auto publish = [&](int cnt, int last, int seq) {
+            if (lane == 0) lmeta[lt % LR] = make_int4(cnt, last, seq, 0);
+            mbar_arrive(BAR(B_LTFULL + lt % LR));             // every lane releases its own writes
+            ++lt;
+        };
+        bool bad = false;
+        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
             const int a = (int)((e0 > tok * T ? e0 : tok * T) - tok * T);
             const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
-            if (!warp_wait(BAR(B_LFREE), (seg & 1) ^ 1, abort_flag)) break;
-            // stage entries [a, z) with one round trip: entry g of the flattened index tensor goes
-            // to list[g - g0], g0 = g_a rounded down to 4 entries, so 16-byte pieces stay aligned
-            const int64_t g_a = tok * T + a, g_z = tok * T + z;
-            const int off = (int)(g_a & 3);
-            const int64_t g0 = g_a - off;
-            const int64_t ga4 = (g_a + 3) & ~(int64_t)3, gz4 = g_z & ~(int64_t)3;
-            if (ga4 >= gz4) {
-                for (int64_t g = g_a + lane; g < g_z; g += 32) cp_async_4(smem_u32(list + (g - g0)), p.idx + g);
-            } else {
-                for (int64_t g = g_a + lane; g < ga4; g += 32) cp_async_4(smem_u32(list + (g - g0)), p.idx + g);
-                for (int64_t g = ga4 + 4 * lane; g < gz4; g += 128) cp_async_16(smem_u32(list + (g - g0)), p.idx + g);
-                for (int64_t g = gz4 + lane; g < g_z; g += 32) cp_async_4(smem_u32(list + (g - g0)), p.idx + g);
-            }
-            cp_async_wait_all();
-            __syncwarp();
+            const int seq = (int)(tok / p.m);
+            const int32_t *irow = p.idx + tok * T;
             {   // warm L2 with the next token's index row
                 const int64_t nt = tok + 1;
                 if (nt * T < e1)
                     for (int j = lane * 32; j < T; j += 32 * 32) prefetch_l2(p.idx + nt * T + j);
             }
-            // compact in place: valid entries move to the front (writes never pass the reads)
-            int nvalid = 0;
-            bool bad = false;
-            for (int j0 = 0; j0 < z - a; j0 += 32) {
-                const int j = j0 + lane;
-                const int v = j < z - a ? list[off + j] : -1;
-                const bool valid = v >= 0 && (int64_t)v < p.n;
-                bad |= (int64_t)v >= p.n;
-                const uint32_t bal = __ballot_sync(0xffffffffu, valid);
-                __syncwarp();
-                if (valid) list[nvalid + __popc(bal & lanemask_lt())] = v;
-                nvalid += __popc(bal);
-                __syncwarp();
+            if (!acquire()) {
+                ok = false;
+                break;
             }
-            if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DS_DEV_BAD_INDEX);
-            if (lane == 0) {
-                *seg_nvalid = nvalid;
-                nvring[seg & 7] = nvalid;   // for the softmax warps, which never read the list
+            fill = 0;
+            int vb[8];
+            auto load = [&](int j0) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const int j = j0 + g * 32 + lane;
+                    vb[g] = j < z ? __ldg(irow + j) : -1;
+                }
+            };
+            load(a);
+            for (int j0 = a; j0 < z && ok; j0 += 256) {
+                int v8[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) v8[g] = vb[g];
+                if (j0 + 256 < z) load(j0 + 256);            // next batch in flight
+#pragma unroll 1
+                for (int g = 0; g < 8 && ok; ++g) {
+                    if (j0 + g * 32 >= z) break;
+                    const int v = v8[g];
+                    const bool valid = v >= 0 && (int64_t)v < p.n;
+                    bad |= (int64_t)v >= p.n;
+                    const uint32_t bal = __ballot_sync(0xffffffffu, valid);
+                    const int c = __popc(bal), pos = __popc(bal & lanemask_lt());
+                    const int space = BN - fill;
+                    int32_t *tile = list + (lt % LR) * BN;
+                    if (valid && pos < space) tile[fill + pos] = v;
+                    if (c > space) {
+                        // the tile is full and more entries follow: publish it, take the next
+                        __syncwarp();
+                        publish(BN, 0, seq);
+                        if (!acquire()) {
+                            ok = false;
+                            break;
+                        }
+                        tile = list + (lt % LR) * BN;
+                        if (valid && pos >= space) tile[pos - space] = v;
+                        fill = c - space;
+                    } else {
+                        fill += c;
+                    }
+                }
             }
-            mbar_arrive(BAR(B_LFULL));          // every lane releases its own list stores
+            if (!ok) break;
+            __syncwarp();
+            publish(fill, 1, seq);                            // the segment's last (maybe empty) tile
         }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DS_DEV_BAD_INDEX);
     } else if (pw >= 0) {
         // ================== row gather: cp.async into the 128-byte-swizzled ring ==================
         // A row half of DH columns is U = DH / 8 units of 16 bytes; each warp instruction copies
-        // 32 / U whole rows, so every global access is a contiguous row piece.
+        // 32 / U whole rows, so every global access is a contiguous row piece.  The row numbers
+        // come from the index ring, tile by tile, in the compaction warp's order.
         constexpr int U = C::DH / 8;
         constexpr int RPW = 32 / U;                      // rows per warp instruction
         const int rsub = lane / U, unit = lane % U;
         const int chunk = unit / 8, u8 = unit % 8;
         const bool writer = pw == 0 && lane == 0;
         const int ptid = pw * 32 + lane;
-        int it = 0, seg = 0;
+        // L2 prefetch: producer thread i pulls 128-byte line i % (DH/64) of row i / (DH/64) of the
+        // ring tile PREFETCH tiles ahead (when already written), so the copies mostly hit L2
+        constexpr int LINES = C::DH / 64;                // 128-byte lines per row half
+        const int pf_row = ptid / LINES, pf_line = ptid % LINES;
+        auto prefetch_tile = [&](int itp) {
+            if (!mbar_test_wait(BAR(B_LTFULL + itp % LR), (uint32_t)(itp / LR) & 1u)) return;
+            const int4 lm = lmeta[itp % LR];
+            const uint16_t *kvl = p.kv + ((int64_t)lm.z * p.n) * (int64_t)D + crank * C::DH + pf_line * 64;
+            const int32_t *tile = list + (itp % LR) * BN;
+            for (int r = pf_row; r < lm.x; r += C::NPROD / LINES) prefetch_l2(kvl + (int64_t)tile[r] * D);
+        };
+        int it = 0;
         bool ok = true;
-        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok, ++seg) {
-            if (!warp_wait(BAR(B_LFULL), seg & 1, abort_flag)) break;
-            const int nvalid = *seg_nvalid;
-            const int ntiles = nvalid > 0 ? (nvalid + BN - 1) / BN : 1;
+        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
             const uint16_t *kvb = p.kv + ((tok / p.m) * p.n) * (int64_t)D + crank * C::DH + unit * 8;
-            // L2 prefetch: producer thread i pulls 128-byte line i % (DH/64) of row i / (DH/64) of a
-            // tile PREFETCH tiles ahead, so the shared-memory copies below mostly hit L2
-            constexpr int LINES = C::DH / 64;                   // 128-byte lines per row half
-            const int pf_row = ptid / LINES, pf_line = ptid % LINES;
-            const uint16_t *kvl = p.kv + ((tok / p.m) * p.n) * (int64_t)D + crank * C::DH + pf_line * 64;
-            auto prefetch_tile = [&](int tt) {
-                for (int r = pf_row; r < BN; r += C::NPROD / LINES) {
-                    const int k = tt * BN + r;
-                    if (k < nvalid) prefetch_l2(kvl + (int64_t)list[k] * D);
+            for (;; ++it) {
+                // index tile it, then its stage
+                if (!warp_wait(BAR(B_LTFULL + it % LR), (uint32_t)(it / LR) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-            };
-            for (int tt = 0; tt < PREFETCH && tt < ntiles; ++tt) prefetch_tile(tt);
-            for (int t = 0; t < ntiles; ++t, ++it) {
-                if (t + PREFETCH < ntiles) prefetch_tile(t + PREFETCH);
+                const int4 lm = lmeta[it % LR];
+                prefetch_tile(it + PREFETCH);
                 const int stage = it % NSTAGE;
                 if (!warp_wait(BAR(B_EMPTY + stage), ((it / NSTAGE) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const int cnt = nvalid - t * BN < BN ? nvalid - t * BN : BN;
+                const int cnt = lm.x;
+                const int32_t *tile = list + (it % LR) * BN;
                 const uint32_t dst0 = base + C::SM_KV + stage * C::TILE_BYTES + chunk * C::CHUNK_BYTES;
 #pragma unroll 4
                 for (int r = pw * RPW + rsub; r < cnt; r += C::NPROD_WARPS * RPW) {
                     // row r, 16-byte unit u8 of its 128-byte chunk: swizzled to unit u8 ^ (r % 8)
-                    const int v = list[t * BN + r];
+                    const int v = tile[r];
                     cp_async_16(dst0 + r * 128 + ((u8 ^ (r & 7)) << 4), kvb + (int64_t)v * D);
                 }
                 cp_async_arrive_noinc(BAR(B_FULL + stage));
                 if (writer) {
-                    meta[stage] = make_int2(cnt, t == ntiles - 1 ? 1 : 0);
+                    meta[stage] = make_int2(cnt, lm.y);
                     mbar_arrive(BAR(B_FULL + stage));
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_LTFREE + it % LR));   // this warp is done with the tile
+                if (lm.y) {
+                    ++it;
+                    break;
+                }
             }
-            if (!ok) break;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_LFREE));   // this warp is done with the list
         }
         cp_async_wait_all();                              // nothing may land after the CTA exits
     } else if (warp == W_MMA) {
@@ -582,14 +622,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
             float m_used = -INFINITY, l = 0.0f;
             bool any = false;
-            // the segment's first tile has landed, so its valid-entry count is published; the
-            // later tiles need no wait here (their scores come after their rows)
+            // each tile's row count and last flag come with its rows (the producers' meta)
             if (!warp_wait(BAR(B_FULL + it % NSTAGE), (it / NSTAGE) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
-            const int nv = nvring[seg & 7];
-            if (nv == 0) {
+            int2 cur = meta[it % NSTAGE];
+            if (cur.x == 0) {
                 // a segment without a single valid row: its only tile loads nothing; once all
                 // 128 threads and the MMA thread have seen it, thread 0 hands the stage back
                 mbar_arrive(BAR(B_ZREAD));
@@ -602,7 +641,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
             } else {
-                for (int tile = 0;; ++tile) {
+                for (;;) {
                     // tile J: own scores from TMEM (+ the peer's partial scores) -> online softmax
                     // -> P (bf16) into shared memory
                     const int sb = J & 1;
@@ -650,7 +689,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         // the exchange warps tell the peer when this buffer is free again (after
                         // the P V of this tile, whose P is written here below)
                     }
-                    const int cnt = nv - tile * BN < BN ? nv - tile * BN : BN;
+                    const int cnt = cur.x;
                     if (cnt < BN) {
 #pragma unroll
                         for (int j = 0; j < BN; ++j)
@@ -717,7 +756,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     mbar_arrive(BAR(B_PFULL + sb));
                     ++J;
                     ++it;
-                    if ((tile + 1) * BN >= nv) break;
+                    if (cur.y) break;
+                    if (!warp_wait(BAR(B_FULL + it % NSTAGE), (it / NSTAGE) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    cur = meta[it % NSTAGE];
                 }
                 if (!ok) break;
             }
