@@ -165,17 +165,14 @@ __host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t E, in
     return (int64_t)(((uint64_t)c * (uint64_t)E) / (uint64_t)G);
 }
 
-// Lane 0 waits for the whole warp (acquire) and broadcasts the outcome; every other lane's
-// accesses to the guarded data come after it receives that value.  Having every lane re-check the
-// barrier, or adding a warp barrier, costs about a microsecond or a quarter of one per tile on
-// this path (measured).  The warp proceeds together or not at all, so warp-collective tcgen05
-// instructions never diverge.
+// Every lane waits for the phase itself (acquire) and the warp proceeds together or not at all,
+// so warp-collective tcgen05 instructions never diverge.  (Measured on this path: one polling
+// lane plus a broadcast costs about twice as much per wait, and a wake-up three times as long.)
 // kCluster: the phase was completed from the other CTA of the cluster (acquire at cluster scope).
 template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait<kCluster>(bar, parity, abort, kWaitLimitNs);
-    return __shfl_sync(0xffffffffu, ok, 0);
+    const bool ok = mbar_wait<kCluster>(bar, parity, abort, kWaitLimitNs);
+    return __all_sync(0xffffffffu, ok);
 }
 
 template <int D>
@@ -210,7 +207,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(B_SFULL + i), 1);
             mbar_init(BAR(B_SFREE + i), C::CL == 2 ? 8 : 4);   // one arrival per reading warp
-            mbar_init(BAR(B_PFULL + i), 128);
+            mbar_init(BAR(B_PFULL + i), 4);       // one arrival per softmax warp
 
         }
         for (int i = 0; i < C::NX; ++i) {
@@ -752,8 +749,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
                         st_shared_v4(prow + ((u ^ (t & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                    // each thread's P stores are made visible to the MMA (async proxy), then one
+                    // arrival per warp
                     fence_proxy_async_smem();
-                    mbar_arrive(BAR(B_PFULL + sb));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(B_PFULL + sb));
                     ++J;
                     ++it;
                     if (cur.y) break;
