@@ -60,7 +60,6 @@ int ds_kv_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int
 
 size_t ds_sparse_attn_workspace_bytes(int b, int m, int h, int d, int topk) {
     if (b < 0 || m < 0 || h < 1 || h > 128 || topk < 0 || !supported_head_dim(d)) return 0;
-    if (topk > kTcMaxTopk) return 0;
     return sparse_attn_tc_workspace_bytes(b, m, h, d, topk);
 }
 
@@ -80,7 +79,6 @@ int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float
     if (topk == 0) {   // nothing to attend to: every output is 0
         return cudaMemsetAsync(o, 0, (size_t)b * m * h * d * sizeof(uint16_t), st) == cudaSuccess ? DS_OK : DS_ECUDA;
     }
-    if (topk > kTcMaxTopk || n * b > INT32_MAX) return launch_sparse_attn_simt(a, st);
     return launch_sparse_attn_tc(a, st);
 }
 

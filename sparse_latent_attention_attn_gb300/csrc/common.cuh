@@ -42,9 +42,7 @@ struct AttnArgs {
     unsigned int *status;
 };
 
-int launch_sparse_attn_simt(const AttnArgs &a, cudaStream_t stream);
 int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream);
 size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk);
-constexpr int kTcMaxTopk = 4096;   // longest index row the tensor-core kernel stages in shared memory
 
 }  // namespace dsattn

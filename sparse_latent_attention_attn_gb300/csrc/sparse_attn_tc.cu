@@ -1035,6 +1035,7 @@ int64_t choose_clusters(int64_t ntok, int topk, int gmax) {
     int64_t k = gmax / ntok;
     const int64_t kmax = topk / (2 * BN) > 1 ? topk / (2 * BN) : 1;
     if (k > kmax) k = kmax;
+    if (k > 32) k = 32;   // the combine kernel merges at most 32 parts per token
     if (k < 1) k = 1;
     return ntok * k;
 }
@@ -1071,6 +1072,17 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     const bool split = splits_tokens(ntok, a.topk, G);
     const size_t need = split ? (size_t)G * 2 * ((size_t)SLOT_HEADS * D + 2 * SLOT_HEADS) * sizeof(float) : 0;
     if (a.workspace_bytes < need || (need && !a.workspace)) return DS_EWORKSPACE;
+    // the combine's table of cut tokens, checked before anything is launched
+    CombineParams cpar;
+    if (split) {
+        cpar.sink = a.sink;
+        cpar.ws = static_cast<const float *>(a.workspace);
+        cpar.o = a.o;
+        cpar.h = a.h;
+        cpar.pad_ = 0.0f;
+        cpar.ncut = cut_tokens(ntok * a.topk, a.topk, G, cpar.cut);
+        if (cpar.ncut <= 0) return DS_EUNSUPPORTED;
+    }
 
     Params p;
     p.q = a.q;
@@ -1106,14 +1118,6 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     cfg.numAttrs = C::CL > 1 ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D>, p) != cudaSuccess) return DS_ECUDA;
     if (split) {
-        CombineParams cpar;
-        cpar.sink = a.sink;
-        cpar.ws = static_cast<const float *>(a.workspace);
-        cpar.o = a.o;
-        cpar.h = a.h;
-        cpar.pad_ = 0.0f;
-        cpar.ncut = cut_tokens(p.E, a.topk, G, cpar.cut);
-        if (cpar.ncut <= 0) return DS_EUNSUPPORTED;
         cudaLaunchConfig_t ccfg = {};
         ccfg.gridDim = dim3((unsigned)cpar.ncut, (unsigned)((a.h + kCombineHeadsPerBlock - 1) / kCombineHeadsPerBlock), 1);
         ccfg.blockDim = dim3(32 * kCombineHeadsPerBlock, 1, 1);

@@ -255,6 +255,9 @@ EDGE = [
     (10, 2, 2, 8, 64, 20, 50, 0.1, True),        # duplicates count as listed
     (11, 1, 1, 128, 512, 100, 1, 0.0, False),
     (12, 1, 4, 64, 512, 5000, 2176, 0.02, False),
+    # index rows longer than any tile ring: one or two tokens split over 32 clusters each
+    (13, 1, 2, 32, 256, 9000, 5000, 0.05, False),
+    (14, 1, 1, 64, 512, 12000, 8192, 0.02, False),
 ]
 
 
