@@ -68,11 +68,14 @@ struct Cfg {
     static constexpr int NCHUNK = DH / 64;          // 128-byte column chunks per row
     static constexpr int CHUNK_BYTES = BN * 128;
     static constexpr int TILE_BYTES = BN * DH * 2;
-    static constexpr int NSTAGE = 5;                // tiles in flight in shared memory
+    // tiles in flight in shared memory; with the d split the fifth stage's 32 KB holds a third
+    // exchange buffer instead, which lets the peer's scores of tile J + 3 arrive while tile J is
+    // still in P V
+    static constexpr int NSTAGE = CL == 2 ? 4 : 5;
     // exchange buffers (tiles of the peer's partial scores).  With the d split, P of tile J is
     // written into exchange buffer J % NX once its scores have been read, and the peer may send
     // tile J + NX there once this CTA's P V of tile J is done.
-    static constexpr int NX = CL == 2 ? 2 : 0;
+    static constexpr int NX = CL == 2 ? 3 : 0;
     static constexpr int NXD = NX > 0 ? NX : 1;     // divisor for buffer arithmetic
     // separate P buffers (no d split): the softmax writes P of tile J into buffer J % NP without
     // waiting, because the MMA thread issues S(J) only after P V of tile J - NP (so S(J)'s
@@ -123,8 +126,11 @@ enum : int {
     B_EMPTY = B_FULL + 5,       // [NSTAGE] MMA -> producer: stage free
     B_SFULL = B_EMPTY + 5,      // [2] MMA -> softmax, exchange: S ready (or the end marker)
     B_SFREE = B_SFULL + 2,      // [2] softmax, exchange -> MMA: S buffer read
-    B_PFULL = B_SFREE + 2,      // [2] softmax -> MMA: P written to shared memory
-    B_PVDONE = B_PFULL + 2,     // [4] MMA -> softmax, exchange: P V of tile J done (slot J % 4)
+    // [4] softmax -> MMA: P of tile J written (slot J % 4).  Four slots: with three exchange
+    // buffers the softmax can finish tile J + 2 before the MMA thread has seen tile J, but not
+    // tile J + 4 (its peer scores need the P V of tile J + 1)
+    B_PFULL = B_SFREE + 2,
+    B_PVDONE = B_PFULL + 4,     // [4] MMA -> softmax, exchange: P V of tile J done (slot J % 4)
     B_QREADY = B_PVDONE + 4,    // softmax -> MMA: Q of the segment in TMEM
     B_OFREE = B_QREADY + 1,     // softmax -> MMA: epilogue has read O
     B_XFULL = B_OFREE + 1,      // [NX] peer -> me: peer's partial scores are in my exchange buffer
@@ -207,14 +213,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(B_SFULL + i), 1);
             mbar_init(BAR(B_SFREE + i), C::CL == 2 ? 8 : 4);   // one arrival per reading warp
-            mbar_init(BAR(B_PFULL + i), 4);       // one arrival per softmax warp
 
         }
         for (int i = 0; i < C::NX; ++i) {
             mbar_init(BAR(B_XFULL + i), 1);     // armed by the receiver; the peer's bytes complete it
             mbar_init(BAR(B_XFREE + i), 4);     // one arrival per exchange warp of the peer
         }
-        for (int i = 0; i < 4; ++i) mbar_init(BAR(B_PVDONE + i), 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(BAR(B_PFULL + i), 4);       // one arrival per softmax warp
+            mbar_init(BAR(B_PVDONE + i), 1);
+        }
         mbar_init(BAR(B_QREADY), 128);
         mbar_init(BAR(B_OFREE), 128);
         mbar_init(BAR(B_DRAIN), 1);
@@ -473,7 +481,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 if (pq_head != pq_tail) {
                     const int q = pq_head & 3;
                     const int Jp = pq_J[q];
-                    if (mbar_test_wait(BAR(B_PFULL + (Jp & 1)), (Jp >> 1) & 1) &&
+                    if (mbar_test_wait(BAR(B_PFULL + (Jp & 3)), (Jp >> 2) & 1) &&
                         (!pq_first[q] || pq_seg[q] == 0 || mbar_test_wait(BAR(B_OFREE), (pq_seg[q] - 1) & 1))) {
                         // P was written by st.shared (generic proxy) and fenced by its writers
                         tc_fence_after();
@@ -753,7 +761,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     // arrival per warp
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(BAR(B_PFULL + sb));
+                    if (lane == 0) mbar_arrive(BAR(B_PFULL + (J & 3)));
                     ++J;
                     ++it;
                     if (cur.y) break;

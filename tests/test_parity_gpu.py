@@ -310,6 +310,23 @@ def test_attn_out_of_range_index_is_skipped_and_flagged(ds):
     assert ds.device_status() == 0
 
 
+def test_repeated_calls_finish_without_timeouts(ds):
+    """Many back-to-back calls on a stream-K split with many segments per cluster (prefill: 4096
+    tokens over the clusters, every boundary cutting a token) and on decode_large: every call
+    finishes with the same output and no bounded wait inside the kernel gives up."""
+    for cfg, reps in ((2, 20), (4, 5)):
+        w = wl.WORKLOADS[cfg]
+        gs = GpuStep(w)
+        gs.run()
+        torch.cuda.synchronize()
+        first = gs.o.clone()
+        for _ in range(reps):
+            gs.attend_only()
+        torch.cuda.synchronize()
+        assert ds.device_status() == 0, f"cfg{cfg}: a kernel wait timed out"
+        assert torch.equal(first, gs.o), f"cfg{cfg}: repeated calls differ"
+
+
 def test_attn_argument_errors(ds):
     q, kv, sink, idx = _case(25, 1, 1, 4, 64, 10, 8)
     q, kv, sink, idx = q.cuda(), kv.cuda(), sink.cuda(), idx.cuda()
