@@ -147,6 +147,18 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
                  "r"(remote_bar)
                  : "memory");
 }
+// Bulk copy (copy engine) of `bytes` from this CTA's shared memory into another CTA's shared
+// memory, counted in bytes on that CTA's mbarrier (destination and barrier from mapa).  Both
+// addresses 16-byte aligned, size a multiple of 16.  Part of the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t remote_bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src), "r"(bytes), "r"(remote_bar)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk copy of this thread has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

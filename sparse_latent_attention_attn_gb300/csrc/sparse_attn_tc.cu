@@ -11,7 +11,7 @@
 //  * Rows are gathered once per (token, tile of 64 valid rows) by cp.async into 128-byte-swizzled
 //    shared memory and used by all heads, as the keys (K-major B operand of Q K^T) and as the
 //    values (MN-major B operand of P V).  -1 entries are compacted away first, so they cost
-//    neither bytes nor MMA work; rows of later tiles are pulled into L2 ahead of the copies.
+//    neither bytes nor MMA work.
 //  * Q lives in TMEM (A operand of Q K^T); P is written to shared memory in the swizzled K-major
 //    layout (A operand of P V), so a score buffer is free again as soon as it has been read and the
 //    MMA can run two tiles ahead of the softmax.
@@ -44,11 +44,11 @@ namespace tc {
 using namespace ptx;
 
 constexpr int BN = 64;            // gathered rows per tile: N of Q K^T, K of P V
-constexpr int PREFETCH = 4;       // tiles further ahead whose rows are pulled into L2
 // compacted indices travel from the compaction warp to the gather warps through a ring of LR
-// tiles of BN entries: the tile being gathered, the PREFETCH tiles whose rows go to L2 ahead of
-// it, and one being filled
-constexpr int LR = PREFETCH + 2;
+// tiles of BN entries, so the compaction runs a few tiles ahead of the copies.  (Pulling the rows
+// of later tiles into L2 ahead of the copies was measured and does not help: with every row
+// already in L2 the kernel is no faster, because its pace is set on chip.)
+constexpr int LR = 4;
 constexpr int NTHREADS = 512;     // 16 warps = 4 warpgroups
 constexpr int W_XCH0 = 8;         // warps 8-11: score exchange (split d) or row gather
 constexpr int W_LIST = 12;        // index compaction
@@ -68,14 +68,18 @@ struct Cfg {
     static constexpr int NCHUNK = DH / 64;          // 128-byte column chunks per row
     static constexpr int CHUNK_BYTES = BN * 128;
     static constexpr int TILE_BYTES = BN * DH * 2;
-    // tiles in flight in shared memory; with the d split the fifth stage's 32 KB holds a third
-    // exchange buffer instead, which lets the peer's scores of tile J + 3 arrive while tile J is
-    // still in P V
+    // tiles in flight in shared memory; with the d split the fifth stage's 32 KB holds the
+    // exchange buffers' share instead
     static constexpr int NSTAGE = CL == 2 ? 4 : 5;
+    // With the d split each exchange warp stages its quarter of a score tile in this CTA's shared
+    // memory and hands it to the copy engine as one bulk copy into the peer's exchange buffer, so
+    // the slow cluster-network traffic never sits in the warps' memory instruction queues
+    // (where it delays every shared-memory access of the softmax warps on the same sub-core).
+    static constexpr bool STAGED = true;
     // exchange buffers (tiles of the peer's partial scores).  With the d split, P of tile J is
     // written into exchange buffer J % NX once its scores have been read, and the peer may send
     // tile J + NX there once this CTA's P V of tile J is done.
-    static constexpr int NX = CL == 2 ? 3 : 0;
+    static constexpr int NX = CL == 2 ? (STAGED ? 2 : 3) : 0;
     static constexpr int NXD = NX > 0 ? NX : 1;     // divisor for buffer arithmetic
     // separate P buffers (no d split): the softmax writes P of tile J into buffer J % NP without
     // waiting, because the MMA thread issues S(J) only after P V of tile J - NP (so S(J)'s
@@ -95,11 +99,15 @@ struct Cfg {
     static constexpr int SM_P = SM_KV + NSTAGE * TILE_BYTES;
     static constexpr int SM_X = SM_P + NP * P_BYTES;
     static constexpr int X_STRIDE = 128 * BN * 4;   // one exchange buffer
+    // a buffer holds four lane quarters of 32 rows x BN f32, quarter q at q * XQ, row 32q + i's
+    // 16-byte unit k at q * XQ + (k * 32 + i) * 16: every warp access is 512 contiguous bytes
+    static constexpr int XQ = 32 * BN * 4;
     // shared address of P of tile J (relative to the 1024-aligned base)
     __device__ static uint32_t p_off(int J) {
         return NX > 0 ? (uint32_t)(SM_X + (J % NXD) * X_STRIDE) : (uint32_t)(SM_P + (J % NPD) * P_BYTES);
     }
-    static constexpr int X_BYTES = NX * X_STRIDE;
+    static constexpr int SM_XS = SM_X + NX * X_STRIDE;        // staging buffer (d split, staged)
+    static constexpr int X_BYTES = NX * X_STRIDE + (CL == 2 && STAGED ? X_STRIDE : 0);
     static constexpr int SM_LIST = SM_X + X_BYTES;
     static constexpr int LIST_BYTES = LR * BN * 4;  // the index ring
     static constexpr int SM_BAR = SM_LIST + LIST_BYTES;
@@ -235,8 +243,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         *s_end = -1;
         fence_mbar_init();
         if constexpr (C::CL == 2) {
-            // the exchange buffers expect the peer's live score rows of tiles 0 .. NX-1
-            const uint32_t xbytes = (uint32_t)(p.h < 128 ? p.h : 128) * BN * 4;
+            // the exchange buffers expect the peer's quarters with live rows, tiles 0 .. NX-1
+            const uint32_t xbytes = (uint32_t)((p.h < 128 ? p.h : 128) + 31) / 32 * C::XQ;
             for (int i = 0; i < C::NX; ++i) mbar_arrive_expect_tx(BAR(B_XFULL + i), xbytes);
         }
     }
@@ -354,18 +362,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         const int rsub = lane / U, unit = lane % U;
         const int chunk = unit / 8, u8 = unit % 8;
         const bool writer = pw == 0 && lane == 0;
-        const int ptid = pw * 32 + lane;
-        // L2 prefetch: producer thread i pulls 128-byte line i % (DH/64) of row i / (DH/64) of the
-        // ring tile PREFETCH tiles ahead (when already written), so the copies mostly hit L2
-        constexpr int LINES = C::DH / 64;                // 128-byte lines per row half
-        const int pf_row = ptid / LINES, pf_line = ptid % LINES;
-        auto prefetch_tile = [&](int itp) {
-            if (!mbar_test_wait(BAR(B_LTFULL + itp % LR), (uint32_t)(itp / LR) & 1u)) return;
-            const int4 lm = lmeta[itp % LR];
-            const uint16_t *kvl = p.kv + ((int64_t)lm.z * p.n) * (int64_t)D + crank * C::DH + pf_line * 64;
-            const int32_t *tile = list + (itp % LR) * BN;
-            for (int r = pf_row; r < lm.x; r += C::NPROD / LINES) prefetch_l2(kvl + (int64_t)tile[r] * D);
-        };
         int it = 0;
         bool ok = true;
         for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
@@ -377,7 +373,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     break;
                 }
                 const int4 lm = lmeta[it % LR];
-                prefetch_tile(it + PREFETCH);
                 const int stage = it % NSTAGE;
                 if (!warp_wait(BAR(B_EMPTY + stage), ((it / NSTAGE) & 1) ^ 1, abort_flag)) {
                     ok = false;
@@ -540,16 +535,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         __syncwarp();
     } else if (C::CL == 2 && warp >= W_XCH0 && warp < W_XCH0 + 4) {
         // ======================= score exchange (d split across the cluster) =======================
-        // Warp w reads TMEM lane quarter w % 4 of each finished score tile and stores it into the
+        // Warp w reads TMEM lane quarter w % 4 of each finished score tile and sends it to the
         // peer's exchange buffer, so the softmax warps never wait on the cluster network to send.
+        // Quarters without a live head are not sent (the receiver expects only the others).
         const int quarter = warp & 3;
-        const int t = quarter * 32 + lane;               // head row = TMEM lane
-        const bool live = t < p.h;
+        const bool live_q = quarter * 32 < p.h;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         constexpr uint32_t XSTRIDE = C::X_STRIDE;
-        const uint32_t xpeer = mapa(base + C::SM_X, peer);
-        const uint32_t xfull_peer = mapa(BAR(B_XFULL), peer);   // counts the bytes of each store
+        const uint32_t xpeer = mapa(base + C::SM_X, peer) + quarter * C::XQ;
+        const uint32_t xfull_peer = mapa(BAR(B_XFULL), peer);   // counts the bytes of each copy
         const uint32_t xfree_peer = mapa(BAR(B_XFREE), peer);
+        const uint32_t stage_q = base + C::SM_XS + quarter * C::XQ;   // this warp's staging quarter
         for (int J = 0; has_work; ++J) {
             const int sb = J & 1;
             const uint32_t ph = (J >> 1) & 1;
@@ -565,8 +561,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             }
             if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) break;
             if (*s_end == J) break;
-            // the peer's exchange buffer for tile J is free (its P V of tile J - NX is done)
-            if (!warp_wait<true>(BAR(B_XFREE + xs), xph ^ 1, abort_flag)) break;
             tc_fence_after();
             uint32_t r0[32], r1[32];
             tmem_ld32(tmem + lane_off + C::S_COL + sb * BN, r0);
@@ -576,20 +570,47 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
-            // rows of heads >= h are never read, so only live rows cross the cluster; each
-            // asynchronous store counts its bytes on the peer's barrier (no fence needed)
-            const uint32_t rbuf = xpeer + xs * XSTRIDE, rbar = xfull_peer + 8u * xs;
-            if (live) {
+            const uint32_t rbar = xfull_peer + 8u * xs;
+            if constexpr (C::STAGED) {
+                // the staging quarter is free once the copy of the previous tile has read it
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+                if (live_q) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    st_async_v4(rbuf + (k * 128 + t) * 16, __uint_as_float(r0[4 * k]), __uint_as_float(r0[4 * k + 1]),
-                                __uint_as_float(r0[4 * k + 2]), __uint_as_float(r0[4 * k + 3]), rbar);
+                    for (int k = 0; k < 8; ++k)
+                        st_shared_v4(stage_q + (k * 32 + lane) * 16, r0[4 * k], r0[4 * k + 1], r0[4 * k + 2], r0[4 * k + 3]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    st_async_v4(rbuf + ((8 + k) * 128 + t) * 16, __uint_as_float(r1[4 * k]),
-                                __uint_as_float(r1[4 * k + 1]), __uint_as_float(r1[4 * k + 2]),
-                                __uint_as_float(r1[4 * k + 3]), rbar);
+                    for (int k = 0; k < 8; ++k)
+                        st_shared_v4(stage_q + ((8 + k) * 32 + lane) * 16, r1[4 * k], r1[4 * k + 1], r1[4 * k + 2],
+                                     r1[4 * k + 3]);
+                    fence_proxy_async_smem();            // the copy engine reads what was written here
+                }
+                // the peer's exchange buffer for tile J is free (its P V of tile J - NX is done)
+                if (!warp_wait<true>(BAR(B_XFREE + xs), xph ^ 1, abort_flag)) break;
+                if (live_q && lane == 0) {
+                    bulk_copy_to_peer(xpeer + xs * XSTRIDE, stage_q, C::XQ, rbar);
+                    bulk_commit_group();
+                }
+            } else {
+                // the peer's exchange buffer for tile J is free (its P V of tile J - NX is done)
+                if (!warp_wait<true>(BAR(B_XFREE + xs), xph ^ 1, abort_flag)) break;
+                // each asynchronous store counts its bytes on the peer's barrier (no fence needed)
+                const uint32_t rbuf = xpeer + xs * XSTRIDE + lane * 16;
+                if (live_q) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_async_v4(rbuf + k * 512, __uint_as_float(r0[4 * k]), __uint_as_float(r0[4 * k + 1]),
+                                    __uint_as_float(r0[4 * k + 2]), __uint_as_float(r0[4 * k + 3]), rbar);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_async_v4(rbuf + (8 + k) * 512, __uint_as_float(r1[4 * k]), __uint_as_float(r1[4 * k + 1]),
+                                    __uint_as_float(r1[4 * k + 2]), __uint_as_float(r1[4 * k + 3]), rbar);
+                }
             }
+        }
+        // the staging buffer must stay valid until the copy engine has read it
+        if constexpr (C::STAGED) {
+            if (lane == 0) bulk_wait_read_all();
         }
     } else if (warp < 4) {
         // ============================ softmax + epilogue (warps 0-3) ============================
@@ -679,12 +700,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         // arm the buffer for tile J + NX (its bytes cannot come before every
                         // softmax warp has released tile J below)
                         if (t == 0)
-                            mbar_arrive_expect_tx(BAR(B_XFULL + xs), (uint32_t)(p.h < 128 ? p.h : 128) * BN * 4);
-                        const uint32_t xbuf = base + C::SM_X + xs * XSTRIDE;
+                            mbar_arrive_expect_tx(BAR(B_XFULL + xs), (uint32_t)((p.h < 128 ? p.h : 128) + 31) / 32 * C::XQ);
+                        const uint32_t xbuf = base + C::SM_X + xs * XSTRIDE + warp * C::XQ + lane * 16;
                         if (live) {
 #pragma unroll
                             for (int k = 0; k < BN / 4; ++k) {
-                                const float4 v = ld_shared_v4(xbuf + (k * 128 + t) * 16);
+                                const float4 v = ld_shared_v4(xbuf + k * 512);
                                 s[4 * k] += v.x;
                                 s[4 * k + 1] += v.y;
                                 s[4 * k + 2] += v.z;
