@@ -75,11 +75,14 @@ struct Cfg {
     // memory and hands it to the copy engine as one bulk copy into the peer's exchange buffer, so
     // the slow cluster-network traffic never sits in the warps' memory instruction queues
     // (where it delays every shared-memory access of the softmax warps on the same sub-core).
-    static constexpr bool STAGED = true;
+    // PACKED: each partial score crosses as the top three bytes of its f32 (see pack3 below),
+    // which makes room for a third exchange buffer next to the staging buffer.
+    static constexpr bool PACKED = true;
+    static constexpr int XB = PACKED ? 3 : 4;       // bytes per exchanged score
     // exchange buffers (tiles of the peer's partial scores).  With the d split, P of tile J is
     // written into exchange buffer J % NX once its scores have been read, and the peer may send
     // tile J + NX there once this CTA's P V of tile J is done.
-    static constexpr int NX = CL == 2 ? (STAGED ? 2 : 3) : 0;
+    static constexpr int NX = CL == 2 ? (PACKED ? 3 : 2) : 0;
     static constexpr int NXD = NX > 0 ? NX : 1;     // divisor for buffer arithmetic
     // separate P buffers (no d split): the softmax writes P of tile J into buffer J % NP without
     // waiting, because the MMA thread issues S(J) only after P V of tile J - NP (so S(J)'s
@@ -98,16 +101,18 @@ struct Cfg {
     static constexpr int SM_KV = 0;
     static constexpr int SM_P = SM_KV + NSTAGE * TILE_BYTES;
     static constexpr int SM_X = SM_P + NP * P_BYTES;
-    static constexpr int X_STRIDE = 128 * BN * 4;   // one exchange buffer
-    // a buffer holds four lane quarters of 32 rows x BN f32, quarter q at q * XQ, row 32q + i's
-    // 16-byte unit k at q * XQ + (k * 32 + i) * 16: every warp access is 512 contiguous bytes
-    static constexpr int XQ = 32 * BN * 4;
+    // an exchange buffer holds four lane quarters of 32 rows x BN scores (XB bytes each), quarter
+    // q at q * XQ, row 32q + i's 16-byte unit k at q * XQ + (k * 32 + i) * 16: every warp access
+    // is 512 contiguous bytes.  P of the tile (128 rows of 128 bytes) is later written over it.
+    static constexpr int XQ = 32 * BN * XB;
+    static constexpr int X_STRIDE = 4 * XQ;         // one exchange buffer
+    static constexpr int XU = BN * XB / 16;         // 16-byte units per row
     // shared address of P of tile J (relative to the 1024-aligned base)
     __device__ static uint32_t p_off(int J) {
         return NX > 0 ? (uint32_t)(SM_X + (J % NXD) * X_STRIDE) : (uint32_t)(SM_P + (J % NPD) * P_BYTES);
     }
-    static constexpr int SM_XS = SM_X + NX * X_STRIDE;        // staging buffer (d split, staged)
-    static constexpr int X_BYTES = NX * X_STRIDE + (CL == 2 && STAGED ? X_STRIDE : 0);
+    static constexpr int SM_XS = SM_X + NX * X_STRIDE;        // staging buffer (d split)
+    static constexpr int X_BYTES = NX * X_STRIDE + (CL == 2 ? X_STRIDE : 0);
     static constexpr int SM_LIST = SM_X + X_BYTES;
     static constexpr int LIST_BYTES = LR * BN * 4;  // the index ring
     static constexpr int SM_BAR = SM_LIST + LIST_BYTES;
@@ -116,6 +121,8 @@ struct Cfg {
     static_assert(Q_COL + DH / 2 <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(SM_P % 1024 == 0 && P_BYTES % 1024 == 0, "swizzled operands are 1024-byte aligned");
+    static_assert(CL == 1 || (SM_X % 1024 == 0 && X_STRIDE % 1024 == 0 && X_STRIDE >= P_BYTES),
+                  "P of a tile is written over its exchange buffer");
     static_assert(NSTAGE <= 5 && NX <= 3, "barrier slots");
 };
 
@@ -178,6 +185,29 @@ struct Params {
 __host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t E, int64_t G) {
     return (int64_t)(((uint64_t)c * (uint64_t)E) / (uint64_t)G);
 }
+
+// Exchange encoding of partial scores (d split): a score crosses the cluster as the top three
+// bytes of its f32 (sign, exponent, 15 mantissa bits) and is rebuilt with byte 0 a copy of byte 1,
+// i.e. within 2^-15 relative of the original; infinities and NaNs stay what they were.  Each CTA
+// applies the same rounding to its own half (round3) before the two halves are added, so both
+// CTAs compute bit-identical scores and take identical softmax decisions.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+// four scores -> three words: the high halves of a, b; of c, d; then byte 1 of a, b, c, d
+__device__ __forceinline__ void pack3(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t &w0, uint32_t &w1,
+                                      uint32_t &w2) {
+    w0 = prmt(a, b, 0x7632);
+    w1 = prmt(c, d, 0x7632);
+    w2 = prmt(prmt(a, b, 0x0051), prmt(c, d, 0x0051), 0x5410);
+}
+__device__ __forceinline__ float4 unpack3(uint32_t w0, uint32_t w1, uint32_t w2) {
+    return make_float4(__uint_as_float(prmt(w0, w2, 0x1044)), __uint_as_float(prmt(w0, w2, 0x3255)),
+                       __uint_as_float(prmt(w1, w2, 0x1066)), __uint_as_float(prmt(w1, w2, 0x3277)));
+}
+__device__ __forceinline__ float round3(uint32_t x) { return __uint_as_float(prmt(x, x, 0x3211)); }
 
 // Every lane waits for the phase itself (acquire) and the warp proceeds together or not at all,
 // so warp-collective tcgen05 instructions never diverge.  (Measured on this path: one polling
@@ -570,48 +600,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
-            const uint32_t rbar = xfull_peer + 8u * xs;
-            if constexpr (C::STAGED) {
-                // the staging quarter is free once the copy of the previous tile has read it
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
-                if (live_q) {
+            // the staging quarter is free once the copy of the previous tile has read it
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            if (live_q) {
+                const uint32_t srow = stage_q + lane * 16;
+                if constexpr (C::PACKED) {
+                    // 16 scores -> 12 words -> three 16-byte units, four times
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w[12];
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int j = 16 * c + 4 * g;
+                            const uint32_t *v = j < 32 ? r0 + j : r1 + (j - 32);
+                            pack3(v[0], v[1], v[2], v[3], w[3 * g], w[3 * g + 1], w[3 * g + 2]);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 3; ++u)
+                            st_shared_v4(srow + (3 * c + u) * 512, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
+                } else {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        st_shared_v4(stage_q + (k * 32 + lane) * 16, r0[4 * k], r0[4 * k + 1], r0[4 * k + 2], r0[4 * k + 3]);
+                        st_shared_v4(srow + k * 512, r0[4 * k], r0[4 * k + 1], r0[4 * k + 2], r0[4 * k + 3]);
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        st_shared_v4(stage_q + ((8 + k) * 32 + lane) * 16, r1[4 * k], r1[4 * k + 1], r1[4 * k + 2],
-                                     r1[4 * k + 3]);
-                    fence_proxy_async_smem();            // the copy engine reads what was written here
+                        st_shared_v4(srow + (8 + k) * 512, r1[4 * k], r1[4 * k + 1], r1[4 * k + 2], r1[4 * k + 3]);
                 }
-                // the peer's exchange buffer for tile J is free (its P V of tile J - NX is done)
-                if (!warp_wait<true>(BAR(B_XFREE + xs), xph ^ 1, abort_flag)) break;
-                if (live_q && lane == 0) {
-                    bulk_copy_to_peer(xpeer + xs * XSTRIDE, stage_q, C::XQ, rbar);
-                    bulk_commit_group();
-                }
-            } else {
-                // the peer's exchange buffer for tile J is free (its P V of tile J - NX is done)
-                if (!warp_wait<true>(BAR(B_XFREE + xs), xph ^ 1, abort_flag)) break;
-                // each asynchronous store counts its bytes on the peer's barrier (no fence needed)
-                const uint32_t rbuf = xpeer + xs * XSTRIDE + lane * 16;
-                if (live_q) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_async_v4(rbuf + k * 512, __uint_as_float(r0[4 * k]), __uint_as_float(r0[4 * k + 1]),
-                                    __uint_as_float(r0[4 * k + 2]), __uint_as_float(r0[4 * k + 3]), rbar);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_async_v4(rbuf + (8 + k) * 512, __uint_as_float(r1[4 * k]), __uint_as_float(r1[4 * k + 1]),
-                                    __uint_as_float(r1[4 * k + 2]), __uint_as_float(r1[4 * k + 3]), rbar);
-                }
+                fence_proxy_async_smem();                // the copy engine reads what was written here
+            }
+            // the peer's exchange buffer for tile J is free (its P V of tile J - NX is done)
+            if (!warp_wait<true>(BAR(B_XFREE + xs), xph ^ 1, abort_flag)) break;
+            if (live_q && lane == 0) {
+                bulk_copy_to_peer(xpeer + xs * XSTRIDE, stage_q, C::XQ, xfull_peer + 8u * xs);
+                bulk_commit_group();
             }
         }
         // the staging buffer must stay valid until the copy engine has read it
-        if constexpr (C::STAGED) {
-            if (lane == 0) bulk_wait_read_all();
-        }
+        if (lane == 0) bulk_wait_read_all();
     } else if (warp < 4) {
         // ============================ softmax + epilogue (warps 0-3) ============================
         setmaxnreg_inc<REG_SOFTMAX>();
@@ -688,8 +715,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     float s[BN];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        s[j] = __uint_as_float(r0[j]);
-                        s[32 + j] = __uint_as_float(r1[j]);
+                        // with the d split this CTA's half is rounded exactly as the peer sees it
+                        s[j] = C::CL == 2 && C::PACKED ? round3(r0[j]) : __uint_as_float(r0[j]);
+                        s[32 + j] = C::CL == 2 && C::PACKED ? round3(r1[j]) : __uint_as_float(r1[j]);
                     }
                     if constexpr (C::CL == 2) {
                         const int xs = J % C::NXD;
@@ -703,13 +731,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                             mbar_arrive_expect_tx(BAR(B_XFULL + xs), (uint32_t)((p.h < 128 ? p.h : 128) + 31) / 32 * C::XQ);
                         const uint32_t xbuf = base + C::SM_X + xs * XSTRIDE + warp * C::XQ + lane * 16;
                         if (live) {
+                            if constexpr (C::PACKED) {
 #pragma unroll
-                            for (int k = 0; k < BN / 4; ++k) {
-                                const float4 v = ld_shared_v4(xbuf + k * 512);
-                                s[4 * k] += v.x;
-                                s[4 * k + 1] += v.y;
-                                s[4 * k + 2] += v.z;
-                                s[4 * k + 3] += v.w;
+                                for (int c = 0; c < 4; ++c) {
+                                    uint32_t w[12];
+#pragma unroll
+                                    for (int u = 0; u < 3; ++u) {
+                                        const uint4 q4 = ld_shared_u4(xbuf + (3 * c + u) * 512);
+                                        w[4 * u] = q4.x;
+                                        w[4 * u + 1] = q4.y;
+                                        w[4 * u + 2] = q4.z;
+                                        w[4 * u + 3] = q4.w;
+                                    }
+#pragma unroll
+                                    for (int g = 0; g < 4; ++g) {
+                                        const float4 v = unpack3(w[3 * g], w[3 * g + 1], w[3 * g + 2]);
+                                        const int j = 16 * c + 4 * g;
+                                        s[j] += v.x;
+                                        s[j + 1] += v.y;
+                                        s[j + 2] += v.z;
+                                        s[j + 3] += v.w;
+                                    }
+                                }
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < BN / 4; ++k) {
+                                    const float4 v = ld_shared_v4(xbuf + k * 512);
+                                    s[4 * k] += v.x;
+                                    s[4 * k + 1] += v.y;
+                                    s[4 * k + 2] += v.z;
+                                    s[4 * k + 3] += v.w;
+                                }
                             }
                         }
                         // the exchange warps tell the peer when this buffer is free again (after
