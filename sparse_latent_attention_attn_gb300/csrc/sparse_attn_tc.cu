@@ -699,8 +699,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     // -> P (bf16) into shared memory
                     const int sb = J & 1;
                     const uint32_t ph = (J >> 1) & 1;
-                    if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) {
+                    // A warp that gives up on a wait below, before the named barrier of this tile,
+                    // still arrives there, so the other softmax warps are never left waiting on it
+                    // (their own next wait then sees the abort flag).
+                    auto leave = [&]() {
+                        if constexpr (C::CL == 2) named_bar_arrive(1, 128);
                         ok = false;
+                    };
+                    if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) {
+                        leave();
                         break;
                     }
                     tc_fence_after();
@@ -722,7 +729,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     if constexpr (C::CL == 2) {
                         const int xs = J % C::NXD;
                         if (!warp_wait<true>(BAR(B_XFULL + xs), (uint32_t)(J / C::NXD) & 1u, abort_flag)) {
-                            ok = false;
+                            leave();
                             break;
                         }
                         // arm the buffer for tile J + NX (its bytes cannot come before every
@@ -789,7 +796,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         // move the running max: wait for the P V in flight, rescale O and l
                         const int Jp = J - 1;
                         if (!warp_wait(BAR(B_PVDONE + (Jp & 3)), (Jp >> 2) & 1, abort_flag)) {
-                            ok = false;
+                            leave();
                             break;
                         }
                         tc_fence_after();
