@@ -60,6 +60,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
 constexpr int SLOT_HEADS = 128;   // partial slots are laid out for 128 heads
+// A partial slot: O of SLOT_HEADS heads x d (f32, element (h, c) at ((c / 4) * SLOT_HEADS + h) * 4
+// + c % 4, so a warp's accesses with one thread per head are 512 contiguous bytes), then the
+// running maxima and the sums of the heads.
 
 template <int D>
 struct Cfg {
@@ -906,7 +909,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     ws[SLOT_HEADS * D + t] = any ? m_used : -INFINITY;
                     ws[SLOT_HEADS * D + SLOT_HEADS + t] = l;
                 }
-                float4 *dst = reinterpret_cast<float4 *>(ws + (size_t)t * D + crank * C::DH);
+                float4 *dst = reinterpret_cast<float4 *>(ws) + (size_t)(crank * C::DH / 4) * SLOT_HEADS + t;
 #pragma unroll 1
                 for (int c = 0; c < C::DH / 32; ++c) {
                     uint32_t r[32];
@@ -917,10 +920,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     if (live) {
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
-                            dst[c * 8 + k] = any ? make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                                               __uint_as_float(r[4 * k + 2]),
-                                                               __uint_as_float(r[4 * k + 3]))
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                            dst[(size_t)(c * 8 + k) * SLOT_HEADS] =
+                                any ? make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                                  __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
                     }
                 }
@@ -951,10 +954,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
 
 // Merge the partials of every token that a range boundary cut, add the sink once, write bf16.
 // The host lists the cut tokens: token, first part (cluster), number of parts and, per part, the
-// partial slot it wrote (0: the part's first segment, 1: its last).  Block (i, y) merges heads
-// 8y..8y+7 of cut token i, one warp per head: lane j first reads part j's running max and sum,
-// the warp reduces them, then every lane accumulates its D/32 elements over the parts.
-constexpr int kCombineHeadsPerBlock = 8;
+// partial slot it wrote (0: the part's first segment, 1: its last).  Block (i, y) merges columns
+// [y * kCombineCols, (y + 1) * kCombineCols) of cut token i for every head, one thread per head,
+// so each of its loads from the slots is 512 contiguous bytes per warp.
+constexpr int kCombineCols = 64;
 constexpr int kMaxCut = 160;      // cut tokens: at most one per range boundary, G <= SM count
 
 struct CombineParams {
@@ -968,73 +971,51 @@ struct CombineParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(32 * kCombineHeadsPerBlock) sparse_attn_combine_kernel(const CombineParams cp) {
+__global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const CombineParams cp) {
     grid_dependency_wait();   // launched as a programmatic dependent of the attention kernel
-    const int hh = blockIdx.y * kCombineHeadsPerBlock + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    const int hh = threadIdx.x;
     if (hh >= cp.h || (int)blockIdx.x >= cp.ncut) return;
     const int4 c = cp.cut[blockIdx.x];
     const int64_t tok = c.x;
     const int kf = c.y, np = c.z;
     const uint32_t slots = (uint32_t)c.w;
     constexpr size_t SLOT = (size_t)SLOT_HEADS * D + 2 * SLOT_HEADS;
-    constexpr int PER = D / 32;                 // elements per lane
-    constexpr int VW = PER >= 4 ? 4 : PER;      // floats per vector load
-    constexpr int NV = PER / VW;                // vector loads per lane per partial
-    static_assert(PER % VW == 0 && (VW == 2 || VW == 4), "combine vector width");
+    constexpr int COLS = D < kCombineCols ? D : kCombineCols;
     auto part = [&](int i) -> const float * {
         return cp.ws + ((size_t)(kf + i) * 2 + ((slots >> i) & 1u)) * SLOT;
     };
-    // running maxima and sums of the parts, one part per lane (np <= 32)
-    float mi = -INFINITY, li = 0.0f;
-    if (lane < np) {
-        const float *ws = part(lane);
-        mi = ws[SLOT_HEADS * D + hh];
-        li = ws[SLOT_HEADS * D + SLOT_HEADS + hh];
-    }
     const float sink2 = cp.sink[hh] * kLog2e;
-    float top = fmaxf(mi, sink2);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, off));
-    const float wi = (lane < np && mi != -INFINITY) ? exp2f(mi - top) : 0.0f;
-    float den = wi * li;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    den += exp2f(sink2 - top);
-    float acc[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.0f;
+    float top = sink2;
+    for (int i = 0; i < np; ++i) top = fmaxf(top, part(i)[SLOT_HEADS * D + hh]);
+    float den = exp2f(sink2 - top);
     for (int i = 0; i < np; ++i) {
-        const float w = __shfl_sync(0xffffffffu, wi, i);
-        if (w == 0.0f) continue;
-        const float *orow = part(i) + (size_t)hh * D;
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            if constexpr (VW == 4) {
-                const float4 x = reinterpret_cast<const float4 *>(orow)[v * 32 + lane];
-                acc[4 * v] += w * x.x;
-                acc[4 * v + 1] += w * x.y;
-                acc[4 * v + 2] += w * x.z;
-                acc[4 * v + 3] += w * x.w;
-            } else {
-                const float2 x = reinterpret_cast<const float2 *>(orow)[v * 32 + lane];
-                acc[2 * v] += w * x.x;
-                acc[2 * v + 1] += w * x.y;
-            }
-        }
+        const float mi = part(i)[SLOT_HEADS * D + hh];
+        if (mi != -INFINITY) den += exp2f(mi - top) * part(i)[SLOT_HEADS * D + SLOT_HEADS + hh];
     }
     const float inv = 1.0f / den;
-    uint16_t *dst = cp.o + (tok * cp.h + hh) * (int64_t)D;
+    const int c0 = blockIdx.y * COLS;
+    float acc[COLS];
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        if constexpr (VW == 4) {
-            reinterpret_cast<uint2 *>(dst)[v * 32 + lane] =
-                make_uint2(pack_bf16x2(acc[4 * v] * inv, acc[4 * v + 1] * inv),
-                           pack_bf16x2(acc[4 * v + 2] * inv, acc[4 * v + 3] * inv));
-        } else {
-            reinterpret_cast<uint32_t *>(dst)[v * 32 + lane] = pack_bf16x2(acc[2 * v] * inv, acc[2 * v + 1] * inv);
+    for (int j = 0; j < COLS; ++j) acc[j] = 0.0f;
+    for (int i = 0; i < np; ++i) {
+        const float mi = part(i)[SLOT_HEADS * D + hh];
+        if (mi == -INFINITY) continue;
+        const float w = exp2f(mi - top) * inv;
+        const float4 *src = reinterpret_cast<const float4 *>(part(i)) + (size_t)(c0 / 4) * SLOT_HEADS + hh;
+#pragma unroll
+        for (int k = 0; k < COLS / 4; ++k) {
+            const float4 x = src[(size_t)k * SLOT_HEADS];
+            acc[4 * k] += w * x.x;
+            acc[4 * k + 1] += w * x.y;
+            acc[4 * k + 2] += w * x.z;
+            acc[4 * k + 3] += w * x.w;
         }
     }
+    uint4 *dst = reinterpret_cast<uint4 *>(cp.o + (tok * cp.h + hh) * (int64_t)D + c0);
+#pragma unroll
+    for (int k = 0; k < COLS / 8; ++k)
+        dst[k] = make_uint4(pack_bf16x2(acc[8 * k], acc[8 * k + 1]), pack_bf16x2(acc[8 * k + 2], acc[8 * k + 3]),
+                            pack_bf16x2(acc[8 * k + 4], acc[8 * k + 5]), pack_bf16x2(acc[8 * k + 6], acc[8 * k + 7]));
 }
 
 // The cut tokens of a launch (host): every token that some range boundary falls inside.
@@ -1207,8 +1188,8 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D>, p) != cudaSuccess) return DS_ECUDA;
     if (split) {
         cudaLaunchConfig_t ccfg = {};
-        ccfg.gridDim = dim3((unsigned)cpar.ncut, (unsigned)((a.h + kCombineHeadsPerBlock - 1) / kCombineHeadsPerBlock), 1);
-        ccfg.blockDim = dim3(32 * kCombineHeadsPerBlock, 1, 1);
+        ccfg.gridDim = dim3((unsigned)cpar.ncut, (unsigned)((D + kCombineCols - 1) / kCombineCols), 1);
+        ccfg.blockDim = dim3(SLOT_HEADS, 1, 1);
         ccfg.stream = stream;
         ccfg.attrs = attr;   // programmatic serialization only
         ccfg.numAttrs = 1;
