@@ -43,6 +43,11 @@ typedef struct CUstream_st *ds_stream_t;
 
 /* Bits of the device status word (ds_device_status). */
 #define DS_DEV_TIMEOUT 1u     /* a bounded wait inside a kernel gave up; that launch's output is invalid */
+/* Every wait inside ds_sparse_attn's kernel gives up after 2 s, sets DS_DEV_TIMEOUT, drains the
+ * launch's own copies and MMAs and returns, so the context stays usable.  To exercise that path,
+ * a call made while the environment variable DSATTN_TEST_STALL is "1" has its gather warps
+ * withhold the first tile's arrivals: the call takes about 2 s, its output is invalid and
+ * DS_DEV_TIMEOUT is raised.  Nothing sets the variable; it exists for tests. */
 #define DS_DEV_BAD_INDEX 2u   /* an index >= n was seen; the entry was skipped                       */
 
 /*

@@ -33,6 +33,7 @@
 //    path while every exponent stays <= 2^8.
 //  * Every wait is bounded: past a time limit the kernel flags DS_DEV_TIMEOUT, drains its own
 //    copies and MMAs, frees TMEM and returns.
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -181,6 +182,9 @@ struct Params {
     int G;            // clusters
     float scale_log2; // softmax scale * log2(e)
     unsigned int *status;
+    // test switch for the timeout path (DSATTN_TEST_STALL): the gather warps withhold their
+    // arrivals for the first tile, so a bounded wait runs out
+    int stall_first_tile;
 };
 
 // Start of cluster c's range of the flattened entry space.  The host guarantees G * E < 2^63,
@@ -420,10 +424,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     const int v = tile[r];
                     cp_async_16(dst0 + r * 128 + ((u8 ^ (r & 7)) << 4), kvb + (int64_t)v * D);
                 }
-                cp_async_arrive_noinc(BAR(B_FULL + stage));
-                if (writer) {
-                    meta[stage] = make_int2(cnt, lm.y);
-                    mbar_arrive(BAR(B_FULL + stage));
+                if (!(p.stall_first_tile && it == 0)) {
+                    cp_async_arrive_noinc(BAR(B_FULL + stage));
+                    if (writer) {
+                        meta[stage] = make_int2(cnt, lm.y);
+                        mbar_arrive(BAR(B_FULL + stage));
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(B_LTFREE + it % LR));   // this warp is done with the tile
@@ -1168,6 +1174,8 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     p.G = (int)G;
     p.scale_log2 = a.scale * kLog2e;
     p.status = a.status;
+    const char *stall = std::getenv("DSATTN_TEST_STALL");
+    p.stall_first_tile = stall != nullptr && stall[0] == '1';
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(C::CL * G), 1, 1);

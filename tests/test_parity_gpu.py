@@ -327,6 +327,25 @@ def test_repeated_calls_finish_without_timeouts(ds):
         assert torch.equal(first, gs.o), f"cfg{cfg}: repeated calls differ"
 
 
+@pytest.mark.parametrize("d,h,b,topk", [(512, 64, 4, 700), (64, 8, 2, 300)])
+def test_timed_out_wait_is_reported_and_context_stays_usable(ds, monkeypatch, d, h, b, topk):
+    """The kernel's bounded waits, made to run out without any GPU fault: with the test switch
+    DSATTN_TEST_STALL the gather warps withhold the first tile's arrivals, so the MMA thread's
+    wait gives up after its time limit.  The call must end (no hang), raise DS_DEV_TIMEOUT, and
+    leave the context usable: the next call without the switch is clean and agrees with the
+    oracle.  Covers the 2-CTA cluster path (d = 512) and the single-CTA path (d = 64)."""
+    q, kv, sink, idx = _case(40 + d, b, 1, h, d, 2048, topk)
+    scale = d ** -0.5
+    assert ds.device_status() == 0
+    monkeypatch.setenv("DSATTN_TEST_STALL", "1")
+    ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
+    bits_after = ds.device_status()
+    monkeypatch.delenv("DSATTN_TEST_STALL")
+    assert bits_after & ds.DS_DEV_TIMEOUT, f"expected a timeout, status bits {bits_after}"
+    _check_case(ds, q, kv, sink, idx, scale)
+    assert ds.device_status() == 0
+
+
 def test_attn_argument_errors(ds):
     q, kv, sink, idx = _case(25, 1, 1, 4, 64, 10, 8)
     q, kv, sink, idx = q.cuda(), kv.cuda(), sink.cuda(), idx.cuda()
