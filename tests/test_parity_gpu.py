@@ -269,6 +269,26 @@ def test_attn_edge_shapes(ds, case):
     assert ds.device_status() == 0
 
 
+@pytest.mark.parametrize("qscale", [8.0, 32.0])
+def test_attn_peaked_scores_on_the_split_path(ds, qscale):
+    """Large logits on the d = 512 path, where each CTA of the cluster adds the peer's partial
+    scores carried in three bytes (relative error <= 2^-15 per partial score).  q is scaled so
+    the partial logits reach tens to hundreds of log2 units: attention that is nearly one-hot,
+    where a score error shows up directly in the weights.  Also a workload where the two halves'
+    partials cancel: q's second half is minus its first half and kv's halves are equal, so every
+    full score is 0 and the output is the plain mean of the rows (with the sink)."""
+    q, kv, sink, idx = _case(30, 2, 2, 128, 512, 1500, 700, 0.02)
+    q = (q.float() * qscale).to(torch.bfloat16)
+    _check_case(ds, q, kv, sink, idx, 512 ** -0.5)
+    assert ds.device_status() == 0
+    qc = q.clone()
+    qc[..., 256:] = -qc[..., :256]
+    kvc = kv.clone()
+    kvc[..., 256:] = kvc[..., :256]
+    _check_case(ds, qc, kvc, sink, idx, 512 ** -0.5)
+    assert ds.device_status() == 0
+
+
 def test_attn_all_invalid_rows_give_zero(ds):
     q, kv, sink, idx = _case(20, 2, 3, 64, 512, 300, 130)
     idx[1, 2] = -1
