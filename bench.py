@@ -443,7 +443,11 @@ def run_ours(args):
     h2d, d2h = sets[0].io_bytes()
     e2e = None
     if args.e2e_steps > 0:
-        pipe = sets[:2]
+        # three sets in flight (one uploading, one computing, one downloading); a set beyond the
+        # timed-loop sets is made for it when needed
+        pipe = list(sets[:3])
+        while len(pipe) < 3:
+            pipe.append(StepSet(w, device, seed=w.seed + 7919 * len(pipe) + 104729 * rank))
         host = []
         for st_ in pipe:
             host.append({"q": st_.q.cpu().pin_memory(), "c": st_.cidx.cpu().pin_memory(),
