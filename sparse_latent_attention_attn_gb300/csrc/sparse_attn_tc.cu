@@ -17,9 +17,10 @@
 //    MMA can run two tiles ahead of the softmax.
 //  * head_dim 512: O[128 x 512] f32 alone would fill TMEM, so a 2-CTA cluster splits the d columns:
 //    each CTA gathers and multiplies its own 256 columns and the two partial score tiles are summed
-//    through distributed shared memory.  Dedicated exchange warps send this CTA's partial scores
-//    to the peer while the softmax warps work on the previous tile; both CTAs then run the
-//    identical softmax.
+//    through distributed shared memory.  Dedicated exchange warps pack this CTA's partial scores
+//    (3 bytes each) into a local staging buffer and hand them to the copy engine as one bulk copy
+//    per lane quarter into the peer's exchange buffer, while the softmax warps work on the
+//    previous tile; both CTAs then run the identical softmax.
 //  * Warp roles (16 warps): 0-3 softmax and epilogue (thread = head = TMEM lane); 4-7 and 14-15
 //    row gather, plus 8-11 when d is not split; 8-11 score exchange when it is; 12 index
 //    compaction; 13 TMEM allocation + single-thread MMA issue, in whatever order its inputs
