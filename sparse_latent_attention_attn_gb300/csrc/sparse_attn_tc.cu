@@ -26,9 +26,11 @@
 //    compaction; 13 TMEM allocation + single-thread MMA issue, in whatever order its inputs
 //    become ready.
 //  * Persistent clusters take contiguous ranges of the flattened (token, index entry) space, so
-//    the load is balanced whatever the batch; a token cut by a range boundary leaves f32 partials
-//    (running max, sum, unnormalised O) in the workspace and a combine kernel merges them with the
-//    sink.  Whole tokens are normalised with the sink in the epilogue and written as bf16.
+//    the load is balanced whatever the batch; the ranges also charge each token a fixed cost for
+//    the work of a segment change (epilogue, next q, pipeline refill), so clusters that start more
+//    tokens take fewer entries.  A token cut by a range boundary leaves f32 partials (running max,
+//    sum, unnormalised O) in the workspace and a combine kernel merges them with the sink.  Whole
+//    tokens are normalised with the sink in the epilogue and written as bf16.
 //  * Online softmax in the log2 domain with a lazy rescale: the running max is only moved (and O
 //    rescaled) when a tile's max exceeds it by more than 2^8, which keeps the rescale off the hot
 //    path while every exponent stays <= 2^8.
@@ -176,8 +178,10 @@ struct Params {
     uint16_t *o;
     float *ws;
     int64_t n;
-    int64_t E;        // b * m * topk entries
+    int64_t ntok;     // b * m tokens of topk entries each
     int topk;
+    int seg_cost;     // K of range_start, in entries
+    int wide;         // q and o 32-byte aligned: their rows move in 32-byte accesses
     int m;
     int h;
     int G;            // clusters
@@ -188,10 +192,19 @@ struct Params {
     int stall_first_tile;
 };
 
-// Start of cluster c's range of the flattened entry space.  The host guarantees G * E < 2^63,
+// Start of cluster c's range of the flattened entry space (token t holds entries [t T, t T + T)).
+// The G ranges split a cost line evenly, on which each token costs its T entries plus K: the fixed
+// work of a segment (the epilogue, the next token's q, refilling the row pipeline), measured at
+// about four tiles of rows.  A cluster that starts more tokens then gets fewer entries, instead of
+// finishing last.  A cut of the cost line inside a token's K part falls on that token's first
+// entry; K = 0 is the even split of the entries.  The host guarantees G * ntok * (T + K) < 2^63,
 // so the product is exact in 64 bits (a 128-bit division is a long software routine on the GPU).
-__host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t E, int64_t G) {
-    return (int64_t)(((uint64_t)c * (uint64_t)E) / (uint64_t)G);
+__host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t ntok, int64_t T, int64_t K, int64_t G) {
+    const int64_t TK = T + K;
+    if (TK <= 0 || G <= 0) return 0;
+    const int64_t x = (int64_t)(((uint64_t)c * (uint64_t)(ntok * TK)) / (uint64_t)G);
+    const int64_t tok = x / TK, r = x - tok * TK;
+    return tok * T + (r > K ? r - K : 0);
 }
 
 // Exchange encoding of partial scores (d split): a score crosses the cluster as the top three
@@ -247,8 +260,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     const uint32_t crank = C::CL == 2 ? cluster_ctarank() : 0u;
     const uint32_t peer = crank ^ 1u;
     const int64_t cid = blockIdx.x / C::CL;
-    const int64_t e0 = range_start(cid, p.E, p.G), e1 = range_start(cid + 1, p.E, p.G);
     const int T = p.topk;
+    const int64_t e0 = range_start(cid, p.ntok, T, p.seg_cost, p.G);
+    const int64_t e1 = range_start(cid + 1, p.ntok, T, p.seg_cost, p.G);
 
     // ---- set-up --------------------------------------------------------------------------------
     if (threadIdx.x == 0) {
@@ -657,22 +671,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         const bool live = t < p.h;
         const float sink2 = live ? p.sink[t] * kLog2e : 0.0f;
         constexpr uint32_t XSTRIDE = C::X_STRIDE;
+        auto q_row = [&](int64_t tok) {
+            return reinterpret_cast<const uint4 *>(p.q + (tok * p.h + t) * (int64_t)D + crank * C::DH);
+        };
         auto load_q = [&](int64_t tok) {
-            // this CTA's DH columns of q[tok][t] into TMEM columns [Q_COL, Q_COL + DH/2) of lane t
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (tok * p.h + t) * (int64_t)D + crank * C::DH);
-#pragma unroll 1
-            for (int c = 0; c < C::DH / 64; ++c) {
-                uint32_t r[32];
+            // this CTA's DH columns of q[tok][t] into TMEM columns [Q_COL, Q_COL + DH/2) of lane t.
+            // Every load of the row is in flight at once (DH <= 256: at most 128 registers), so a
+            // token change costs one memory latency, not one per 64 columns.  These loads queue
+            // behind the row gathers in the SM's memory pipeline, so fewer, wider ones issue sooner.
+            const uint4 *src = q_row(tok);
+            uint32_t r[C::NCHUNK][32];
+            if (p.wide) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint4 v = live ? __ldg(src + c * 8 + k) : make_uint4(0, 0, 0, 0);
-                    r[4 * k] = v.x;
-                    r[4 * k + 1] = v.y;
-                    r[4 * k + 2] = v.z;
-                    r[4 * k + 3] = v.w;
-                }
-                tmem_st32(tmem + lane_off + C::Q_COL + c * 32, r);
+                for (int c = 0; c < C::NCHUNK; ++c)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t w8[8];
+                        if (live) ld_global_nc_v8(src + c * 8 + 2 * k, w8);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) r[c][8 * k + i] = live ? w8[i] : 0u;
+                    }
+            } else {
+#pragma unroll
+                for (int c = 0; c < C::NCHUNK; ++c)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint4 v = live ? __ldg(src + c * 8 + k) : make_uint4(0, 0, 0, 0);
+                        r[c][4 * k] = v.x;
+                        r[c][4 * k + 1] = v.y;
+                        r[c][4 * k + 2] = v.z;
+                        r[c][4 * k + 3] = v.w;
+                    }
             }
+#pragma unroll
+            for (int c = 0; c < C::NCHUNK; ++c) tmem_st32(tmem + lane_off + C::Q_COL + c * 32, r[c]);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(BAR(B_QREADY));
@@ -683,6 +715,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok, ++seg) {
             const int a = (int)((e0 > tok * T ? e0 : tok * T) - tok * T);
             const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
+            if (live && (tok + 1) * T < e1) {
+                // the next token's q row is read as soon as this segment's scores are all read:
+                // ask for it in L2 now, so that read does not wait on HBM
+                const char *nq = reinterpret_cast<const char *>(q_row(tok + 1));
+#pragma unroll
+                for (int i = 0; i < C::DH * 2 / 128; ++i) prefetch_l2(nq + i * 128);
+            }
             float m_used = -INFINITY, l = 0.0f;
             bool any = false;
             // each tile's row count and last flag come with its rows (the producers' meta)
@@ -882,30 +921,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 tc_fence_after();
             }
             const bool whole = a == 0 && z == T;
+            // O leaves TMEM EG x 32 columns per wait (at most 128 registers), not 32 at a time
+            constexpr int EG = C::DH / 32 < 4 ? C::DH / 32 : 4;
             if (whole) {
                 const float top = fmaxf(m_used, sink2);
                 const float w = any ? ex2(m_used - top) : 0.0f;
                 const float inv = w / (l * w + ex2(sink2 - top));
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (tok * p.h + t) * (int64_t)D + crank * C::DH);
 #pragma unroll 1
-                for (int c = 0; c < C::DH / 32; ++c) {
-                    uint32_t r[32];
+                for (int c0 = 0; c0 < C::DH / 32; c0 += EG) {
+                    uint32_t r[EG][32];
                     if (any) {
-                        tmem_ld32(tmem + lane_off + C::O_COL + c * 32, r);
+#pragma unroll
+                        for (int g = 0; g < EG; ++g) tmem_ld32(tmem + lane_off + C::O_COL + (c0 + g) * 32, r[g]);
                         tmem_ld_wait(r);
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < EG; ++g)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) r[g][i] = 0u;
                     }
-                    if (live) {
+                    if (live && p.wide) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            uint32_t w4[4];
+                        for (int g = 0; g < EG; ++g)
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float x0 = any ? __uint_as_float(r[8 * k + 2 * i]) * inv : 0.0f;
-                                const float x1 = any ? __uint_as_float(r[8 * k + 2 * i + 1]) * inv : 0.0f;
-                                w4[i] = pack_bf16x2(x0, x1);
+                            for (int k = 0; k < 2; ++k) {
+                                uint32_t w8[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float x0 = __uint_as_float(r[g][16 * k + 2 * i]) * inv;
+                                    const float x1 = __uint_as_float(r[g][16 * k + 2 * i + 1]) * inv;
+                                    w8[i] = pack_bf16x2(x0, x1);
+                                }
+                                st_global_v8(dst + (c0 + g) * 4 + 2 * k, w8);
                             }
-                            dst[c * 4 + k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                        }
+                    } else if (live) {
+#pragma unroll
+                        for (int g = 0; g < EG; ++g)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float x0 = __uint_as_float(r[g][8 * k + 2 * i]) * inv;
+                                    const float x1 = __uint_as_float(r[g][8 * k + 2 * i + 1]) * inv;
+                                    w4[i] = pack_bf16x2(x0, x1);
+                                }
+                                dst[(c0 + g) * 4 + k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            }
                     }
                 }
             } else {
@@ -918,20 +981,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 }
                 float4 *dst = reinterpret_cast<float4 *>(ws) + (size_t)(crank * C::DH / 4) * SLOT_HEADS + t;
 #pragma unroll 1
-                for (int c = 0; c < C::DH / 32; ++c) {
-                    uint32_t r[32];
+                for (int c0 = 0; c0 < C::DH / 32; c0 += EG) {
+                    uint32_t r[EG][32];
                     if (any) {
-                        tmem_ld32(tmem + lane_off + C::O_COL + c * 32, r);
+#pragma unroll
+                        for (int g = 0; g < EG; ++g) tmem_ld32(tmem + lane_off + C::O_COL + (c0 + g) * 32, r[g]);
                         tmem_ld_wait(r);
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < EG; ++g)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) r[g][i] = 0u;
                     }
                     if (live) {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            dst[(size_t)(c * 8 + k) * SLOT_HEADS] =
-                                any ? make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                                  __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
+                        for (int g = 0; g < EG; ++g)
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                dst[(size_t)((c0 + g) * 8 + k) * SLOT_HEADS] =
+                                    make_float4(__uint_as_float(r[g][4 * k]), __uint_as_float(r[g][4 * k + 1]),
+                                                __uint_as_float(r[g][4 * k + 2]), __uint_as_float(r[g][4 * k + 3]));
+                            }
                     }
                 }
             }
@@ -1028,24 +1098,26 @@ __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const C
 // The cut tokens of a launch (host): every token that some range boundary falls inside.
 // Returns the number of entries written to cut (at most kMaxCut), or -1 when a token has more
 // than 32 parts or there are too many cut tokens.
-int cut_tokens(int64_t E, int64_t T, int64_t G, int4 *cut) {
+int cut_tokens(int64_t ntok, int64_t T, int64_t K, int64_t G, int4 *cut) {
+    const int64_t E = ntok * T;
+    auto start = [&](int64_t c) { return range_start(c, ntok, T, K, G); };
     int n = 0;
     int64_t last_tok = -1;
     for (int64_t c = 1; c < G; ++c) {
-        const int64_t eb = range_start(c, E, G);
+        const int64_t eb = start(c);
         if (eb % T == 0 || eb >= E) continue;
         const int64_t tok = eb / T;
         if (tok == last_tok) continue;               // already listed through an earlier boundary
         last_tok = tok;
         // parts: clusters whose ranges meet [tok T, tok T + T)
         int64_t kf = c - 1;
-        while (kf > 0 && range_start(kf, E, G) > tok * T) --kf;
+        while (kf > 0 && start(kf) > tok * T) --kf;
         int np = 0;
         uint32_t slots = 0;
-        for (int64_t k = kf; k < G && range_start(k, E, G) < (tok + 1) * T; ++k) {
-            if (range_start(k + 1, E, G) <= range_start(k, E, G)) continue;   // empty range
+        for (int64_t k = kf; k < G && start(k) < (tok + 1) * T; ++k) {
+            if (start(k + 1) <= start(k)) continue;   // empty range
             if (np >= 32) return -1;
-            if (range_start(k, E, G) / T != tok) slots |= 1u << np;          // token is k's last segment
+            if (start(k) / T != tok) slots |= 1u << np;          // token is k's last segment
             if (np == 0) kf = k;
             ++np;
         }
@@ -1116,11 +1188,15 @@ int64_t choose_clusters(int64_t ntok, int topk, int gmax) {
     return ntok * k;
 }
 
+// K of range_start: the per-segment cost when clusters run several tokens each (stream-K); when
+// the clusters split tokens evenly every part has the same fixed work, so the entries split evenly.
+int64_t seg_cost(int64_t ntok, int64_t G) { return G <= ntok ? 4 * BN : 0; }
+
 bool splits_tokens(int64_t ntok, int topk, int64_t G) {
     if (G <= 1 || topk == 0) return false;
-    const int64_t E = ntok * topk;
+    const int64_t K = seg_cost(ntok, G);
     for (int64_t c = 1; c < G; ++c)
-        if (range_start(c, E, G) % topk != 0) return true;
+        if (range_start(c, ntok, topk, K, G) % topk != 0) return true;
     return false;
 }
 
@@ -1144,7 +1220,8 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     if (gmax <= 0) return DS_ECUDA;
     const int64_t ntok = (int64_t)a.b * a.m;
     const int64_t G = choose_clusters(ntok, a.topk, gmax);
-    if (a.topk > 0 && ntok > (INT64_MAX / (G + 1)) / a.topk) return DS_EUNSUPPORTED;   // G * E < 2^63
+    const int64_t K = seg_cost(ntok, G);
+    if (a.topk > 0 && ntok > (INT64_MAX / (G + 1)) / (a.topk + K)) return DS_EUNSUPPORTED;   // G * ntok * (T + K) < 2^63
     const bool split = splits_tokens(ntok, a.topk, G);
     const size_t need = split ? (size_t)G * 2 * ((size_t)SLOT_HEADS * D + 2 * SLOT_HEADS) * sizeof(float) : 0;
     if (a.workspace_bytes < need || (need && !a.workspace)) return DS_EWORKSPACE;
@@ -1156,7 +1233,7 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
         cpar.o = a.o;
         cpar.h = a.h;
         cpar.pad_ = 0.0f;
-        cpar.ncut = cut_tokens(ntok * a.topk, a.topk, G, cpar.cut);
+        cpar.ncut = cut_tokens(ntok, a.topk, K, G, cpar.cut);
         if (cpar.ncut <= 0) return DS_EUNSUPPORTED;
     }
 
@@ -1168,8 +1245,10 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     p.o = a.o;
     p.ws = static_cast<float *>(a.workspace);
     p.n = a.n;
-    p.E = ntok * a.topk;
+    p.ntok = ntok;
     p.topk = a.topk;
+    p.seg_cost = (int)K;
+    p.wide = (((uintptr_t)a.q | (uintptr_t)a.o) & 31u) == 0;
     p.m = a.m;
     p.h = a.h;
     p.G = (int)G;

@@ -289,6 +289,33 @@ def test_attn_peaked_scores_on_the_split_path(ds, qscale):
     assert ds.device_status() == 0
 
 
+@pytest.mark.parametrize("d,h,ntok,topk", [(512, 16, 200, 300), (512, 8, 160, 129), (64, 8, 400, 200)])
+def test_attn_stream_k_every_token(ds, d, h, ntok, topk):
+    """More tokens than co-resident clusters: each cluster runs a range of the (token, entry)
+    space that starts and ends inside tokens, weighted by a fixed cost per token, and the combine
+    kernel merges every cut token.  Every token is checked, cut or whole."""
+    q, kv, sink, idx = _case(50 + topk, ntok // 2, 2, h, d, 3 * topk, topk, 0.05)
+    _check_case(ds, q, kv, sink, idx, d ** -0.5)
+    assert ds.device_status() == 0
+
+
+@pytest.mark.parametrize("d,h,b,m,topk", [(512, 128, 3, 2, 700), (256, 32, 2, 3, 300), (64, 8, 2, 2, 100)])
+def test_attn_q_and_o_aligned_to_16_bytes_only(ds, d, h, b, m, topk):
+    """q and o 16 bytes past a 32-byte boundary (the interface asks for 16): the kernel moves
+    their rows in 16-byte accesses instead of 32-byte ones, and the output is bit-identical to the
+    one written from 32-byte aligned buffers."""
+    q, kv, sink, idx = _case(40 + d, b, m, h, d, 2 * topk, topk, 0.05)
+    o_aligned, _ = _check_case(ds, q, kv, sink, idx, d ** -0.5)
+    qbuf = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    obuf = torch.zeros(q.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    q16, o16 = qbuf[8:].view(q.shape), obuf[8:].view(q.shape)
+    assert q16.data_ptr() % 32 == 16 and o16.data_ptr() % 32 == 16
+    q16.copy_(q.cuda())
+    ds.sparse_attn(q16, kv.cuda(), sink.cuda(), idx.cuda(), d ** -0.5, o=o16)
+    assert torch.equal(o16, o_aligned)
+    assert ds.device_status() == 0
+
+
 def test_attn_all_invalid_rows_give_zero(ds):
     q, kv, sink, idx = _case(20, 2, 3, 64, 512, 300, 130)
     idx[1, 2] = -1
