@@ -39,6 +39,10 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
 __global__ void __launch_bounds__(256) kv_quant_ring_kernel(uint16_t *__restrict__ kv, int64_t kv_bstride,
                                                             uint16_t *__restrict__ ring, int64_t ring_bstride,
                                                             int b, int s, int d, int64_t start_pos, int window) {
+    // a kernel launched after this one as a programmatic dependent (the attention kernel) may be
+    // scheduled as soon as every block of this grid is running; it still waits for this grid to
+    // finish (griddepcontrol.wait) before it reads the ring
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int nblk = d / 32;
     const int64_t total = (int64_t)b * s * nblk;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
