@@ -317,9 +317,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     // everything above overlaps the previous kernel on the stream (launched as a programmatic
     // dependent); from here on the inputs it may have written are read, and outputs written
     grid_dependency_wait();
-    // the combine kernel (a programmatic dependent) may be scheduled now, onto SMs this grid leaves
-    // free or frees; it waits for this whole grid to finish before it reads a partial
-    grid_launch_dependents();
     // warpgroups 1-3 give registers back to the softmax warpgroup before they branch
     if (warp >= 4) setmaxnreg_dec<REG_OTHER>();
 
