@@ -10,6 +10,10 @@ namespace {
 
 __global__ void __launch_bounds__(256) window_idx_kernel(int32_t *__restrict__ idx, int64_t ld, int64_t nrows,
                                                          int rows, int cols, int64_t start_pos, int window) {
+    // a kernel launched after this one as a programmatic dependent (the attention kernel) may be
+    // scheduled as soon as every block of this grid is running; it still waits for this grid to
+    // finish (griddepcontrol.wait) before it reads the index rows
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t total = nrows * cols;
     const int oldest = (int)(start_pos % window) + 1;  // decode: slot holding the oldest token
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
