@@ -61,6 +61,12 @@ def _load():
         lib.oracle_act_quant_inplace.restype = i32
         lib.oracle_kv_quant_ring_write.argtypes = [P, i64, P, i64, i32, i32, i32, i64, i32]
         lib.oracle_kv_quant_ring_write.restype = i32
+        lib.oracle_kv_quantize_fp8.argtypes = [P, i64, i32, P, P]
+        lib.oracle_kv_quantize_fp8.restype = i32
+        lib.oracle_kv_dequantize_fp8.argtypes = [P, P, i64, i32, P]
+        lib.oracle_kv_dequantize_fp8.restype = i32
+        lib.oracle_kv_quant_ring_write_fp8.argtypes = [P, i64, P, P, i64, i32, i32, i32, i64, i32]
+        lib.oracle_kv_quant_ring_write_fp8.restype = i32
         attn_args = [P, P, i64, P, P, i32, f32, P, i32, i32, i32, i32, P, i64, i32]
         lib.oracle_sparse_attn.argtypes = attn_args
         lib.oracle_sparse_attn.restype = i32
@@ -111,6 +117,46 @@ def kv_quant_ring_write(kv_bits: np.ndarray, ring_bits: np.ndarray, start_pos: i
                                             start_pos, window)
     if rc != 0:
         raise ValueError("kv_quant_ring_write: bad arguments")
+
+
+def kv_quantize_fp8(x_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """fp8 row store of bf16 bit patterns ``[..., d]``: (e4m3fn codes ``[..., d]`` uint8,
+    per-32 scale exponents ``[..., d / 32]`` int8, scale = 2^k)."""
+    assert x_bits.dtype == np.uint16 and x_bits.shape[-1] % FP8_BLOCK == 0
+    x = np.ascontiguousarray(x_bits)
+    d = x.shape[-1]
+    rows = x.size // d
+    codes = np.empty(x.shape, dtype=np.uint8)
+    exps = np.empty(x.shape[:-1] + (d // FP8_BLOCK,), dtype=np.int8)
+    if _load().oracle_kv_quantize_fp8(_ptr(x), rows, d, _ptr(codes), _ptr(exps)) != 0:
+        raise ValueError("kv_quantize_fp8: bad arguments")
+    return codes, exps
+
+
+def kv_dequantize_fp8(codes: np.ndarray, exps: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of an fp8 row store (inverse of ``kv_quantize_fp8`` up to the round trip)."""
+    assert codes.dtype == np.uint8 and exps.dtype == np.int8
+    d = codes.shape[-1]
+    assert exps.shape == codes.shape[:-1] + (d // FP8_BLOCK,)
+    c, e = np.ascontiguousarray(codes), np.ascontiguousarray(exps)
+    out = np.empty(codes.shape, dtype=np.uint16)
+    if _load().oracle_kv_dequantize_fp8(_ptr(c), _ptr(e), c.size // d, d, _ptr(out)) != 0:
+        raise ValueError("kv_dequantize_fp8: bad arguments")
+    return out
+
+
+def kv_quant_ring_write_fp8(kv_bits: np.ndarray, codes: np.ndarray, exps: np.ndarray, start_pos: int,
+                            window: int) -> None:
+    """kv_bits ``[b][s][d]`` (rounded in place); the fp8 ring ``codes [b][R][d]``, ``exps
+    [b][R][d/32]`` (R >= window rows per sequence, slots 0..window-1 updated)."""
+    assert kv_bits.dtype == np.uint16 and codes.dtype == np.uint8 and exps.dtype == np.int8
+    b, s, d = kv_bits.shape
+    R = codes.shape[1]
+    assert codes.shape == (b, R, d) and exps.shape == (b, R, d // FP8_BLOCK) and R >= window
+    rc = _load().oracle_kv_quant_ring_write_fp8(_ptr(kv_bits), s * d, _ptr(codes), _ptr(exps), R, b, s, d,
+                                                start_pos, window)
+    if rc != 0:
+        raise ValueError("kv_quant_ring_write_fp8: bad arguments")
 
 
 def sparse_attn(q_bits: np.ndarray, kv_bits: np.ndarray, sink: np.ndarray, idx: np.ndarray, scale: float,

@@ -127,10 +127,10 @@ static void e4m3_build_table(void) {
     }
 }
 
-/* Nearest e4m3fn value to y, ties to the even code (even mantissa).  y must lie in [-448, 448]. */
-float oracle_e4m3_round(float y) {
+/* Code (0..126, the table position) of the e4m3fn magnitude nearest to a >= 0, ties to the even
+ * code (even mantissa).  a must lie in [0, 448]. */
+static int e4m3_nearest_code(double a) {
     pthread_once(&e4m3_once, e4m3_build_table);
-    double a = fabs((double)y);
     int k = 0;                               /* largest code with value <= a */
     while (k + 1 < 127 && e4m3_table[k + 1] <= a) ++k;
     int pick = k;
@@ -139,7 +139,12 @@ float oracle_e4m3_round(float y) {
         if (above < below) pick = k + 1;
         else if (above == below) pick = (k % 2 == 0) ? k : k + 1;
     }
-    double r = e4m3_table[pick];
+    return pick;
+}
+
+/* Nearest e4m3fn value to y, ties to the even code (even mantissa).  y must lie in [-448, 448]. */
+float oracle_e4m3_round(float y) {
+    double r = e4m3_table[e4m3_nearest_code(fabs((double)y))];
     return (float)(signbit(y) ? -r : r);     /* sign-magnitude: -0 stays -0 */
 }
 
@@ -171,6 +176,67 @@ int oracle_act_quant_inplace(uint16_t *x, int64_t n) {
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* fp8 row store: the quantised values kept as e4m3fn codes plus one power-of-two scale        */
+/* exponent per block ([attn] act_quant_inplace, Precision; [query-latent] the compressed      */
+/* cache holds quantised values).  Decoding a row gives exactly the bf16 round trip above.     */
+/* ------------------------------------------------------------------------------------------ */
+
+/* One block: the same scale and rounding as quant_block, kept as codes (bit 7 the sign, bits
+ * 0-6 the position in the ascending table of magnitudes, i.e. the e4m3fn bit pattern) and the
+ * scale's exponent k (scale = 2^k). */
+static void quant_block_codes(const uint16_t *x, uint8_t *codes, int8_t *k_out) {
+    float amax = 0.0f;
+    for (int i = 0; i < ORACLE_FP8_BLOCK; ++i) {
+        float a = fabsf(bf16_bits_to_f32(x[i]));
+        if (a > amax) amax = a;
+    }
+    if (amax < 1e-4f) amax = 1e-4f;
+    float scale = oracle_pow2_ceil(amax / ORACLE_E4M3_MAX);
+    int k;
+    frexpf(scale, &k);                       /* scale = 0.5 * 2^k, so scale = 2^(k - 1) */
+    *k_out = (int8_t)(k - 1);
+    for (int i = 0; i < ORACLE_FP8_BLOCK; ++i) {
+        float y = bf16_bits_to_f32(x[i]) / scale;
+        if (y > ORACLE_E4M3_MAX) y = ORACLE_E4M3_MAX;
+        if (y < -ORACLE_E4M3_MAX) y = -ORACLE_E4M3_MAX;
+        int code = e4m3_nearest_code(fabs((double)y));
+        codes[i] = (uint8_t)((signbit(y) ? 0x80 : 0) | code);
+    }
+}
+
+/* rows x d bf16 values (row-major, d a multiple of FP8_BLOCK) into codes[rows][d] and
+ * exps[rows][d / FP8_BLOCK].  Returns 0, or -1. */
+int oracle_kv_quantize_fp8(const uint16_t *x, int64_t rows, int d, uint8_t *codes, int8_t *exps) {
+    if (rows < 0 || d <= 0 || d % ORACLE_FP8_BLOCK != 0) return -1;
+    const int nb = d / ORACLE_FP8_BLOCK;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int c = 0; c < nb; ++c)
+            quant_block_codes(x + r * d + (int64_t)c * ORACLE_FP8_BLOCK, codes + r * d + (int64_t)c * ORACLE_FP8_BLOCK,
+                              exps + r * nb + c);
+    return 0;
+}
+
+/* codes[rows][d] and exps[rows][d / FP8_BLOCK] back to bf16: value = (+-table[code]) * 2^k,
+ * exact in bf16.  The NaN codes 0x7f / 0xff (never written by the quantiser) decode to NaN. */
+int oracle_kv_dequantize_fp8(const uint8_t *codes, const int8_t *exps, int64_t rows, int d, uint16_t *out) {
+    if (rows < 0 || d <= 0 || d % ORACLE_FP8_BLOCK != 0) return -1;
+    pthread_once(&e4m3_once, e4m3_build_table);
+    const int nb = d / ORACLE_FP8_BLOCK;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int c = 0; c < d; ++c) {
+            uint8_t code = codes[r * d + c];
+            int k = exps[r * nb + c / ORACLE_FP8_BLOCK];
+            if ((code & 0x7f) == 0x7f) {
+                out[r * d + c] = 0x7fc0u;
+                continue;
+            }
+            double v = ldexp(e4m3_table[code & 0x7f], k);
+            out[r * d + c] = f32_to_bf16_bits((float)((code & 0x80) ? -v : v));
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Ring write  ([latent] window_kv_cache; [attn] ring-cache paragraph, WindowCache, attention) */
 /* ------------------------------------------------------------------------------------------ */
 
@@ -191,6 +257,30 @@ int oracle_kv_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring,
                 int64_t slot = (start_pos + t) % window;
                 memcpy(ring + (int64_t)bi * ring_bstride + slot * d, row, (size_t)d * sizeof(uint16_t));
             }
+        }
+    }
+    return 0;
+}
+
+/*
+ * The ring write with an fp8 row store as the ring: kv rows rounded in place as above, and the
+ * ring slot of each of the last `window` rows receives that row's codes and exponents, computed
+ * from the row as given (one quantisation pass, so its decode equals the rounded row).  ring
+ * slots are rows of codes[bi][slot][d] and exps[bi][slot][d / FP8_BLOCK], batch stride
+ * ring_bstride rows.
+ */
+int oracle_kv_quant_ring_write_fp8(uint16_t *kv, int64_t kv_bstride, uint8_t *codes, int8_t *exps,
+                                   int64_t ring_bstride, int b, int s, int d, int64_t start_pos, int window) {
+    if (b < 0 || s < 0 || d <= 0 || d % ORACLE_FP8_BLOCK != 0 || window <= 0 || start_pos < 0) return -1;
+    const int nb = d / ORACLE_FP8_BLOCK;
+    for (int bi = 0; bi < b; ++bi) {
+        for (int t = 0; t < s; ++t) {
+            uint16_t *row = kv + (int64_t)bi * kv_bstride + (int64_t)t * d;
+            if (t >= s - window) {
+                int64_t slot = (int64_t)bi * ring_bstride + (start_pos + t) % window;
+                oracle_kv_quantize_fp8(row, 1, d, codes + slot * d, exps + slot * nb);
+            }
+            oracle_act_quant_inplace(row, d);
         }
     }
     return 0;

@@ -275,6 +275,92 @@ def test_ring_write_rounds_in_place_and_keeps_last_window(oracle_mod):
 
 
 # ----------------------------------------------------------------------------------------------
+# fp8 row store (codes + per-32 power-of-two exponents)
+# ----------------------------------------------------------------------------------------------
+
+def _fp8_store_reference_torch(x_bf16: torch.Tensor):
+    """Codes and exponents with library primitives: f32 amax/448, frexp pow2 ceiling, torch's
+    float8_e4m3fn cast read back as its bit pattern."""
+    x = x_bf16.to(torch.float32).reshape(-1, 32)
+    amax = x.abs().amax(dim=1).clamp(min=torch.tensor(1e-4, dtype=torch.float32))
+    r = amax / torch.tensor(448.0, dtype=torch.float32)
+    m, e = torch.frexp(r)
+    scale = torch.where(m == 0.5, r, torch.ldexp(torch.ones_like(r), e))
+    k = torch.frexp(scale)[1] - 1
+    y = (x / scale[:, None]).clamp(-448, 448)
+    codes = y.to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.numpy().reshape(-1), k.to(torch.int8).numpy()
+
+
+def _fp8_decode_torch(codes: np.ndarray, exps: np.ndarray) -> np.ndarray:
+    c = torch.from_numpy(codes.reshape(-1, 32).copy()).view(torch.float8_e4m3fn).to(torch.float32)
+    v = torch.ldexp(c, torch.from_numpy(exps.reshape(-1, 1).astype(np.int32)))
+    return to_bits(v.reshape(-1))
+
+
+def test_fp8_store_exhaustive_bf16_patterns_match_library(oracle_mod):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = torch.isfinite(from_bits(pats).to(torch.float32)).numpy()
+    pats = np.where(finite, pats, np.uint16(0))
+    want_c, want_k = _fp8_store_reference_torch(from_bits(pats).clone())
+    codes, exps = oracle_mod.kv_quantize_fp8(pats.reshape(-1, 64))
+    assert np.array_equal(codes.reshape(-1), want_c)
+    assert np.array_equal(exps.reshape(-1), want_k)
+
+
+@pytest.mark.parametrize("anchor_exp", [-20, -9, -1, 0, 7, 40])
+def test_fp8_store_every_bf16_value_at_fixed_scale(oracle_mod, anchor_exp):
+    anchor = 448.0 * 2.0 ** anchor_exp
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = from_bits(pats).to(torch.float64)
+    vals = vals[torch.isfinite(vals) & (vals.abs() <= anchor)].to(torch.bfloat16)
+    nb = (vals.numel() + 30) // 31
+    blocks = torch.zeros((nb, 32), dtype=torch.bfloat16)
+    flat = torch.zeros(nb * 31, dtype=torch.bfloat16)
+    flat[: vals.numel()] = vals
+    blocks[:, :31] = flat.view(nb, 31)
+    blocks[:, 31] = anchor
+    want_c, want_k = _fp8_store_reference_torch(blocks)
+    codes, exps = oracle_mod.kv_quantize_fp8(to_bits(blocks))
+    assert np.array_equal(codes.reshape(-1), want_c)
+    assert np.array_equal(exps.reshape(-1), want_k)
+
+
+def test_fp8_store_decodes_to_the_round_trip(oracle_mod):
+    g = torch.Generator().manual_seed(8)
+    x = torch.randn((2048, 64), generator=g) * torch.exp(torch.randn((2048, 1), generator=g) * 6)
+    x = to_bits(x)
+    codes, exps = oracle_mod.kv_quantize_fp8(x)
+    dec = oracle_mod.kv_dequantize_fp8(codes, exps)
+    assert np.array_equal(dec, to_bits(_quant_reference_torch(from_bits(x).clone())))
+    assert np.array_equal(dec.reshape(-1), _fp8_decode_torch(codes, exps))
+    # the decoded rows are a fixed point of the round trip
+    assert np.array_equal(oracle_mod.act_quant_inplace(dec.copy().reshape(-1)), dec.reshape(-1))
+    # zero blocks: every code +0 at the floor exponent of 1e-4 / 448 (2^-22)
+    zc, ze = oracle_mod.kv_quantize_fp8(np.zeros((1, 32), dtype=np.uint16))
+    assert (zc == 0).all() and (ze == -22).all()
+
+
+def test_fp8_ring_write_matches_round_trip_and_store(oracle_mod):
+    g = torch.Generator().manual_seed(9)
+    b, s, d, W, p0, R = 3, 20, 64, 8, 37, 11
+    raw = to_bits(torch.randn((b, s, d), generator=g) * 3)
+    kv = raw.copy()
+    codes = np.full((b, R, d), 0x55, dtype=np.uint8)
+    exps = np.full((b, R, d // 32), 99, dtype=np.int8)
+    oracle_mod.kv_quant_ring_write_fp8(kv, codes, exps, p0, W)
+    assert np.array_equal(kv, oracle_mod.act_quant_inplace(raw.copy().reshape(-1)).reshape(b, s, d))
+    want_c, want_k = oracle_mod.kv_quantize_fp8(raw)
+    slots = set()
+    for t in range(s - W, s):
+        sl = (p0 + t) % W
+        slots.add(sl)
+        assert np.array_equal(codes[:, sl], want_c[:, t]) and np.array_equal(exps[:, sl], want_k[:, t])
+    assert (codes[:, W:] == 0x55).all() and (exps[:, W:] == 99).all()   # rows past the window untouched
+    assert slots == set(range(W))
+
+
+# ----------------------------------------------------------------------------------------------
 # sparse_attn
 # ----------------------------------------------------------------------------------------------
 
