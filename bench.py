@@ -165,9 +165,10 @@ def profiled_traffic(workload: str, launches_units: float):
 # ----------------------------------------------------------------------------------------------
 
 class StepSet:
-    def __init__(self, w: wl.Workload, device, seed: int):
+    def __init__(self, w: wl.Workload, device, seed: int, kv_mode: str = "bf16"):
         from sparse_latent_attention_attn_gb300 import dsattn
         self.w = w
+        self.fp8 = kv_mode == "fp8"
         inp = wl.make_step_inputs(w, device=device, seed=seed)
         self.q, self.kv, self.sink = inp.q, inp.kv, inp.sink
         self.cidx = inp.cidx
@@ -182,6 +183,11 @@ class StepSet:
             self.new_kv = None
             self.ring = torch.zeros((w.b, w.window, w.d), dtype=torch.bfloat16, device=device)
         del inp
+        if self.fp8:
+            # the fp8 row store of the whole kv (window ring in its leading rows, then the
+            # compressed rows, all kept quantised); self.kv becomes its bf16 decode (the round trip)
+            self.codes, self.exps = dsattn.kv_quantize_fp8(self.kv)
+            dsattn.kv_quant_ring_write(self.kv, None, 0, 1)
         need = dsattn.sparse_attn_workspace_bytes(w.b, w.m, w.h, w.d, w.topk)
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         # library kernels per step: ring write, window rows, sparse_attn (+ combine when tokens are cut)
@@ -192,15 +198,25 @@ class StepSet:
         from sparse_latent_attention_attn_gb300 import dsattn
         if ev is not None:
             ev[0].record()
-        dsattn.sparse_attn(self.q, self.kv, self.sink, self.idx, self.w.scale, o=self.o, workspace=self.ws)
+        self._attn(dsattn)
         if ev is not None:
             ev[1].record()
+
+    def _attn(self, dsattn):
+        if self.fp8:
+            dsattn.sparse_attn_fp8kv(self.q, self.codes, self.exps, self.sink, self.idx, self.w.scale, o=self.o,
+                                     workspace=self.ws)
+        else:
+            dsattn.sparse_attn(self.q, self.kv, self.sink, self.idx, self.w.scale, o=self.o, workspace=self.ws)
 
     def run(self, ev_attn=None):
         """The whole step; events (start, end) bracket the sparse_attn launch when given."""
         from sparse_latent_attention_attn_gb300 import dsattn
         w = self.w
-        if w.decode:
+        if w.decode and self.fp8:
+            dsattn.kv_quant_ring_write_fp8(self.new_kv, self.codes, self.exps, w.start_pos, w.window)
+            dsattn.window_topk_idxs(self.idx, w.b, 1, w.start_pos, w.window)
+        elif w.decode:
             dsattn.kv_quant_ring_write(self.new_kv, self.ring, w.start_pos, w.window)
             dsattn.window_topk_idxs(self.idx, w.b, 1, w.start_pos, w.window)
         else:
@@ -208,7 +224,7 @@ class StepSet:
             dsattn.window_topk_idxs(self.idx, w.b, w.s, 0, w.window)
         if ev_attn is not None:
             ev_attn[0].record()
-        dsattn.sparse_attn(self.q, self.kv, self.sink, self.idx, w.scale, o=self.o, workspace=self.ws)
+        self._attn(dsattn)
         if ev_attn is not None:
             ev_attn[1].record()
 
@@ -217,7 +233,8 @@ class StepSet:
         w = self.w
         valid = int((self.idx >= 0).sum().item())
         units = valid * w.h
-        bytes_ = valid * w.d * 2 + 2 * w.b * w.m * w.h * w.d * 2 + self.idx.numel() * 4 + w.h * 4
+        row_bytes = (w.d + w.d // 32) if self.fp8 else w.d * 2    # codes + exponents, or bf16
+        bytes_ = valid * row_bytes + 2 * w.b * w.m * w.h * w.d * 2 + self.idx.numel() * 4 + w.h * 4
         flops = 4 * w.d * units
         return units, bytes_, flops
 
@@ -373,6 +390,11 @@ def run_ours(args):
     w = wl.WORKLOADS[args.config]
     if args.batch:   # smaller batch of the same workload (profiling captures)
         w = dataclasses.replace(w, b=args.batch, name=f"{w.name}[b={args.batch}]")
+    if args.kv == "fp8":
+        if not w.decode or w.d != 512:
+            print(json.dumps({"error": "--kv fp8 needs a decode workload with head_dim 512"}))
+            return 1
+        w = dataclasses.replace(w, name=f"{w.name}_fp8kv")
     peaks = load_peaks()
 
     # enough independent input sets that the gathered rows of consecutive steps miss in L2
@@ -380,7 +402,7 @@ def run_ours(args):
     nsets = args.sets or max(1, min(24, -(-4 * L2_BYTES // max(per_set_bytes, 1))))
     if w.n_comp * w.b * w.d * 2 > 4 * L2_BYTES:
         nsets = args.sets or 2
-    sets = [StepSet(w, device, seed=w.seed + 7919 * k + 104729 * rank) for k in range(nsets)]
+    sets = [StepSet(w, device, seed=w.seed + 7919 * k + 104729 * rank, kv_mode=args.kv) for k in range(nsets)]
     torch.cuda.synchronize()
 
     # one CUDA graph per input set holds a whole step (the three library calls); replaying graphs
@@ -447,7 +469,7 @@ def run_ours(args):
         # timed-loop sets is made for it when needed
         pipe = list(sets[:3])
         while len(pipe) < 3:
-            pipe.append(StepSet(w, device, seed=w.seed + 7919 * len(pipe) + 104729 * rank))
+            pipe.append(StepSet(w, device, seed=w.seed + 7919 * len(pipe) + 104729 * rank, kv_mode=args.kv))
         host = []
         for st_ in pipe:
             host.append({"q": st_.q.cpu().pin_memory(), "c": st_.cidx.cpu().pin_memory(),
@@ -523,8 +545,11 @@ def run_ours(args):
         roof["algorithmic_flops"] = flops
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": 1e3 * slowest_s / args.steps, "higher_is_better": True,
-               "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out, f32 accumulate",
-               "data": "synthetic (seeded, N(0,1) bf16 q/kv, N(0,1) f32 sink)",
+               "scaling": "weak", "vs_baseline": None,
+               "dtype": ("bf16 q/o, kv as e4m3 codes + per-32 power-of-two exponents, f32 accumulate"
+                         if args.kv == "fp8" else "bf16 in/out, f32 accumulate"),
+               "data": "synthetic (seeded, N(0,1) bf16 q/kv, N(0,1) f32 sink)"
+                       + ("; kv rows stored quantised (fp8 row store)" if args.kv == "fp8" else ""),
                "config": workload_config(w, nsets), "roofline": roof, "cpu_baseline": public(cpu), "e2e": e2e,
                "gpu_launches": sets[0].launches * args.steps, "clocks": clk, "device_status": status,
                "units_per_step": units}
@@ -544,6 +569,8 @@ def main(argv=None):
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate through (0 = automatic)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="kv rows as bf16, or as the fp8 row store (decode, head_dim 512)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=60.0,

@@ -138,6 +138,58 @@ int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float
                    void *workspace, size_t workspace_bytes, ds_stream_t stream);
 
 /*
+ * fp8 row store -- KV rows kept as their quantised values instead of the bf16 round trip.
+ * Sources: "Module attn", act_quant_inplace and the Precision paragraph (the quantised value is
+ * an e4m3 code times a power-of-two scale per block of 32, exact in bf16); "DeepSeek V4.1",
+ * attention/query-latent (the compressed cache holds quantised values).  The pages define the
+ * quantisation; storing its codes, rather than the bf16 values they decode to, is this
+ * library's layout:
+ *     codes  uint8 [rows][d]        e4m3fn bit pattern of x / scale (clamped, nearest even)
+ *     exps   int8  [rows][d / 32]   k with scale = 2^k for the block (k in [-22, 120] for finite x)
+ * A row decodes to exactly the bf16 row that ds_kv_quant_ring_write leaves behind, at 1 + 1/32
+ * bytes per value instead of 2.
+ */
+
+/*
+ * ds_kv_quantize_fp8 -- rows of bf16 values into the fp8 row store (x is not modified).
+ * x          device bf16 [rows][d], contiguous, 16-byte aligned
+ * codes      device uint8 [rows][d], 16-byte aligned, written
+ * exps       device int8 [rows][d / 32], written
+ * d          multiple of 32.  Bit-exact with the definition of ds_kv_quant_ring_write's scale and
+ *            rounding.  Errors: DS_EINVAL (null pointer, rows < 0, d % 32 != 0, misalignment).
+ */
+int ds_kv_quantize_fp8(const uint16_t *x, int64_t rows, int d, uint8_t *codes, int8_t *exps,
+                       ds_stream_t stream);
+
+/*
+ * ds_kv_quant_ring_write_fp8 -- ds_kv_quant_ring_write with an fp8 row store as the ring.
+ * kv rows are rounded in place exactly as ds_kv_quant_ring_write does; the token at position
+ * start_pos + t with t >= s - window stores its codes and exponents (from the same single
+ * quantisation pass) in ring row (bi, (start_pos + t) % window), i.e. codes at
+ * ring_codes + (bi * ring_bstride + slot) * d and exps at ring_exps + (bi * ring_bstride + slot)
+ * * (d / 32).  ring_bstride is in rows (>= window), so the ring may be the first rows of an fp8
+ * row store of [b][n][d] that ds_sparse_attn_fp8kv reads.
+ * Errors: DS_EINVAL (null pointer, d % 32 != 0, misalignment, negative sizes, window < 1,
+ *         ring_bstride < window).
+ */
+int ds_kv_quant_ring_write_fp8(uint16_t *kv, int64_t kv_bstride, uint8_t *ring_codes, int8_t *ring_exps,
+                               int64_t ring_bstride, int b, int s, int d, int64_t start_pos, int window,
+                               ds_stream_t stream);
+
+/*
+ * ds_sparse_attn_fp8kv -- ds_sparse_attn reading its rows from an fp8 row store.
+ * The gathered rows are decoded on chip to the same bf16 values, so the result is bit-identical
+ * to ds_sparse_attn on the decoded rows (same shape, same device), at half the gathered bytes.
+ * kv_codes   device uint8 [b][n][d], 16-byte aligned
+ * kv_exps    device int8 [b][n][d / 32]; every exponent must lie in [-126, 127]
+ * Other arguments, the workspace (ds_sparse_attn_workspace_bytes) and the errors are those of
+ * ds_sparse_attn.  Supported: d = 512, 1 <= h <= 128 (DS_EUNSUPPORTED otherwise).
+ */
+int ds_sparse_attn_fp8kv(const uint16_t *q, const uint8_t *kv_codes, const int8_t *kv_exps, int64_t n,
+                         const float *sink, const int32_t *idx, int topk, float scale, uint16_t *o, int b,
+                         int m, int h, int d, void *workspace, size_t workspace_bytes, ds_stream_t stream);
+
+/*
  * ds_sparse_attn_static_scratch -- ds_sparse_attn for callers that cannot allocate device memory.
  * The pages have no counterpart to this call; it exists for integration.  Some callers cannot
  * call cudaMalloc where they run attention (a runtime or memory manager that owns every device

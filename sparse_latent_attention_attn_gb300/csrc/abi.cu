@@ -73,7 +73,46 @@ int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float
     if (!aligned16(q) || !aligned16(o) || (kv && !aligned16(kv))) return DS_EINVAL;
     const size_t need = ds_sparse_attn_workspace_bytes(b, m, h, d, topk);
     if (workspace_bytes < need || (need > 0 && !workspace)) return DS_EWORKSPACE;
-    AttnArgs a{q, kv, n, sink, idx, topk, scale, o, b, m, h, d, workspace, workspace_bytes, status_word()};
+    AttnArgs a{q, kv, nullptr, nullptr, n, sink, idx, topk, scale, o, b, m, h, d, workspace, workspace_bytes,
+               status_word()};
+    if (!a.status) return DS_ECUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (topk == 0) {   // nothing to attend to: every output is 0
+        return cudaMemsetAsync(o, 0, (size_t)b * m * h * d * sizeof(uint16_t), st) == cudaSuccess ? DS_OK : DS_ECUDA;
+    }
+    return launch_sparse_attn_tc(a, st);
+}
+
+int ds_kv_quantize_fp8(const uint16_t *x, int64_t rows, int d, uint8_t *codes, int8_t *exps, ds_stream_t stream) {
+    if (rows < 0 || d <= 0 || d % 32 != 0) return DS_EINVAL;
+    if (rows == 0) return DS_OK;
+    if (!x || !codes || !exps || !aligned16(x) || !aligned16(codes)) return DS_EINVAL;
+    return launch_kv_quantize_fp8(x, rows, d, codes, exps, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ds_kv_quant_ring_write_fp8(uint16_t *kv, int64_t kv_bstride, uint8_t *ring_codes, int8_t *ring_exps,
+                               int64_t ring_bstride, int b, int s, int d, int64_t start_pos, int window,
+                               ds_stream_t stream) {
+    if (!kv || !ring_codes || !ring_exps || b < 0 || s < 0 || d <= 0 || d % 32 != 0 || window < 1 || start_pos < 0)
+        return DS_EINVAL;
+    if (kv_bstride < (int64_t)s * d || kv_bstride % 8 != 0 || !aligned16(kv)) return DS_EINVAL;
+    if (ring_bstride < window || !aligned16(ring_codes)) return DS_EINVAL;
+    return launch_kv_quant_ring_fp8(kv, kv_bstride, ring_codes, ring_exps, ring_bstride, b, s, d, start_pos, window,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ds_sparse_attn_fp8kv(const uint16_t *q, const uint8_t *kv_codes, const int8_t *kv_exps, int64_t n,
+                         const float *sink, const int32_t *idx, int topk, float scale, uint16_t *o, int b, int m,
+                         int h, int d, void *workspace, size_t workspace_bytes, ds_stream_t stream) {
+    if (b < 0 || m < 0 || n < 0 || topk < 0 || h < 1) return DS_EINVAL;
+    if (d != 512 || h > 128) return DS_EUNSUPPORTED;
+    if ((int64_t)b * m == 0) return DS_OK;
+    if (!q || !o || !sink || (topk > 0 && (!idx || !kv_codes || !kv_exps))) return DS_EINVAL;
+    if (!aligned16(q) || !aligned16(o) || (kv_codes && !aligned16(kv_codes))) return DS_EINVAL;
+    const size_t need = ds_sparse_attn_workspace_bytes(b, m, h, d, topk);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return DS_EWORKSPACE;
+    AttnArgs a{q, nullptr, kv_codes, kv_exps, n, sink, idx, topk, scale, o, b, m, h, d, workspace,
+               workspace_bytes, status_word()};
     if (!a.status) return DS_ECUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (topk == 0) {   // nothing to attend to: every output is 0

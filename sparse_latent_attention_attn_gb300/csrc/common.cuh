@@ -26,10 +26,16 @@ int launch_window_idx(int32_t *idx, int64_t ld, int b, int rows, int cols, int64
                       cudaStream_t stream);
 int launch_kv_quant_ring(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b, int s,
                          int d, int64_t start_pos, int window, cudaStream_t stream);
+int launch_kv_quant_ring_fp8(uint16_t *kv, int64_t kv_bstride, uint8_t *codes, int8_t *exps, int64_t ring_bstride,
+                             int b, int s, int d, int64_t start_pos, int window, cudaStream_t stream);
+int launch_kv_quantize_fp8(const uint16_t *x, int64_t rows, int d, uint8_t *codes, int8_t *exps,
+                           cudaStream_t stream);
 
 struct AttnArgs {
     const uint16_t *q;
     const uint16_t *kv;
+    const uint8_t *kv8;    // non-null: gather from the fp8 row store (codes + exponents) instead
+    const int8_t *kexp;
     int64_t n;
     const float *sink;
     const int32_t *idx;

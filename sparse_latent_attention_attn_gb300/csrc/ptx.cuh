@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace dsattn {
@@ -346,6 +347,27 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
+}
+
+// Sixteen e4m3fn codes (bytes in column order) times 2^k as eight bf16 pairs, low half the lower
+// column.  Each pair widens exactly to f16 (cvt.rn.f16x2.e4m3x2), then f32, where the power of two
+// applies exactly; the bf16 rounding is exact too, as the value has at most 4 significant bits.
+// k must lie in [-126, 127].
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi);
+__device__ __forceinline__ void dequant_e4m3x16(const uint4 c, int k, uint32_t (&w)[8]) {
+    const float sc = __uint_as_float((uint32_t)(k + 127) << 23);
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint16_t pair = (uint16_t)(cw[i] >> (16 * h));
+            uint32_t f2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f2) : "h"(pair));
+            const float lo = __half2float(__ushort_as_half((unsigned short)(f2 & 0xffffu))) * sc;
+            const float hi = __half2float(__ushort_as_half((unsigned short)(f2 >> 16))) * sc;
+            w[2 * i + h] = pack_bf16x2(lo, hi);
+        }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -173,6 +173,8 @@ static_assert(SEND_OFF + 4 <= 512, "barrier block");
 struct Params {
     const uint16_t *q;
     const uint16_t *kv;
+    const uint8_t *kv8;       // fp8 row store (F8 kernels): e4m3fn codes [b][n][d]
+    const int8_t *kexp;       //   and per-32 scale exponents [b][n][d / 32]
     const float *sink;
     const int32_t *idx;
     uint16_t *o;
@@ -240,9 +242,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int D>
+template <int D, bool F8 = false>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Params p) {
     using C = Cfg<D>;
+    static_assert(!F8 || C::CL == 2, "the fp8 row store is read by the d-split (d = 512) kernel");
     constexpr int NSTAGE = C::NSTAGE;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -404,6 +407,79 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             publish(fill, 1, seq);                            // the segment's last (maybe empty) tile
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(p.status, DS_DEV_BAD_INDEX);
+    } else if (F8 && pw >= 0) {
+        // ============== row gather from the fp8 row store, decoded into the bf16 ring ==============
+        // A row half is DH e4m3 codes (U8 = DH / 16 units of 16 bytes, half a 32-value block each)
+        // and DH / 32 scale exponents.  A lane takes one unit of a row: its 16 codes and their
+        // block's exponent, loaded as soon as the tile's row numbers are known (before its stage
+        // is free, so the loads overlap that wait), then decoded to 32 bytes of bf16 -- exactly
+        // the values of the bf16 round trip -- and stored swizzled like the cp.async path's rows.
+        constexpr int U8 = C::DH / 16;
+        constexpr int RPW8 = 32 / U8;                    // rows per warp instruction
+        constexpr int STEP = C::NPROD_WARPS * RPW8;
+        constexpr int MAXR = (BN + STEP - 1) / STEP;     // rows per lane and tile, at most
+        const int rsub = lane / U8, unit = lane % U8;
+        const int chunk = unit / 4, ua = 2 * (unit % 4); // the two bf16 units 2 unit, 2 unit + 1
+        const bool writer = pw == 0 && lane == 0;
+        int it = 0;
+        bool ok = true;
+        for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
+            const int64_t row0 = (tok / p.m) * p.n;
+            const uint8_t *cb = p.kv8 + row0 * (int64_t)D + crank * C::DH + unit * 16;
+            const int8_t *xb = p.kexp + row0 * (int64_t)(D / 32) + crank * (C::DH / 32) + unit / 2;
+            for (;; ++it) {
+                if (!warp_wait(BAR(B_LTFULL + it % LR), (uint32_t)(it / LR) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int4 lm = lmeta[it % LR];
+                const int cnt = lm.x;
+                const int32_t *tile = list + (it % LR) * BN;
+                uint4 cv[MAXR];
+                int kx[MAXR];
+#pragma unroll
+                for (int i = 0; i < MAXR; ++i) {
+                    const int r = i * STEP + pw * RPW8 + rsub;
+                    if (r < cnt) {
+                        const int64_t v = tile[r];
+                        cv[i] = __ldg(reinterpret_cast<const uint4 *>(cb + v * D));
+                        kx[i] = __ldg(xb + v * (D / 32));
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_LTFREE + it % LR));   // this warp is done with the tile
+                const int stage = it % NSTAGE;
+                if (!warp_wait(BAR(B_EMPTY + stage), ((it / NSTAGE) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst0 = base + C::SM_KV + stage * C::TILE_BYTES + chunk * C::CHUNK_BYTES;
+#pragma unroll
+                for (int i = 0; i < MAXR; ++i) {
+                    const int r = i * STEP + pw * RPW8 + rsub;
+                    if (r < cnt) {
+                        uint32_t w[8];
+                        dequant_e4m3x16(cv[i], kx[i], w);
+                        const uint32_t rowa = dst0 + r * 128;
+                        st_shared_v4(rowa + ((ua ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+                        st_shared_v4(rowa + (((ua + 1) ^ (r & 7)) << 4), w[4], w[5], w[6], w[7]);
+                    }
+                }
+                // the MMA reads the stage through the async proxy
+                fence_proxy_async_smem();
+                if (!(p.stall_first_tile && it == 0)) {
+                    mbar_arrive(BAR(B_FULL + stage));
+                    if (writer) {
+                        meta[stage] = make_int2(cnt, lm.y);
+                        mbar_arrive(BAR(B_FULL + stage));
+                    }
+                }
+                if (lm.y) {
+                    ++it;
+                    break;
+                }
+            }
+        }
     } else if (pw >= 0) {
         // ================== row gather: cp.async into the 128-byte-swizzled ring ==================
         // A row half of DH columns is U = DH / 8 units of 16 bytes; each warp instruction copies
@@ -1133,24 +1209,24 @@ int cut_tokens(int64_t ntok, int64_t T, int64_t K, int64_t G, int4 *cut) {
 
 struct DeviceInfo {
     int sms = 0;
-    int max_clusters[4] = {0, 0, 0, 0};   // per head_dim variant, co-resident clusters
-    bool ready[4] = {false, false, false, false};
+    int max_clusters[5] = {0, 0, 0, 0, 0};   // per kernel variant, co-resident clusters
+    bool ready[5] = {false, false, false, false, false};
 };
 constexpr int kMaxDev = 64;
 DeviceInfo g_dev[kMaxDev];
 std::mutex g_dev_mutex;
 
-template <int D>
-constexpr int dvar() { return D == 64 ? 0 : D == 128 ? 1 : D == 256 ? 2 : 3; }
+template <int D, bool F8>
+constexpr int dvar() { return F8 ? 4 : D == 64 ? 0 : D == 128 ? 1 : D == 256 ? 2 : 3; }
 
-template <int D>
+template <int D, bool F8 = false>
 int max_clusters(int dev) {
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     DeviceInfo &di = g_dev[dev];
-    if (di.ready[dvar<D>()]) return di.max_clusters[dvar<D>()];
+    if (di.ready[dvar<D, F8>()]) return di.max_clusters[dvar<D, F8>()];
     using C = Cfg<D>;
     if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (cudaFuncSetAttribute(sparse_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(sparse_attn_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
         return 0;
     int nclusters = di.sms;
@@ -1166,12 +1242,12 @@ int max_clusters(int dev) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&nclusters, sparse_attn_tc_kernel<D>, &cfg) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveClusters(&nclusters, sparse_attn_tc_kernel<D, F8>, &cfg) != cudaSuccess ||
             nclusters < 1)
             return 0;
     }
-    di.max_clusters[dvar<D>()] = nclusters;
-    di.ready[dvar<D>()] = true;
+    di.max_clusters[dvar<D, F8>()] = nclusters;
+    di.ready[dvar<D, F8>()] = true;
     return nclusters;
 }
 
@@ -1211,12 +1287,12 @@ size_t workspace_bytes_for(int64_t ntok, int topk) {
     return (size_t)G * 2 * ((size_t)SLOT_HEADS * D + 2 * SLOT_HEADS) * sizeof(float);
 }
 
-template <int D>
+template <int D, bool F8 = false>
 int launch(const AttnArgs &a, cudaStream_t stream) {
     using C = Cfg<D>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return DS_ECUDA;
-    const int gmax = max_clusters<D>(dev);
+    const int gmax = max_clusters<D, F8>(dev);
     if (gmax <= 0) return DS_ECUDA;
     const int64_t ntok = (int64_t)a.b * a.m;
     const int64_t G = choose_clusters(ntok, a.topk, gmax);
@@ -1240,6 +1316,8 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     Params p;
     p.q = a.q;
     p.kv = a.kv;
+    p.kv8 = a.kv8;
+    p.kexp = a.kexp;
     p.sink = a.sink;
     p.idx = a.idx;
     p.o = a.o;
@@ -1273,7 +1351,7 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = C::CL > 1 ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D>, p) != cudaSuccess) return DS_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D, F8>, p) != cudaSuccess) return DS_ECUDA;
     if (split) {
         cudaLaunchConfig_t ccfg = {};
         ccfg.gridDim = dim3((unsigned)cpar.ncut, (unsigned)((D + kCombineCols - 1) / kCombineCols), 1);
@@ -1301,6 +1379,7 @@ size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk) {
 }
 
 int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream) {
+    if (a.kv8) return a.d == 512 ? tc::launch<512, true>(a, stream) : DS_EUNSUPPORTED;
     switch (a.d) {
         case 64: return tc::launch<64>(a, stream);
         case 128: return tc::launch<128>(a, stream);

@@ -46,6 +46,12 @@ _lib.ds_sparse_attn_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.ds_sparse_attn_workspace_bytes.restype = _sz
 _lib.ds_sparse_attn.argtypes = [_P, _P, _i64, _P, _P, _i32, _f32, _P, _i32, _i32, _i32, _i32, _P, _sz, _P]
 _lib.ds_sparse_attn.restype = _i32
+_lib.ds_kv_quantize_fp8.argtypes = [_P, _i64, _i32, _P, _P, _P]
+_lib.ds_kv_quantize_fp8.restype = _i32
+_lib.ds_kv_quant_ring_write_fp8.argtypes = [_P, _i64, _P, _P, _i64, _i32, _i32, _i32, _i64, _i32, _P]
+_lib.ds_kv_quant_ring_write_fp8.restype = _i32
+_lib.ds_sparse_attn_fp8kv.argtypes = [_P, _P, _P, _i64, _P, _P, _i32, _f32, _P, _i32, _i32, _i32, _i32, _P, _sz, _P]
+_lib.ds_sparse_attn_fp8kv.restype = _i32
 _lib.ds_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint)]
 _lib.ds_device_status.restype = _i32
 _lib.ds_status_string.argtypes = [_i32]
@@ -147,6 +153,84 @@ def sparse_attn(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor, idx: torc
     _check("ds_sparse_attn",
            _lib.ds_sparse_attn(_ptr(q), _ptr(kv), n, _ptr(sink), _ptr(idx), topk, float(scale), _ptr(o), b, m, h, d,
                                _ptr(workspace), ws_bytes, _stream(stream)))
+    return o
+
+
+def kv_quantize_fp8(x: torch.Tensor, codes: torch.Tensor | None = None, exps: torch.Tensor | None = None,
+                    stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """fp8 row store of bf16 rows ``x [..., d]`` (contiguous): e4m3fn codes ``[..., d]`` uint8 and
+    per-32 scale exponents ``[..., d / 32]`` int8 (scale = 2^k)."""
+    _need(x, torch.bfloat16, "x")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    d = x.shape[-1]
+    if d % 32:
+        raise ValueError("the last dimension must be a multiple of 32")
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if exps is None:
+        exps = torch.empty(x.shape[:-1] + (d // 32,), dtype=torch.int8, device=x.device)
+    _need(codes, torch.uint8, "codes")
+    _need(exps, torch.int8, "exps")
+    if codes.shape != x.shape or exps.shape != x.shape[:-1] + (d // 32,) or not codes.is_contiguous() \
+            or not exps.is_contiguous():
+        raise ValueError("codes must be shaped like x and exps like x with d / 32 columns, both contiguous")
+    _check("ds_kv_quantize_fp8",
+           _lib.ds_kv_quantize_fp8(_ptr(x), x.numel() // d if d else 0, d, _ptr(codes), _ptr(exps), _stream(stream)))
+    return codes, exps
+
+
+def kv_quant_ring_write_fp8(kv: torch.Tensor, ring_codes: torch.Tensor, ring_exps: torch.Tensor, start_pos: int,
+                            window: int, stream=None) -> None:
+    """fp8 round trip of ``kv`` [b][s][d] in place; the ring is an fp8 row store ``ring_codes``
+    [b][R][d] uint8, ``ring_exps`` [b][R][d/32] int8 (R >= window; it may be the leading rows of
+    the store ``sparse_attn_fp8kv`` reads)."""
+    _need(kv, torch.bfloat16, "kv")
+    _need(ring_codes, torch.uint8, "ring_codes")
+    _need(ring_exps, torch.int8, "ring_exps")
+    b, s, d = kv.shape
+    if kv.stride(2) != 1 or kv.stride(1) != d:
+        raise ValueError("kv rows must be contiguous")
+    R = ring_codes.shape[1]
+    if ring_codes.shape != (b, R, d) or ring_exps.shape != (b, R, d // 32) or not ring_codes.is_contiguous() \
+            or not ring_exps.is_contiguous() or R < window:
+        raise ValueError("the ring must be contiguous [b][>=window][d] codes and [b][>=window][d/32] exps")
+    _check("ds_kv_quant_ring_write_fp8",
+           _lib.ds_kv_quant_ring_write_fp8(_ptr(kv), kv.stride(0), _ptr(ring_codes), _ptr(ring_exps), R, b, s, d,
+                                           start_pos, window, _stream(stream)))
+
+
+def sparse_attn_fp8kv(q: torch.Tensor, kv_codes: torch.Tensor, kv_exps: torch.Tensor, sink: torch.Tensor,
+                      idx: torch.Tensor, scale: float, o: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """``sparse_attn`` with the rows read from an fp8 row store: kv_codes [b][n][d] uint8,
+    kv_exps [b][n][d/32] int8.  Bit-identical to ``sparse_attn`` on the decoded rows."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv_codes, torch.uint8, "kv_codes")
+    _need(kv_exps, torch.int8, "kv_exps")
+    _need(sink, torch.float32, "sink")
+    _need(idx, torch.int32, "idx")
+    b, m, h, d = q.shape
+    n = kv_codes.shape[1]
+    topk = idx.shape[2]
+    if kv_codes.shape != (b, n, d) or kv_exps.shape != (b, n, d // 32) or idx.shape[:2] != (b, m) \
+            or sink.shape != (h,):
+        raise ValueError("shape mismatch")
+    for t, name in ((q, "q"), (kv_codes, "kv_codes"), (kv_exps, "kv_exps"), (idx, "idx"), (sink, "sink")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if o is None:
+        o = torch.empty_like(q)
+    elif o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous bf16 tensor shaped like q")
+    need = sparse_attn_workspace_bytes(b, m, h, d, topk)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("ds_sparse_attn_fp8kv",
+           _lib.ds_sparse_attn_fp8kv(_ptr(q), _ptr(kv_codes), _ptr(kv_exps), n, _ptr(sink), _ptr(idx), topk,
+                                     float(scale), _ptr(o), b, m, h, d, _ptr(workspace), ws_bytes,
+                                     _stream(stream)))
     return o
 
 

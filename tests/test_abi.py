@@ -26,7 +26,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("ds_window_topk_idxs", "ds_kv_quant_ring_write", "ds_sparse_attn",
-                     "ds_sparse_attn_workspace_bytes", "ds_device_status", "ds_status_string"):
+                     "ds_sparse_attn_workspace_bytes", "ds_device_status", "ds_status_string",
+                     "ds_kv_quantize_fp8", "ds_kv_quant_ring_write_fp8", "ds_sparse_attn_fp8kv"):
         assert required in names
 
 
@@ -74,6 +75,29 @@ def test_host_side_argument_checks(lib):
     assert q(fake, 40, None, 0, 1, 1, 40, 0, 8, None) == -1   # d not a multiple of 32
     assert q(None, 64, None, 0, 1, 1, 64, 0, 8, None) == -1
     assert q(P(4104), 64, None, 0, 1, 1, 64, 0, 8, None) == -1  # misaligned
+
+
+def test_fp8_store_argument_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)   # never dereferenced: every call below fails its checks first
+    z = lib.ds_kv_quantize_fp8
+    z.argtypes = [P, ctypes.c_int64, ctypes.c_int, P, P, P]
+    assert z(fake, 4, 40, fake, fake, None) == -1             # d not a multiple of 32
+    assert z(None, 4, 64, fake, fake, None) == -1
+    assert z(fake, 4, 64, P(4100), fake, None) == -1          # misaligned codes
+    assert z(None, 0, 64, None, None, None) == 0              # nothing to do
+    r = lib.ds_kv_quant_ring_write_fp8
+    r.argtypes = [P, ctypes.c_int64, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int64, ctypes.c_int, P]
+    assert r(fake, 64, fake, fake, 7, 1, 1, 64, 0, 8, None) == -1     # ring rows < window
+    assert r(fake, 64, None, fake, 8, 1, 1, 64, 0, 8, None) == -1
+    f = lib.ds_sparse_attn_fp8kv
+    f.argtypes = [P, P, P, ctypes.c_int64, P, P, ctypes.c_int, ctypes.c_float, P, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, P, ctypes.c_size_t, P]
+    assert f(fake, fake, fake, 10, fake, fake, 4, 0.1, fake, 1, 1, 4, 64, None, 0, None) == -2   # d = 512 only
+    assert f(fake, None, fake, 10, fake, fake, 4, 0.1, fake, 1, 1, 4, 512, None, 0, None) == -1
+    assert f(fake, fake, None, 10, fake, fake, 4, 0.1, fake, 1, 1, 4, 512, None, 0, None) == -1
+    assert f(fake, P(4104), fake, 10, fake, fake, 4, 0.1, fake, 1, 1, 4, 512, None, 0, None) == -1
 
 
 def test_workspace_query_is_host_only(lib):

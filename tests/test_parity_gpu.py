@@ -404,3 +404,118 @@ def test_attn_argument_errors(ds):
     with pytest.raises(ds.DsError) as e:
         ds.sparse_attn(big_h, kv, torch.zeros(129, device="cuda"), idx, 0.1)
     assert e.value.status == ds.DS_EUNSUPPORTED
+
+
+# ----------------------------------------------------------------------------------------------
+# fp8 row store (codes + per-32 exponents) and sparse_attn reading it
+# ----------------------------------------------------------------------------------------------
+
+def _spread_rows(seed, rows, d):
+    """bf16 rows whose 32-blocks span magnitudes from 2^-20 to 2^20 (subnormal e4m3 codes, ties)."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((rows, d), generator=g) * torch.exp2(torch.randint(-20, 21, (rows, d // 32), generator=g)
+                                                          .float().repeat_interleave(32, dim=1))
+    return x.to(torch.bfloat16)
+
+
+def test_fp8_quantize_bit_exact(ds):
+    x = _spread_rows(60, 1500, 512)
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    pats = np.where(np.isfinite(bits_to_f32(pats)), pats, np.uint16(0)).reshape(-1, 64)
+    for xb in (bits(x), pats):
+        codes, exps = ds.kv_quantize_fp8(_bf16_from_bits(xb).cuda())
+        want_c, want_k = oracle.kv_quantize_fp8(xb)
+        assert np.array_equal(codes.cpu().numpy(), want_c)
+        assert np.array_equal(exps.cpu().numpy(), want_k)
+
+
+def bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+@pytest.mark.parametrize("b,s,d,W,p0", [(3, 20, 64, 8, 37), (2, 1, 512, 128, 10000), (1, 300, 512, 128, 0)])
+def test_fp8_ring_write_bit_exact(ds, b, s, d, W, p0):
+    g = torch.Generator().manual_seed(61 + s)
+    kv = (torch.randn((b, s, d), generator=g) * 4).to(torch.bfloat16)
+    R = W + 5
+    codes = torch.full((b, R, d), 0x55, dtype=torch.uint8)
+    exps = torch.full((b, R, d // 32), 99, dtype=torch.int8)
+    kv_o, codes_o, exps_o = bits(kv).copy(), codes.numpy().copy(), exps.numpy().copy()   # bits() of a CPU tensor is a view
+    oracle.kv_quant_ring_write_fp8(kv_o, codes_o, exps_o, p0, W)
+    kv_g, codes_g, exps_g = kv.cuda(), codes.cuda(), exps.cuda()
+    ds.kv_quant_ring_write_fp8(kv_g, codes_g, exps_g, p0, W)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(kv_g), kv_o)
+    assert np.array_equal(codes_g.cpu().numpy(), codes_o)
+    assert np.array_equal(exps_g.cpu().numpy(), exps_o)
+
+
+FP8_ATTN = [
+    # seed, b, m, h, n, topk, neg
+    (70, 2, 2, 64, 700, 640, 0.05),
+    (71, 1, 3, 128, 2000, 1000, 0.02),
+    (72, 2, 2, 128, 300, 63, 0.0),
+    (73, 2, 2, 33, 300, 129, 0.3),
+    (74, 1, 4, 64, 5000, 2176, 0.02),
+    (75, 100, 2, 16, 900, 300, 0.05),     # more tokens than clusters: cut tokens and the combine
+    (76, 1, 1, 64, 12000, 8192, 0.02),    # one token split over many clusters
+]
+
+
+@pytest.mark.parametrize("case", FP8_ATTN, ids=[f"f{c[0]}" for c in FP8_ATTN])
+def test_attn_fp8kv_is_bit_identical_to_bf16_on_decoded_rows(ds, case):
+    """The fp8 gather decodes each row on chip to the bf16 values of the round trip, so the MMA
+    sees identical operands: the output must equal ds_sparse_attn on the decoded rows bit for bit,
+    and match the oracle on those rows."""
+    seed, b, m, h, n, topk, neg = case
+    q, _, sink, idx = _case(seed, b, m, h, 512, n, topk, neg)
+    kv = _spread_rows(seed, b * n, 512).view(b, n, 512)
+    codes, exps = ds.kv_quantize_fp8(kv.cuda())
+    dec = oracle.kv_dequantize_fp8(codes.cpu().numpy(), exps.cpu().numpy())
+    assert np.array_equal(dec, oracle.act_quant_inplace(bits(kv).copy().reshape(-1)).reshape(dec.shape))
+    kv_dec = _bf16_from_bits(dec)
+    o_bf16, _ = _check_case(ds, q, kv_dec, sink, idx, 512 ** -0.5)
+    o_f8 = ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), 512 ** -0.5)
+    assert torch.equal(o_f8, o_bf16)
+    assert ds.device_status() == 0
+
+
+def test_attn_fp8kv_ring_then_attend(ds):
+    """The fp8 ring write into the leading rows of an fp8 row store, then attention over window
+    and compressed rows: equal to the bf16 pipeline (round-tripped ring inside a bf16 kv)."""
+    b, W, ncomp, h, d, p0 = 4, 128, 1500, 64, 512, 5000
+    n = W + ncomp
+    g = torch.Generator().manual_seed(80)
+    kv = _spread_rows(81, b * n, d).view(b, n, d)
+    new = (torch.randn((b, 1, d), generator=g) * 2).to(torch.bfloat16)
+    codes, exps = ds.kv_quantize_fp8(kv.cuda())
+    kv_bf = _bf16_from_bits(oracle.kv_dequantize_fp8(codes.cpu().numpy(), exps.cpu().numpy())).cuda()
+    new_a, new_b = new.cuda(), new.cuda()
+    ds.kv_quant_ring_write_fp8(new_a, codes, exps, p0, W)
+    ds.kv_quant_ring_write(new_b, kv_bf, p0, W)
+    q, _, sink, idx = _case(82, b, 1, h, d, n, 700, 0.02)
+    o_f8 = ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), d ** -0.5)
+    o_bf = ds.sparse_attn(q.cuda(), kv_bf, sink.cuda(), idx.cuda(), d ** -0.5)
+    assert torch.equal(new_a, new_b)
+    assert torch.equal(o_f8, o_bf)
+    ref = oracle.sparse_attn(bits(q), bits(kv_bf), sink.numpy(), idx.numpy(), d ** -0.5)
+    assert_close_bf16(bits(o_f8), ref)
+    assert ds.device_status() == 0
+
+
+def test_attn_fp8kv_timed_out_wait_is_reported(ds, monkeypatch):
+    """The bounded-wait abort on the fp8 gather path (see the bf16 test above)."""
+    q, _, sink, idx = _case(90, 4, 1, 64, 512, 2048, 700)
+    kv = _spread_rows(90, 4 * 2048, 512).view(4, 2048, 512)
+    codes, exps = ds.kv_quantize_fp8(kv.cuda())
+    assert ds.device_status() == 0
+    monkeypatch.setenv("DSATTN_TEST_STALL", "1")
+    ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), 512 ** -0.5)
+    bits_after = ds.device_status()
+    monkeypatch.delenv("DSATTN_TEST_STALL")
+    assert bits_after & ds.DS_DEV_TIMEOUT, f"expected a timeout, status bits {bits_after}"
+    o = ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), 512 ** -0.5)
+    dec = oracle.kv_dequantize_fp8(codes.cpu().numpy(), exps.cpu().numpy())
+    ref = oracle.sparse_attn(bits(q), dec, sink.numpy(), idx.numpy(), 512 ** -0.5)
+    assert_close_bf16(bits(o), ref)
+    assert ds.device_status() == 0
