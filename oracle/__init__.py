@@ -67,6 +67,12 @@ def _load():
         lib.oracle_kv_dequantize_fp8.restype = i32
         lib.oracle_kv_quant_ring_write_fp8.argtypes = [P, i64, P, P, i64, i32, i32, i32, i64, i32]
         lib.oracle_kv_quant_ring_write_fp8.restype = i32
+        lib.oracle_rope_table.argtypes = [P, i64, i32, ctypes.c_double]
+        lib.oracle_rope_table.restype = i32
+        lib.oracle_apply_rotary.argtypes = [P, i64, i32, i32, i64, i64, i64, P, i64, i32]
+        lib.oracle_apply_rotary.restype = i32
+        lib.oracle_kv_rope_quant_ring_write.argtypes = [P, i64, P, i64, i32, i32, i32, i64, i32, i32, P, i64]
+        lib.oracle_kv_rope_quant_ring_write.restype = i32
         attn_args = [P, P, i64, P, P, i32, f32, P, i32, i32, i32, i32, P, i64, i32]
         lib.oracle_sparse_attn.argtypes = attn_args
         lib.oracle_sparse_attn.restype = i32
@@ -157,6 +163,43 @@ def kv_quant_ring_write_fp8(kv_bits: np.ndarray, codes: np.ndarray, exps: np.nda
                                                 start_pos, window)
     if rc != 0:
         raise ValueError("kv_quant_ring_write_fp8: bad arguments")
+
+
+def rope_table(npos: int, dim: int, base: float) -> np.ndarray:
+    """The ratio-0 RoPE table ``[npos][dim/2][2]`` f32 of (cos, sin), no YaRN."""
+    out = np.empty((npos, dim // 2, 2), dtype=np.float32)
+    if _load().oracle_rope_table(_ptr(out), npos, dim, float(base)) != 0:
+        raise ValueError("rope_table: bad arguments")
+    return out
+
+
+def apply_rotary(x_bits: np.ndarray, rd: int, table: np.ndarray, start_pos: int, rows_per_pos: int,
+                 positions_per_seq: int, inverse: bool = False) -> np.ndarray:
+    """Rotate the last ``rd`` values of every row of ``x_bits [..., row_len]`` (bf16 bits, in place);
+    row r is at position start_pos + (r // rows_per_pos) % positions_per_seq."""
+    assert x_bits.dtype == np.uint16 and x_bits.flags["C_CONTIGUOUS"] and table.dtype == np.float32
+    row_len = x_bits.shape[-1]
+    assert table.shape[1] * 2 == rd
+    rc = _load().oracle_apply_rotary(_ptr(x_bits), x_bits.size // row_len, row_len, rd, rows_per_pos,
+                                     positions_per_seq, start_pos, _ptr(np.ascontiguousarray(table)),
+                                     table.shape[0], 1 if inverse else 0)
+    if rc != 0:
+        raise ValueError("apply_rotary: bad arguments or a position outside the table")
+    return x_bits
+
+
+def kv_rope_quant_ring_write(kv_bits: np.ndarray, ring_bits: np.ndarray, start_pos: int, window: int, rd: int,
+                             table: np.ndarray) -> None:
+    """RoPE on the last rd values of kv_bits ``[b][s][d]`` (row t at start_pos + t), then the fp8
+    round trip in place and the ring store into ring_bits ``[b][window][d]``."""
+    assert kv_bits.dtype == np.uint16 and ring_bits.dtype == np.uint16 and table.dtype == np.float32
+    b, s, d = kv_bits.shape
+    assert ring_bits.shape == (b, window, d) and table.shape[1] * 2 == rd
+    rc = _load().oracle_kv_rope_quant_ring_write(_ptr(kv_bits), s * d, _ptr(ring_bits), window * d, b, s, d,
+                                                 start_pos, window, rd, _ptr(np.ascontiguousarray(table)),
+                                                 table.shape[0])
+    if rc != 0:
+        raise ValueError("kv_rope_quant_ring_write: bad arguments")
 
 
 def sparse_attn(q_bits: np.ndarray, kv_bits: np.ndarray, sink: np.ndarray, idx: np.ndarray, scale: float,

@@ -287,6 +287,78 @@ int oracle_kv_quant_ring_write_fp8(uint16_t *kv, int64_t kv_bstride, uint8_t *co
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* RoPE  ([attn] freqs_cis, apply_rotary, Precision; [latent] precompute_freqs_cis,            */
+/* apply_rotary_emb and Attention.forward: rotate the last rope_dim of q and of the kv row,    */
+/* then the inverse rotation on the output)                                                      */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * The ratio-0 table (no YaRN): for position p and pair j < dim/2,
+ *   freq_j = 1 / base^(2j / dim)        (f32: the exponent 2j/dim, the power and the reciprocal)
+ *   angle  = p * freq_j                 (f32 product)
+ *   table[p][j] = (cos angle, sin angle) in f32.
+ * out has npos * dim/2 * 2 floats.
+ */
+int oracle_rope_table(float *out, int64_t npos, int dim, double base) {
+    if (npos < 0 || dim <= 0 || dim % 2 != 0 || !(base > 0.0)) return -1;
+    for (int j = 0; j < dim / 2; ++j) {
+        float e = (float)(2 * j) / (float)dim;
+        float pw = (float)pow(base, (double)e);
+        float freq = 1.0f / pw;
+        for (int64_t p = 0; p < npos; ++p) {
+            float ang = (float)p * freq;
+            out[(p * (dim / 2) + j) * 2] = (float)cos((double)ang);
+            out[(p * (dim / 2) + j) * 2 + 1] = (float)sin((double)ang);
+        }
+    }
+    return 0;
+}
+
+/*
+ * Rotate the last rd values of each row_len-wide row of x (bf16, in place): pair j of the rotated
+ * part, (a, b) = (x[2j], x[2j+1]), is the complex number a + ib, multiplied by cos + i sin of row
+ * r's position (sin negated when inverse) in f32, each product and sum rounded separately:
+ *   a' = a c - b s,  b' = a s + b c,  written back as bf16 (nearest even).
+ * Row r sits at position start_pos + (r / rows_per_pos) % positions_per_seq (e.g. rows of
+ * q or o [b][m][h][d]: rows_per_pos = h, positions_per_seq = m).
+ */
+int oracle_apply_rotary(uint16_t *x, int64_t rows, int row_len, int rd, int64_t rows_per_pos,
+                        int64_t positions_per_seq, int64_t start_pos, const float *table, int64_t table_rows,
+                        int inverse) {
+    if (rows < 0 || rd <= 0 || rd % 2 != 0 || rd > row_len || rows_per_pos < 1 || positions_per_seq < 1)
+        return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t pos = start_pos + (r / rows_per_pos) % positions_per_seq;
+        if (pos < 0 || pos >= table_rows) return -1;
+        uint16_t *v = x + r * row_len + (row_len - rd);
+        for (int j = 0; j < rd / 2; ++j) {
+            float a = bf16_bits_to_f32(v[2 * j]), bb = bf16_bits_to_f32(v[2 * j + 1]);
+            float c = table[(pos * (rd / 2) + j) * 2], sn = table[(pos * (rd / 2) + j) * 2 + 1];
+            if (inverse) sn = -sn;
+            float ac = a * c, bs = bb * sn, as = a * sn, bc = bb * c;
+            v[2 * j] = f32_to_bf16_bits(ac - bs);
+            v[2 * j + 1] = f32_to_bf16_bits(as + bc);
+        }
+    }
+    return 0;
+}
+
+/*
+ * The ring write of a ratio-0 layer's new kv rows with their RoPE first ([attn] module text: RoPE
+ * on the last rope_dim, then the fp8 round trip in place, then the ring): row t of the chunk is
+ * at position start_pos + t.
+ */
+int oracle_kv_rope_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b,
+                                    int s, int d, int64_t start_pos, int window, int rd, const float *table,
+                                    int64_t table_rows) {
+    if (b < 0 || s < 0 || d <= 0 || d % ORACLE_FP8_BLOCK != 0) return -1;
+    for (int bi = 0; bi < b; ++bi)
+        if (oracle_apply_rotary(kv + (int64_t)bi * kv_bstride, s, d, rd, 1, s, start_pos, table, table_rows, 0) != 0)
+            return -1;
+    return oracle_kv_quant_ring_write(kv, kv_bstride, ring, ring_bstride, b, s, d, start_pos, window);
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* sparse_attn  ([attn] sparse_attn and Precision; [attend] sparse_attn_kernel, wrapper)       */
 /* ------------------------------------------------------------------------------------------ */
 

@@ -361,6 +361,87 @@ def test_fp8_ring_write_matches_round_trip_and_store(oracle_mod):
 
 
 # ----------------------------------------------------------------------------------------------
+# RoPE (ratio-0 table, rotation of the last rope_dim values, inverse rotation)
+# ----------------------------------------------------------------------------------------------
+
+def _torch_rope_table(npos, dim, base):
+    """The table as the pages build it: f32 frequencies, outer product with the positions, polar."""
+    freqs = 1.0 / (base ** (torch.arange(0, dim, 2, dtype=torch.float32) / dim))
+    ang = torch.outer(torch.arange(npos).float(), freqs)
+    return torch.view_as_real(torch.polar(torch.ones_like(ang), ang)).numpy()
+
+
+def test_rope_table_matches_library(oracle_mod):
+    t = oracle_mod.rope_table(140000, 64, 10000.0)
+    ref = _torch_rope_table(140000, 64, 10000.0)
+    assert np.abs(t - ref).max() <= 1.2e-7          # cos / sin rounded to f32 either way
+    assert (t[0, :, 0] == 1).all() and (t[0, :, 1] == 0).all()
+    t2 = oracle_mod.rope_table(50, 32, 500.0)
+    assert np.abs(t2 - _torch_rope_table(50, 32, 500.0)).max() <= 1.2e-7
+
+
+def _torch_rotary(x: torch.Tensor, table: np.ndarray, pos: np.ndarray, rd: int, inverse: bool) -> torch.Tensor:
+    """The pages' apply_rotary_emb with library complex arithmetic; x [rows][d], pos [rows]."""
+    fc = torch.view_as_complex(torch.from_numpy(table[pos].copy()))
+    if inverse:
+        fc = fc.conj()
+    y = x.clone()
+    xc = torch.view_as_complex(y[:, -rd:].float().unflatten(-1, (-1, 2)))
+    y[:, -rd:] = torch.view_as_real(xc * fc).flatten(-2).to(torch.bfloat16)
+    return y
+
+
+@pytest.mark.parametrize("inverse", [False, True])
+def test_apply_rotary_matches_library(oracle_mod, inverse):
+    g = torch.Generator().manual_seed(12)
+    b, m, h, d, rd, p0 = 2, 5, 3, 128, 64, 1000
+    x = (torch.randn((b, m, h, d), generator=g) * 5).to(torch.bfloat16)
+    table = oracle_mod.rope_table(1100, rd, 10000.0)
+    got = oracle_mod.apply_rotary(to_bits(x), rd, table, p0, h, m, inverse)
+    pos = p0 + (np.arange(b * m * h) // h) % m
+    want = to_bits(_torch_rotary(x.view(-1, d), table, pos, rd, inverse))
+    assert np.array_equal(got.reshape(-1), want.reshape(-1))
+    assert np.array_equal(got.reshape(-1, d)[:, : d - rd], to_bits(x).reshape(-1, d)[:, : d - rd])
+
+
+def test_apply_rotary_properties(oracle_mod):
+    g = torch.Generator().manual_seed(13)
+    x = torch.randn((64, 512), generator=g).to(torch.bfloat16)
+    table = oracle_mod.rope_table(5000, 64, 10000.0)
+    xb = to_bits(x)
+    # position 0 is the identity, exactly
+    assert np.array_equal(oracle_mod.apply_rotary(xb.copy(), 64, table, 0, 64, 1), xb)
+    # the inverse undoes the rotation up to the two bf16 roundings; norms of pairs are kept
+    fwd = oracle_mod.apply_rotary(xb.copy(), 64, table, 4321, 1, 1)
+    back = oracle_mod.apply_rotary(fwd.copy(), 64, table, 4321, 1, 1, inverse=True)
+    x64, f64, b64 = bits_to_f64(xb)[:, -64:], bits_to_f64(fwd)[:, -64:], bits_to_f64(back)[:, -64:]
+    assert np.abs(b64 - x64).max() <= 2 * 2.0 ** -8 * np.abs(x64).max()
+    n0 = x64[:, 0::2] ** 2 + x64[:, 1::2] ** 2
+    n1 = f64[:, 0::2] ** 2 + f64[:, 1::2] ** 2
+    assert np.allclose(n1, n0, rtol=2 ** -6, atol=1e-6)
+    assert not np.array_equal(fwd, xb)
+
+
+def test_rope_ring_write_is_rotation_then_round_trip(oracle_mod):
+    g = torch.Generator().manual_seed(14)
+    b, s, d, W, p0, rd = 2, 12, 64, 8, 0, 32
+    raw = to_bits(torch.randn((b, s, d), generator=g) * 3)
+    table = oracle_mod.rope_table(64, rd, 10000.0)
+    kv = raw.copy()
+    ring = np.zeros((b, W, d), dtype=np.uint16)
+    oracle_mod.kv_rope_quant_ring_write(kv, ring, p0, W, rd, table)
+    want = raw.copy()
+    for bi in range(b):
+        oracle_mod.apply_rotary(want[bi], rd, table, p0, 1, s)
+    want_ring = np.zeros_like(ring)
+    oracle_mod.kv_quant_ring_write(want, want_ring, p0, W)
+    assert np.array_equal(kv, want) and np.array_equal(ring, want_ring)
+    # and the rotation is by each row's own position: row t of sequence 0, done by the library
+    lib_rot = to_bits(_torch_rotary(from_bits(raw[0]).clone(), table, p0 + np.arange(s), rd, False))
+    assert np.array_equal(oracle_mod.act_quant_inplace(lib_rot.reshape(-1)).reshape(s, d), kv[0])
+
+
+# ----------------------------------------------------------------------------------------------
 # sparse_attn
 # ----------------------------------------------------------------------------------------------
 
