@@ -1,7 +1,9 @@
 /*
  * dsattn.h -- C ABI of libdsattn, the GB300 (sm_103a) hot path of DeepSeek-V4.1 sparse latent
  * attention: the sliding-window index rows, the fp8 round trip of new KV rows into the ring,
- * and sparse_attn itself (gathered-row latent attention with an attention sink).
+ * and sparse_attn itself (gathered-row latent attention with an attention sink); beside them the
+ * RoPE rotation (fused into the ring write, or on its own for the output's inverse rotation) and
+ * an fp8 row store that keeps KV rows as their e4m3 codes.
  *
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers, owned by the caller.  The library allocates no
@@ -18,7 +20,8 @@
  *                                            Attention.forward (window + compressed concatenation)
  *   "Module attn" (deepseek_v41_ref)         Precision paragraph, ring-cache paragraph, FP8_BLOCK,
  *                                            act_quant_inplace, pow2_ceil, sparse_attn,
- *                                            window_topk_idxs, WindowCache, attention
+ *                                            window_topk_idxs, WindowCache, attention,
+ *                                            apply_rotary, freqs_cis
  */
 #ifndef DSATTN_H
 #define DSATTN_H
@@ -136,6 +139,40 @@ size_t ds_sparse_attn_workspace_bytes(int b, int m, int h, int d, int topk);
 int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink,
                    const int32_t *idx, int topk, float scale, uint16_t *o, int b, int m, int h, int d,
                    void *workspace, size_t workspace_bytes, ds_stream_t stream);
+
+/*
+ * ds_apply_rotary -- RoPE (or its inverse) on the last rd values of rows of bf16 values, in place.
+ * Sources: "Module attn", apply_rotary, freqs_cis and the Precision paragraph; "DeepSeek V4.1",
+ * attention/query-latent, precompute_freqs_cis, apply_rotary_emb and Attention.forward (RoPE on
+ * the last rope_dim of q and of the kv row; the inverse rotation on the attention output).
+ *
+ * Row r is at position pos = start_pos + (r / rows_per_pos) % positions_per_seq.  For each pair
+ * j < rd / 2 of its last rd values, (a, b) = (x[2j], x[2j+1]) and (c, s) = table[pos][j]
+ * (s negated when inverse != 0):  a' = a c - b s,  b' = a s + b c,  each product and sum rounded
+ * to f32 separately (no fused multiply-add), then to bf16 (nearest even).  Bit-exact with that.
+ *
+ * x          device bf16 [rows][row_len], 16-byte aligned; in/out.  For q or o [b][m][h][d]:
+ *            rows = b m h, row_len = d, rows_per_pos = h, positions_per_seq = m.
+ * table      device f32 [table_rows][rd / 2][2] of (cos, sin), 8-byte aligned: the RoPE table of
+ *            the layer (the ratio-0 layers: freq_j = 1 / base^(2j / rd), angle = pos freq_j)
+ * rd         multiple of 8, <= row_len; row_len multiple of 8.
+ * Errors: DS_EINVAL (null pointer, sizes, alignment, a position >= table_rows).
+ */
+int ds_apply_rotary(uint16_t *x, int64_t rows, int row_len, int rd, int64_t rows_per_pos, int64_t positions_per_seq,
+                    int64_t start_pos, const float *table, int64_t table_rows, int inverse, ds_stream_t stream);
+
+/*
+ * ds_kv_rope_quant_ring_write -- ds_kv_quant_ring_write for a ratio-0 layer's new kv rows with
+ * their RoPE fused in front: the last rd values of row t are first rotated to position
+ * start_pos + t exactly as ds_apply_rotary does (bf16 result), then the block round trip and the
+ * ring store follow ("Module attn": RoPE on the last rope_dim, then the kv row rounded through
+ * fp8 in place, then the ring).  rd is a multiple of 32 (whole blocks), <= d; table as for
+ * ds_apply_rotary, with start_pos + s - 1 < table_rows.  Other arguments and errors are those of
+ * ds_kv_quant_ring_write.
+ */
+int ds_kv_rope_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b, int s,
+                                int d, int64_t start_pos, int window, int rd, const float *table, int64_t table_rows,
+                                ds_stream_t stream);
 
 /*
  * fp8 row store -- KV rows kept as their quantised values instead of the bf16 round trip.

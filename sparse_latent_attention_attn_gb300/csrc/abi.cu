@@ -83,6 +83,32 @@ int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float
     return launch_sparse_attn_tc(a, st);
 }
 
+int ds_apply_rotary(uint16_t *x, int64_t rows, int row_len, int rd, int64_t rows_per_pos, int64_t positions_per_seq,
+                    int64_t start_pos, const float *table, int64_t table_rows, int inverse, ds_stream_t stream) {
+    if (rows < 0 || rd <= 0 || rd % 8 != 0 || row_len < rd || row_len % 8 != 0 || rows_per_pos < 1 ||
+        positions_per_seq < 1 || start_pos < 0)
+        return DS_EINVAL;
+    if (rows == 0) return DS_OK;
+    if (!x || !table || !aligned16(x) || (reinterpret_cast<uintptr_t>(table) & 7u) != 0) return DS_EINVAL;
+    const int64_t groups = (rows - 1) / rows_per_pos + 1;     // rows sharing a position, counted
+    const int64_t span = groups < positions_per_seq ? groups : positions_per_seq;
+    if (start_pos + span - 1 >= table_rows) return DS_EINVAL;   // a position outside the table
+    return launch_apply_rotary(x, rows, row_len, rd, rows_per_pos, positions_per_seq, start_pos, table, inverse != 0,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ds_kv_rope_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b, int s,
+                                int d, int64_t start_pos, int window, int rd, const float *table, int64_t table_rows,
+                                ds_stream_t stream) {
+    if (!kv || !table || b < 0 || s < 0 || d <= 0 || d % 32 != 0 || window < 1 || start_pos < 0) return DS_EINVAL;
+    if (rd <= 0 || rd % 32 != 0 || rd > d || (reinterpret_cast<uintptr_t>(table) & 7u) != 0) return DS_EINVAL;
+    if (s > 0 && start_pos + s - 1 >= table_rows) return DS_EINVAL;
+    if (kv_bstride < (int64_t)s * d || kv_bstride % 8 != 0 || !aligned16(kv)) return DS_EINVAL;
+    if (ring && (ring_bstride < (int64_t)window * d || ring_bstride % 8 != 0 || !aligned16(ring))) return DS_EINVAL;
+    return launch_kv_rope_quant_ring(kv, kv_bstride, ring, ring_bstride, b, s, d, start_pos, window, rd, table,
+                                     reinterpret_cast<cudaStream_t>(stream));
+}
+
 int ds_kv_quantize_fp8(const uint16_t *x, int64_t rows, int d, uint8_t *codes, int8_t *exps, ds_stream_t stream) {
     if (rows < 0 || d <= 0 || d % 32 != 0) return DS_EINVAL;
     if (rows == 0) return DS_OK;

@@ -30,6 +30,12 @@ int launch_kv_quant_ring_fp8(uint16_t *kv, int64_t kv_bstride, uint8_t *codes, i
                              int b, int s, int d, int64_t start_pos, int window, cudaStream_t stream);
 int launch_kv_quantize_fp8(const uint16_t *x, int64_t rows, int d, uint8_t *codes, int8_t *exps,
                            cudaStream_t stream);
+int launch_kv_rope_quant_ring(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b,
+                              int s, int d, int64_t start_pos, int window, int rd, const float *table,
+                              cudaStream_t stream);
+int launch_apply_rotary(uint16_t *x, int64_t rows, int row_len, int rd, int64_t rows_per_pos,
+                        int64_t positions_per_seq, int64_t start_pos, const float *table, bool inverse,
+                        cudaStream_t stream);
 
 struct AttnArgs {
     const uint16_t *q;

@@ -88,13 +88,31 @@ __device__ __forceinline__ void store_block32(uint16_t *dst, const uint32_t (&w)
     for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
+// One row piece of 16 bf16 pairs rotated by the (cos, sin) pairs at cs: each pair a + ib times
+// c + is in f32 with every product and sum rounded on its own (no fused multiply-add), then
+// rounded to bf16 -- the order the RoPE definition writes.
+__device__ __forceinline__ void rotate16(uint32_t (&w)[16], const float2 *__restrict__ cs, bool inverse) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float a = bf16_lo(w[i]), b = bf16_hi(w[i]);
+        const float2 t = cs[i];
+        const float sn = inverse ? -t.y : t.y;
+        const float re = __fsub_rn(__fmul_rn(a, t.x), __fmul_rn(b, sn));
+        const float im = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, t.x));
+        w[i] = f32_to_bf16_bits(re) | (f32_to_bf16_bits(im) << 16);
+    }
+}
+
 // FP8RING: the ring is an fp8 row store (codes + exponents, ring_bstride in rows); otherwise a
-// bf16 tensor (ring_bstride in elements) that receives the round-tripped row.
-template <bool FP8RING>
+// bf16 tensor (ring_bstride in elements) that receives the round-tripped row.  ROPE: the blocks
+// of the last rd values of row t are first rotated to position start_pos + t (table: rows of
+// rd / 2 (cos, sin) pairs), as the ratio-0 layer does before the round trip.
+template <bool FP8RING, bool ROPE = false>
 __global__ void __launch_bounds__(256) kv_quant_ring_kernel(uint16_t *__restrict__ kv, int64_t kv_bstride,
                                                             uint16_t *__restrict__ ring, uint8_t *__restrict__ codes,
                                                             int8_t *__restrict__ exps, int64_t ring_bstride,
-                                                            int b, int s, int d, int64_t start_pos, int window) {
+                                                            int b, int s, int d, int64_t start_pos, int window,
+                                                            int rd = 0, const float2 *__restrict__ table = nullptr) {
     // a kernel launched after this one as a programmatic dependent (the attention kernel) may be
     // scheduled as soon as every block of this grid is running; it still waits for this grid to
     // finish (griddepcontrol.wait) before it reads the ring
@@ -111,6 +129,10 @@ __global__ void __launch_bounds__(256) kv_quant_ring_kernel(uint16_t *__restrict
         uint32_t w[16], rt[16], cd[8];
         int k;
         load_block32(src, w);
+        if constexpr (ROPE) {
+            if (c * 32 >= d - rd)
+                rotate16(w, table + (start_pos + t) * (rd / 2) + (c * 32 - (d - rd)) / 2, false);
+        }
         quant_block32(w, rt, cd, k);
         store_block32(src, rt);
         if (t >= s - window) {
@@ -169,6 +191,17 @@ int launch_kv_quant_ring_fp8(uint16_t *kv, int64_t kv_bstride, uint8_t *codes, i
     if (total == 0) return DS_OK;
     kv_quant_ring_kernel<true><<<(unsigned)grid_for(total), 256, 0, stream>>>(
         kv, kv_bstride, nullptr, codes, exps, ring_bstride, b, s, d, start_pos, window);
+    return launch_status();
+}
+
+int launch_kv_rope_quant_ring(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b,
+                              int s, int d, int64_t start_pos, int window, int rd, const float *table,
+                              cudaStream_t stream) {
+    const int64_t total = (int64_t)b * s * (d / 32);
+    if (total == 0) return DS_OK;
+    kv_quant_ring_kernel<false, true><<<(unsigned)grid_for(total), 256, 0, stream>>>(
+        kv, kv_bstride, ring, nullptr, nullptr, ring_bstride, b, s, d, start_pos, window, rd,
+        reinterpret_cast<const float2 *>(table));
     return launch_status();
 }
 

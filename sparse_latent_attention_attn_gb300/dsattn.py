@@ -46,6 +46,10 @@ _lib.ds_sparse_attn_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.ds_sparse_attn_workspace_bytes.restype = _sz
 _lib.ds_sparse_attn.argtypes = [_P, _P, _i64, _P, _P, _i32, _f32, _P, _i32, _i32, _i32, _i32, _P, _sz, _P]
 _lib.ds_sparse_attn.restype = _i32
+_lib.ds_apply_rotary.argtypes = [_P, _i64, _i32, _i32, _i64, _i64, _i64, _P, _i64, _i32, _P]
+_lib.ds_apply_rotary.restype = _i32
+_lib.ds_kv_rope_quant_ring_write.argtypes = [_P, _i64, _P, _i64, _i32, _i32, _i32, _i64, _i32, _i32, _P, _i64, _P]
+_lib.ds_kv_rope_quant_ring_write.restype = _i32
 _lib.ds_kv_quantize_fp8.argtypes = [_P, _i64, _i32, _P, _P, _P]
 _lib.ds_kv_quantize_fp8.restype = _i32
 _lib.ds_kv_quant_ring_write_fp8.argtypes = [_P, _i64, _P, _P, _i64, _i32, _i32, _i32, _i64, _i32, _P]
@@ -154,6 +158,50 @@ def sparse_attn(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor, idx: torc
            _lib.ds_sparse_attn(_ptr(q), _ptr(kv), n, _ptr(sink), _ptr(idx), topk, float(scale), _ptr(o), b, m, h, d,
                                _ptr(workspace), ws_bytes, _stream(stream)))
     return o
+
+
+def _check_table(table: torch.Tensor, rd: int) -> None:
+    _need(table, torch.float32, "table")
+    if table.dim() != 3 or table.shape[1] * 2 != rd or table.shape[2] != 2 or not table.is_contiguous():
+        raise ValueError("table must be a contiguous f32 [positions][rd/2][2] of (cos, sin)")
+
+
+def apply_rotary(x: torch.Tensor, rd: int, table: torch.Tensor, start_pos: int, rows_per_pos: int,
+                 positions_per_seq: int, inverse: bool = False, stream=None) -> torch.Tensor:
+    """Rotate the last ``rd`` values of every row of ``x [..., row_len]`` (bf16, contiguous) in place;
+    row r is at position start_pos + (r // rows_per_pos) % positions_per_seq.  For q or o
+    ``[b][m][h][d]``: rows_per_pos = h, positions_per_seq = m."""
+    _need(x, torch.bfloat16, "x")
+    _check_table(table, rd)
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    row_len = x.shape[-1]
+    _check("ds_apply_rotary",
+           _lib.ds_apply_rotary(_ptr(x), x.numel() // row_len if row_len else 0, row_len, rd, rows_per_pos,
+                                positions_per_seq, start_pos, _ptr(table), table.shape[0], 1 if inverse else 0,
+                                _stream(stream)))
+    return x
+
+
+def kv_rope_quant_ring_write(kv: torch.Tensor, ring: torch.Tensor | None, start_pos: int, window: int, rd: int,
+                             table: torch.Tensor, stream=None) -> None:
+    """RoPE on the last ``rd`` values of ``kv`` [b][s][d] (row t at start_pos + t), then the fp8
+    round trip in place and the ring store (see ``kv_quant_ring_write``)."""
+    _need(kv, torch.bfloat16, "kv")
+    _check_table(table, rd)
+    b, s, d = kv.shape
+    if kv.stride(2) != 1 or kv.stride(1) != d:
+        raise ValueError("kv rows must be contiguous")
+    ring_bstride = 0
+    if ring is not None:
+        _need(ring, torch.bfloat16, "ring")
+        if ring.shape[0] != b or ring.shape[2] != d or ring.shape[1] < window or ring.stride(2) != 1 \
+                or ring.stride(1) != d:
+            raise ValueError("ring must be [b][>=window][d] with contiguous rows")
+        ring_bstride = ring.stride(0)
+    _check("ds_kv_rope_quant_ring_write",
+           _lib.ds_kv_rope_quant_ring_write(_ptr(kv), kv.stride(0), _ptr(ring), ring_bstride, b, s, d, start_pos,
+                                            window, rd, _ptr(table), table.shape[0], _stream(stream)))
 
 
 def kv_quantize_fp8(x: torch.Tensor, codes: torch.Tensor | None = None, exps: torch.Tensor | None = None,

@@ -27,7 +27,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("ds_window_topk_idxs", "ds_kv_quant_ring_write", "ds_sparse_attn",
                      "ds_sparse_attn_workspace_bytes", "ds_device_status", "ds_status_string",
-                     "ds_kv_quantize_fp8", "ds_kv_quant_ring_write_fp8", "ds_sparse_attn_fp8kv"):
+                     "ds_kv_quantize_fp8", "ds_kv_quant_ring_write_fp8", "ds_sparse_attn_fp8kv",
+                     "ds_apply_rotary", "ds_kv_rope_quant_ring_write"):
         assert required in names
 
 
@@ -98,6 +99,25 @@ def test_fp8_store_argument_checks(lib):
     assert f(fake, None, fake, 10, fake, fake, 4, 0.1, fake, 1, 1, 4, 512, None, 0, None) == -1
     assert f(fake, fake, None, 10, fake, fake, 4, 0.1, fake, 1, 1, 4, 512, None, 0, None) == -1
     assert f(fake, P(4104), fake, 10, fake, fake, 4, 0.1, fake, 1, 1, 4, 512, None, 0, None) == -1
+
+
+def test_rope_argument_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    r = lib.ds_apply_rotary
+    r.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P,
+                  ctypes.c_int64, ctypes.c_int, P]
+    assert r(fake, 4, 64, 12, 1, 1, 0, fake, 10, 0, None) == -1     # rd not a multiple of 8
+    assert r(fake, 4, 64, 128, 1, 1, 0, fake, 10, 0, None) == -1    # rd > row_len
+    assert r(fake, 9, 64, 32, 3, 3, 8, fake, 10, 0, None) == -1     # rows at positions 8, 9, 10: 10 is past the table
+    assert r(None, 4, 64, 32, 1, 1, 0, fake, 10, 0, None) == -1
+    assert r(fake, 0, 64, 32, 1, 1, 0, fake, 10, 0, None) == 0      # nothing to do
+    k = lib.ds_kv_rope_quant_ring_write
+    k.argtypes = [P, ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                  ctypes.c_int, ctypes.c_int, P, ctypes.c_int64, P]
+    assert k(fake, 64, None, 0, 1, 1, 64, 0, 8, 48, fake, 10, None) == -1   # rd not whole blocks
+    assert k(fake, 64, None, 0, 1, 1, 64, 10, 8, 32, fake, 10, None) == -1  # position 10 outside the table
+    assert k(fake, 64, None, 0, 1, 1, 64, 0, 8, 32, None, 10, None) == -1
 
 
 def test_workspace_query_is_host_only(lib):

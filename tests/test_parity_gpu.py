@@ -519,3 +519,59 @@ def test_attn_fp8kv_timed_out_wait_is_reported(ds, monkeypatch):
     ref = oracle.sparse_attn(bits(q), dec, sink.numpy(), idx.numpy(), 512 ** -0.5)
     assert_close_bf16(bits(o), ref)
     assert ds.device_status() == 0
+
+
+# ----------------------------------------------------------------------------------------------
+# RoPE: the rotation (and its inverse) and the RoPE-then-round-trip ring write
+# ----------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("b,m,h,d,rd,p0,inverse", [(2, 3, 4, 128, 64, 100, False), (2, 3, 4, 128, 64, 100, True),
+                                                   (4, 1, 128, 512, 64, 131072, True), (1, 40, 8, 64, 32, 0, False),
+                                                   (3, 1, 5, 512, 512, 9, False)])
+def test_apply_rotary_bit_exact(ds, b, m, h, d, rd, p0, inverse):
+    g = torch.Generator().manual_seed(100 + d + m)
+    x = (torch.randn((b, m, h, d), generator=g) * 4).to(torch.bfloat16)
+    table = oracle.rope_table(p0 + m, rd, 10000.0)
+    want = oracle.apply_rotary(bits(x).copy(), rd, table, p0, h, m, inverse)
+    xg = x.cuda()
+    ds.apply_rotary(xg, rd, torch.from_numpy(table).cuda(), p0, h, m, inverse)
+    assert np.array_equal(bits(xg), want)
+
+
+@pytest.mark.parametrize("b,s,d,W,p0,rd", [(1, 12, 64, 8, 0, 32), (3, 20, 64, 8, 37, 64), (4, 1, 512, 128, 10000, 64),
+                                           (2, 300, 512, 128, 0, 64)])
+def test_kv_rope_ring_write_bit_exact(ds, b, s, d, W, p0, rd):
+    g = torch.Generator().manual_seed(200 + s)
+    raw = (torch.randn((b, s, d), generator=g) * torch.exp(torch.randn((b, s, 1), generator=g) * 2)).to(torch.bfloat16)
+    table = oracle.rope_table(p0 + s, rd, 10000.0)
+    kv_o = bits(raw).copy()
+    ring_o = np.zeros((b, W, d), dtype=np.uint16)
+    oracle.kv_rope_quant_ring_write(kv_o, ring_o, p0, W, rd, table)
+    kv = raw.cuda()
+    ring = torch.zeros((b, W, d), dtype=torch.bfloat16, device="cuda")
+    ds.kv_rope_quant_ring_write(kv, ring, p0, W, rd, torch.from_numpy(table).cuda())
+    assert np.array_equal(bits(kv), kv_o)
+    assert np.array_equal(bits(ring), ring_o)
+
+
+def test_apply_rotary_rate(ds):
+    """The inverse rotation of decode_large's output (256 tokens x 128 heads x 512, last 64 values
+    rotated) as a memory-bound kernel: CUDA events over repeated launches, printed as GB/s of the
+    bytes it must move (the rotated 128 bytes of each row read and written, the table row read)."""
+    b, h, d, rd, p0 = 256, 128, 512, 64, 131072
+    o = torch.randn((b, 1, h, d), device="cuda").to(torch.bfloat16)
+    table = torch.from_numpy(oracle.rope_table(p0 + 1, rd, 10000.0)).cuda()
+    for _ in range(3):
+        ds.apply_rotary(o, rd, table, p0, h, 1, True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 50
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(n):
+        ds.apply_rotary(o, rd, table, p0, h, 1, True)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    moved = b * h * rd * 2 * 2 + rd * 4
+    print(f"\napply_rotary on decode_large's o: {us:.2f} us per launch, {moved / us / 1e3:.0f} GB/s of {moved} bytes")
+    assert us > 0
