@@ -12,7 +12,11 @@
  *   [latent]   "DeepSeek V4.1", blocks/.../attention/query-latent: Attention.__init__
  *              (window_kv_cache ring buffer), Attention.forward (window + compressed concat).
  *   [attn]     "Module attn" (deepseek_v41_ref API page): the Precision paragraph, the ring-cache
- *              paragraph, FP8_BLOCK, act_quant_inplace, pow2_ceil, sparse_attn, window_topk_idxs.
+ *              paragraph, FP8_BLOCK, act_quant_inplace, pow2_ceil, sparse_attn, window_topk_idxs,
+ *              apply_rotary, freqs_cis.
+ *   [latent] also gives precompute_freqs_cis and apply_rotary_emb (RoPE) and the remark that the
+ *              compressed cache holds quantised values (the fp8 row store below keeps them as
+ *              e4m3 codes plus scale exponents).
  *
  * Everything here is written as plain loops in the order the pages state the steps.  The
  * precision is the pages' own: the fp8 round trip decides its scale in f32 ([attn] pow2_ceil
