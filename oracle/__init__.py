@@ -73,6 +73,8 @@ def _load():
         lib.oracle_apply_rotary.restype = i32
         lib.oracle_kv_rope_quant_ring_write.argtypes = [P, i64, P, i64, i32, i32, i32, i64, i32, i32, P, i64]
         lib.oracle_kv_rope_quant_ring_write.restype = i32
+        lib.oracle_indexer_topk.argtypes = [P, P, P, i32, i32, i32, i32, i64, i64, i32, i32, i64, P, P]
+        lib.oracle_indexer_topk.restype = i32
         attn_args = [P, P, i64, P, P, i32, f32, P, i32, i32, i32, i32, P, i64, i32]
         lib.oracle_sparse_attn.argtypes = attn_args
         lib.oracle_sparse_attn.restype = i32
@@ -200,6 +202,25 @@ def kv_rope_quant_ring_write(kv_bits: np.ndarray, ring_bits: np.ndarray, start_p
                                                  table.shape[0])
     if rc != 0:
         raise ValueError("kv_rope_quant_ring_write: bad arguments")
+
+
+def indexer_topk(q_bits: np.ndarray, k_bits: np.ndarray, w: np.ndarray, start_pos: int, ratio: int, topk: int,
+                 offset: int = 0, return_scores: bool = False):
+    """Indexer scores and top-k: q_bits ``[b][s][H][D]``, k_bits ``[b][T][D]`` (bf16 bits), w
+    ``[b][s][H]`` f32.  Returns idx ``[b][s][kk]`` int32 (and scores ``[b][s][T]`` f32)."""
+    assert q_bits.dtype == np.uint16 and k_bits.dtype == np.uint16 and w.dtype == np.float32
+    b, s, H, D = q_bits.shape
+    T = k_bits.shape[1]
+    assert k_bits.shape == (b, T, D) and w.shape == (b, s, H)
+    kk = min(topk, (start_pos + s) // ratio)
+    idx = np.empty((b, s, max(kk, 0)), dtype=np.int32)
+    scores = np.empty((b, s, T), dtype=np.float32) if return_scores else None
+    got = _load().oracle_indexer_topk(_ptr(np.ascontiguousarray(q_bits)), _ptr(np.ascontiguousarray(k_bits)),
+                                      _ptr(np.ascontiguousarray(w)), b, s, H, D, T, start_pos, ratio, topk, offset,
+                                      None if scores is None else _ptr(scores), _ptr(idx))
+    if got != kk:
+        raise ValueError("indexer_topk: bad arguments (fewer compressed keys than the top-k needs?)")
+    return (idx, scores) if return_scores else idx
 
 
 def sparse_attn(q_bits: np.ndarray, kv_bits: np.ndarray, sink: np.ndarray, idx: np.ndarray, scale: float,

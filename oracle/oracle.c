@@ -363,6 +363,89 @@ int oracle_kv_rope_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* Indexer scoring and top-k  ([latent] Indexer.forward: the index score of every compressed   */
+/* position, the causal compress_lens mask, top-k re-sorted by position, -1 and the offset)    */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * For sequence bi and query i (position start_pos + i) over compressed positions t < T:
+ *   score[t] = sum_h relu(dot(q[bi][i][h], k[bi][t])) * w[bi][i][h]      (f32, h and d in order)
+ * q and k are taken as given: their RoPE and fp4 rounding happen before (the pages only name the
+ * fp4 step), and w already holds the weights projection times softmax_scale * H^-0.5.
+ * compress_lens = (start_pos + i + 1) / ratio (integer division): positions t >= compress_lens
+ * are not visible yet (score -inf in the prefill; in a decode step T equals it).
+ * kk = min(topk, (start_pos + s) / ratio) entries are kept: the kk largest scores, equal scores
+ * by the smaller position first (the pages leave the order of ties open; this is one valid
+ * choice), re-sorted by position; an entry t >= compress_lens becomes -1, the others t + offset.
+ * idx_out[bi][i][0..kk), scores_out[bi][i][0..T) (optional).  Returns kk, or -1.
+ */
+static int cmp_desc_score(const void *pa, const void *pb, void *ctx) {
+    const float *sc = (const float *)ctx;
+    int64_t a = *(const int64_t *)pa, b = *(const int64_t *)pb;
+    if (sc[a] > sc[b]) return -1;
+    if (sc[a] < sc[b]) return 1;
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+static int cmp_i64(const void *pa, const void *pb) {
+    int64_t a = *(const int64_t *)pa, b = *(const int64_t *)pb;
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+/* insertion sort with a context (qsort_r is not portable C11); the oracle's sizes are small */
+static void sort_ctx(int64_t *v, int64_t n, int (*cmp)(const void *, const void *, void *), void *ctx) {
+    for (int64_t i = 1; i < n; ++i) {
+        int64_t x = v[i], j = i - 1;
+        while (j >= 0 && cmp(&v[j], &x, ctx) > 0) {
+            v[j + 1] = v[j];
+            --j;
+        }
+        v[j + 1] = x;
+    }
+}
+
+int oracle_indexer_topk(const uint16_t *q, const uint16_t *k, const float *w, int b, int s, int H, int D, int64_t T,
+                        int64_t start_pos, int ratio, int topk, int64_t offset, float *scores_out, int32_t *idx_out) {
+    if (b < 0 || s < 1 || H < 1 || D < 1 || T < 0 || start_pos < 0 || ratio < 1 || topk < 0) return -1;
+    int64_t kk = (start_pos + s) / ratio;
+    if (kk > topk) kk = topk;
+    if (kk > T) return -1;
+    float *sc = (float *)malloc(sizeof(float) * (size_t)(T > 0 ? T : 1));
+    int64_t *ord = (int64_t *)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1));
+    if (!sc || !ord) {
+        free(sc);
+        free(ord);
+        return -1;
+    }
+    for (int bi = 0; bi < b; ++bi) {
+        for (int i = 0; i < s; ++i) {
+            const int64_t lens = (start_pos + i + 1) / ratio;
+            for (int64_t t = 0; t < T; ++t) {
+                float acc = 0.0f;
+                for (int h = 0; h < H; ++h) {
+                    const uint16_t *qv = q + (((int64_t)bi * s + i) * H + h) * D;
+                    const uint16_t *kv = k + ((int64_t)bi * T + t) * D;
+                    float dot = 0.0f;
+                    for (int d = 0; d < D; ++d) dot += bf16_bits_to_f32(qv[d]) * bf16_bits_to_f32(kv[d]);
+                    float r = dot > 0.0f ? dot : 0.0f;
+                    acc += r * w[((int64_t)bi * s + i) * H + h];
+                }
+                sc[t] = t < lens ? acc : -INFINITY;
+                if (scores_out) scores_out[((int64_t)bi * s + i) * T + t] = sc[t];
+            }
+            for (int64_t t = 0; t < T; ++t) ord[t] = t;
+            sort_ctx(ord, T, cmp_desc_score, sc);
+            qsort(ord, (size_t)kk, sizeof(int64_t), cmp_i64);
+            int32_t *out = idx_out + ((int64_t)bi * s + i) * kk;
+            for (int64_t j = 0; j < kk; ++j) out[j] = ord[j] < lens ? (int32_t)(ord[j] + offset) : -1;
+        }
+    }
+    free(sc);
+    free(ord);
+    return (int)kk;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* sparse_attn  ([attn] sparse_attn and Precision; [attend] sparse_attn_kernel, wrapper)       */
 /* ------------------------------------------------------------------------------------------ */
 

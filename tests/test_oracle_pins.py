@@ -442,6 +442,81 @@ def test_rope_ring_write_is_rotation_then_round_trip(oracle_mod):
 
 
 # ----------------------------------------------------------------------------------------------
+# Indexer scoring and top-k
+# ----------------------------------------------------------------------------------------------
+
+def _indexer_case(seed, b=2, s=24, H=4, D=32, ratio=4, start_pos=0):
+    g = torch.Generator().manual_seed(seed)
+    T = (start_pos + s) // ratio
+    q = torch.randn((b, s, H, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((b, T, D), generator=g).to(torch.bfloat16)
+    w = torch.rand((b, s, H), generator=g) * 0.2
+    return q, k, w
+
+
+def test_indexer_scores_match_library(oracle_mod):
+    q, k, w = _indexer_case(30)
+    idx, sc = oracle_mod.indexer_topk(to_bits(q), to_bits(k), w.numpy(), 0, 4, 3, return_scores=True)
+    dots = torch.einsum("bshd,btd->bsht", q.double(), k.double()).relu()
+    ref = (dots * w.double().unsqueeze(-1)).sum(dim=2)
+    lens = (torch.arange(1, 25) // 4).view(1, -1, 1)
+    ref = ref.masked_fill(torch.arange(6).view(1, 1, -1) >= lens, -math.inf)
+    fin = np.isfinite(sc)
+    assert np.array_equal(fin, np.isfinite(ref.numpy()))
+    assert np.allclose(sc[fin], ref.numpy()[fin], rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("start_pos,s,topk,offset", [(0, 24, 3, 0), (0, 40, 64, 128), (37, 1, 5, 128), (400, 1, 50, 7)])
+def test_indexer_topk_matches_library_selection(oracle_mod, start_pos, s, topk, offset):
+    q, k, w = _indexer_case(31 + start_pos, s=s, start_pos=start_pos)
+    idx, sc = oracle_mod.indexer_topk(to_bits(q), to_bits(k), w.numpy(), start_pos, 4, topk, offset,
+                                      return_scores=True)
+    kk = min(topk, (start_pos + s) // 4)
+    assert idx.shape == (2, s, kk)
+    sct = torch.from_numpy(sc)
+    for bi in range(2):
+        for i in range(s):
+            lens = (start_pos + i + 1) // 4
+            want_valid = sorted(t for t in torch.topk(sct[bi, i], kk).indices.tolist() if t < lens)
+            row = idx[bi, i]
+            assert [int(v) - offset for v in row if v >= 0] == want_valid       # ascending, shifted
+            assert (row == -1).sum() == kk - len(want_valid)                     # the rest is -1
+            assert list(row[: len(want_valid)]) == [v + offset for v in want_valid]
+
+
+def test_indexer_properties(oracle_mod):
+    q, k, w = _indexer_case(32, s=32, H=6)
+    base = oracle_mod.indexer_topk(to_bits(q), to_bits(k), w.numpy(), 0, 4, 4)
+    perm = torch.randperm(6, generator=torch.Generator().manual_seed(1))
+    assert np.array_equal(oracle_mod.indexer_topk(to_bits(q[:, :, perm]), to_bits(k), w[:, :, perm].numpy().copy(),
+                                                  0, 4, 4), base)
+    assert np.array_equal(oracle_mod.indexer_topk(to_bits(q), to_bits(k), (w * 4).numpy(), 0, 4, 4), base)
+    # a head with weight 0 does not matter; a key that dominates every head is always selected
+    w0 = w.clone()
+    w0[:, :, 2] = 0
+    q2 = q.clone()
+    q2[:, :, 2] = torch.randn_like(q2[:, :, 2].float()).to(torch.bfloat16)
+    assert np.array_equal(oracle_mod.indexer_topk(to_bits(q2), to_bits(k), w0.numpy(), 0, 4, 4),
+                          oracle_mod.indexer_topk(to_bits(q), to_bits(k), w0.numpy(), 0, 4, 4))
+    k2 = k.clone()
+    k2[:, 1] = q.float().mean(dim=(1, 2)).mul(50).to(torch.bfloat16)
+    got = oracle_mod.indexer_topk(to_bits(q), to_bits(k2), w.numpy(), 0, 4, 4)
+    for i in range(4, 32):          # visible from query 7 on (compress_lens = (i + 1) // 4 > 1)
+        if (i + 1) // 4 > 1:
+            assert 1 in got[:, i].tolist()[0] and 1 in got[:, i].tolist()[1]
+
+
+def test_indexer_prefill_row_equals_decode_step(oracle_mod):
+    q, k, w = _indexer_case(33, b=1, s=40, H=3)
+    pre = oracle_mod.indexer_topk(to_bits(q), to_bits(k), w.numpy(), 0, 4, 6)
+    for i in (3, 7, 20, 39):
+        T = (i + 1) // 4
+        dec = oracle_mod.indexer_topk(to_bits(q[:, i:i + 1]).copy(), to_bits(k[:, :T]).copy(),
+                                      w[:, i:i + 1].numpy().copy(), i, 4, 6)
+        assert [v for v in pre[0, i] if v >= 0] == [v for v in dec[0, 0] if v >= 0]
+
+
+# ----------------------------------------------------------------------------------------------
 # sparse_attn
 # ----------------------------------------------------------------------------------------------
 
