@@ -575,3 +575,39 @@ def test_apply_rotary_rate(ds):
     moved = b * h * rd * 2 * 2 + rd * 4
     print(f"\napply_rotary on decode_large's o: {us:.2f} us per launch, {moved / us / 1e3:.0f} GB/s of {moved} bytes")
     assert us > 0
+
+
+# ----------------------------------------------------------------------------------------------
+# output canaries: every write of a call stays inside its output and workspace
+# ----------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("d,h,b,m,topk", [(512, 64, 100, 2, 300), (512, 128, 1, 1, 5000), (64, 8, 300, 1, 200)])
+def test_writes_stay_inside_o_and_workspace(ds, fp8, d, h, b, m, topk):
+    """o sits between two 128-byte canary bands inside a larger buffer, the workspace has a 4 KB
+    canary band after the size the library asks for; after the call every canary byte is as it
+    was and o matches the oracle (shapes with cut tokens, so the workspace is used)."""
+    if fp8 and d != 512:
+        pytest.skip("the fp8 row store is read by the d = 512 kernel")
+    q, kv, sink, idx = _case(300 + d + b, b, m, h, d, 2 * topk, topk, 0.05)
+    pad, canary = 64, 0x5A5A
+    big = torch.full((q.numel() + 2 * pad,), canary, dtype=torch.int16, device="cuda")
+    o = big[pad:pad + q.numel()].view(torch.bfloat16).view(q.shape)
+    need = ds.sparse_attn_workspace_bytes(b, m, h, d, topk)
+    ws_big = torch.full((need + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+    ws = ws_big[:need] if need else None
+    if fp8:
+        kv = _spread_rows(300 + b, b * 2 * topk, d).view(b, 2 * topk, d)
+        codes, exps = ds.kv_quantize_fp8(kv.cuda())
+        ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), d ** -0.5, o=o, workspace=ws)
+        kv_ref = oracle.kv_dequantize_fp8(codes.cpu().numpy(), exps.cpu().numpy())
+    else:
+        ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), d ** -0.5, o=o, workspace=ws)
+        kv_ref = bits(kv)
+    torch.cuda.synchronize()
+    bb = big.cpu()
+    assert (bb[:pad] == canary).all() and (bb[pad + q.numel():] == canary).all()
+    assert (ws_big[need:].cpu() == 0xA5).all()
+    ref = oracle.sparse_attn(bits(q), kv_ref, sink.numpy(), idx.numpy(), d ** -0.5)
+    assert_close_bf16(bits(o), ref)
+    assert ds.device_status() == 0
