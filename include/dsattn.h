@@ -47,10 +47,8 @@ typedef struct CUstream_st *ds_stream_t;
 /* Bits of the device status word (ds_device_status). */
 #define DS_DEV_TIMEOUT 1u     /* a bounded wait inside a kernel gave up; that launch's output is invalid */
 /* Every wait inside ds_sparse_attn's kernel gives up after 2 s, sets DS_DEV_TIMEOUT, drains the
- * launch's own copies and MMAs and returns, so the context stays usable.  To exercise that path,
- * a call made while the environment variable DSATTN_TEST_STALL is "1" has its gather warps
- * withhold the first tile's arrivals: the call takes about 2 s, its output is invalid and
- * DS_DEV_TIMEOUT is raised.  Nothing sets the variable; it exists for tests. */
+ * launch's own copies and MMAs and returns, so the context stays usable (ds_test_set_stall
+ * exercises that path). */
 #define DS_DEV_BAD_INDEX 2u   /* an index >= n was seen; the entry was skipped                       */
 
 /*
@@ -258,6 +256,15 @@ size_t ds_sparse_attn_static_scratch_capacity(void);
  * DS_ECUDA.  This is the only call that synchronises.
  */
 int ds_device_status(ds_stream_t stream, unsigned int *bits_out);
+
+/*
+ * ds_test_set_stall -- test hook for the bounded waits (no counterpart on the pages).  While `on`
+ * is nonzero (process-wide, every device), each ds_sparse_attn / ds_sparse_attn_fp8kv launch has
+ * its gather warps withhold the first tile's arrivals: the launch's waits run out after about
+ * 2 s, it drains its own copies and MMAs, raises DS_DEV_TIMEOUT and returns with its output
+ * invalid; no GPU fault is involved.  Default off; nothing in the library turns it on.
+ */
+void ds_test_set_stall(int on);
 
 /* ds_status_string -- static text for a status code. */
 const char *ds_status_string(int status);

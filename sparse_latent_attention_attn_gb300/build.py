@@ -72,7 +72,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) 
             if log.strip():
                 print(log, file=sys.stderr)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, "-shared", "-gencode", GENCODE, "-o", tmp, *[o for o, _ in results]]
+    cmd = [nvcc, "-shared", "-gencode", GENCODE, "-o", tmp, *[o for o, _ in results], "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")

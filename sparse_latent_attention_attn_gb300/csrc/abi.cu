@@ -1,5 +1,7 @@
 // abi.cu -- the extern "C" entry points of libdsattn (declared in include/dsattn.h): argument
-// checks, the per-device status word, and dispatch to the kernels.
+// checks, the per-device status word, NVTX ranges, and dispatch to the kernels.
+#include <nvtx3/nvToolsExt.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -31,6 +33,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
 
+// An NVTX range around each entry point, named after it, so a timeline tool shows where each
+// call's host work (checks, launch) starts and ends.  Without a tool attached it costs a check.
+struct Range {
+    explicit Range(const char *name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+};
+
 }  // namespace
 }  // namespace dsattn
 
@@ -40,6 +49,7 @@ extern "C" {
 
 int ds_window_topk_idxs(int32_t *idx, int64_t ld, int b, int s, int64_t start_pos, int window, int *cols_out,
                         ds_stream_t stream) {
+    const Range range("ds_window_topk_idxs");
     if (!idx || b < 0 || s < 1 || window < 1 || start_pos < 0) return DS_EINVAL;
     if (start_pos > 0 && s != 1) return DS_EUNSUPPORTED;
     const int cols = start_pos == 0 ? (s < window ? s : window) : window;
@@ -51,6 +61,7 @@ int ds_window_topk_idxs(int32_t *idx, int64_t ld, int b, int s, int64_t start_po
 
 int ds_kv_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b, int s,
                            int d, int64_t start_pos, int window, ds_stream_t stream) {
+    const Range range("ds_kv_quant_ring_write");
     if (!kv || b < 0 || s < 0 || d <= 0 || d % 32 != 0 || window < 1 || start_pos < 0) return DS_EINVAL;
     if (kv_bstride < (int64_t)s * d || kv_bstride % 8 != 0 || !aligned16(kv)) return DS_EINVAL;
     if (ring && (ring_bstride < (int64_t)window * d || ring_bstride % 8 != 0 || !aligned16(ring))) return DS_EINVAL;
@@ -66,6 +77,7 @@ size_t ds_sparse_attn_workspace_bytes(int b, int m, int h, int d, int topk) {
 int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink, const int32_t *idx,
                    int topk, float scale, uint16_t *o, int b, int m, int h, int d, void *workspace,
                    size_t workspace_bytes, ds_stream_t stream) {
+    const Range range("ds_sparse_attn");
     if (b < 0 || m < 0 || n < 0 || topk < 0 || h < 1) return DS_EINVAL;
     if (!supported_head_dim(d) || h > 128) return DS_EUNSUPPORTED;
     if ((int64_t)b * m == 0) return DS_OK;
@@ -85,6 +97,7 @@ int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float
 
 int ds_apply_rotary(uint16_t *x, int64_t rows, int row_len, int rd, int64_t rows_per_pos, int64_t positions_per_seq,
                     int64_t start_pos, const float *table, int64_t table_rows, int inverse, ds_stream_t stream) {
+    const Range range("ds_apply_rotary");
     if (rows < 0 || rd <= 0 || rd % 8 != 0 || row_len < rd || row_len % 8 != 0 || rows_per_pos < 1 ||
         positions_per_seq < 1 || start_pos < 0)
         return DS_EINVAL;
@@ -100,6 +113,7 @@ int ds_apply_rotary(uint16_t *x, int64_t rows, int row_len, int rd, int64_t rows
 int ds_kv_rope_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring, int64_t ring_bstride, int b, int s,
                                 int d, int64_t start_pos, int window, int rd, const float *table, int64_t table_rows,
                                 ds_stream_t stream) {
+    const Range range("ds_kv_rope_quant_ring_write");
     if (!kv || !table || b < 0 || s < 0 || d <= 0 || d % 32 != 0 || window < 1 || start_pos < 0) return DS_EINVAL;
     if (rd <= 0 || rd % 32 != 0 || rd > d || (reinterpret_cast<uintptr_t>(table) & 7u) != 0) return DS_EINVAL;
     if (s > 0 && start_pos + s - 1 >= table_rows) return DS_EINVAL;
@@ -110,6 +124,7 @@ int ds_kv_rope_quant_ring_write(uint16_t *kv, int64_t kv_bstride, uint16_t *ring
 }
 
 int ds_kv_quantize_fp8(const uint16_t *x, int64_t rows, int d, uint8_t *codes, int8_t *exps, ds_stream_t stream) {
+    const Range range("ds_kv_quantize_fp8");
     if (rows < 0 || d <= 0 || d % 32 != 0) return DS_EINVAL;
     if (rows == 0) return DS_OK;
     if (!x || !codes || !exps || !aligned16(x) || !aligned16(codes)) return DS_EINVAL;
@@ -119,6 +134,7 @@ int ds_kv_quantize_fp8(const uint16_t *x, int64_t rows, int d, uint8_t *codes, i
 int ds_kv_quant_ring_write_fp8(uint16_t *kv, int64_t kv_bstride, uint8_t *ring_codes, int8_t *ring_exps,
                                int64_t ring_bstride, int b, int s, int d, int64_t start_pos, int window,
                                ds_stream_t stream) {
+    const Range range("ds_kv_quant_ring_write_fp8");
     if (!kv || !ring_codes || !ring_exps || b < 0 || s < 0 || d <= 0 || d % 32 != 0 || window < 1 || start_pos < 0)
         return DS_EINVAL;
     if (kv_bstride < (int64_t)s * d || kv_bstride % 8 != 0 || !aligned16(kv)) return DS_EINVAL;
@@ -130,6 +146,7 @@ int ds_kv_quant_ring_write_fp8(uint16_t *kv, int64_t kv_bstride, uint8_t *ring_c
 int ds_sparse_attn_fp8kv(const uint16_t *q, const uint8_t *kv_codes, const int8_t *kv_exps, int64_t n,
                          const float *sink, const int32_t *idx, int topk, float scale, uint16_t *o, int b, int m,
                          int h, int d, void *workspace, size_t workspace_bytes, ds_stream_t stream) {
+    const Range range("ds_sparse_attn_fp8kv");
     if (b < 0 || m < 0 || n < 0 || topk < 0 || h < 1) return DS_EINVAL;
     if (d != 512 || h > 128) return DS_EUNSUPPORTED;
     if ((int64_t)b * m == 0) return DS_OK;
@@ -146,6 +163,8 @@ int ds_sparse_attn_fp8kv(const uint16_t *q, const uint8_t *kv_codes, const int8_
     }
     return launch_sparse_attn_tc(a, st);
 }
+
+void ds_test_set_stall(int on) { set_test_stall(on != 0); }
 
 int ds_device_status(ds_stream_t stream, unsigned int *bits_out) {
     unsigned int *p = status_word();

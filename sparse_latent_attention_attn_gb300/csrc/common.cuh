@@ -55,6 +55,7 @@ struct AttnArgs {
 };
 
 int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream);
+void set_test_stall(bool on);
 size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk);
 
 }  // namespace dsattn

@@ -1,9 +1,8 @@
-// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, TMA (tile::gather4), the 5th
+// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, bulk copies, the 5th
 // generation tensor core (tcgen05: TMEM allocation, MMA, loads/stores, commits), cluster
 // shared memory, and bounded waits.  Written from the PTX ISA; each wrapper is one instruction.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -41,10 +40,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
-}
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa), releasing at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 // Remote arrive without release semantics: for "done reading your data" signals, where the
 // reads have already returned their values.
@@ -140,18 +135,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-// Asynchronous 16-byte store into another CTA's shared memory; its arrival is counted in bytes
-// on that CTA's mbarrier `remote_bar` (both addresses from mapa).  No fence is involved.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t remote_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-                 "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
-                 "r"(remote_bar)
-                 : "memory");
-}
 // Bulk copy (copy engine) of `bytes` from this CTA's shared memory into another CTA's shared
 // memory, counted in bytes on that CTA's mbarrier (destination and barrier from mapa).  Both
 // addresses 16-byte aligned, size a multiple of 16.  Part of the issuing thread's bulk group.
@@ -164,16 +147,12 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk copy of this thread has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk copy of this thread is complete (its writes done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-                 : "memory");
-    return v;
 }
 // 256-bit global accesses (32-byte aligned addresses): one request per lane for a full 32-byte
 // sector, half the instructions of 16-byte accesses
@@ -197,9 +176,6 @@ __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
 // ---------------------------------------------------------------------------------------------
 // async copies
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // 16 bytes global -> shared, bypassing L1.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
@@ -225,22 +201,8 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
-// Four rows (r0..r3) of a 2-D tensor, columns [x, x + box width), into consecutive shared rows at
-// dst; completion is counted in bytes on `bar`.  The tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t r0, int32_t r1,
-                                            int32_t r2, int32_t r3, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -17,10 +17,11 @@
 //    MMA can run two tiles ahead of the softmax.
 //  * head_dim 512: O[128 x 512] f32 alone would fill TMEM, so a 2-CTA cluster splits the d columns:
 //    each CTA gathers and multiplies its own 256 columns and the two partial score tiles are summed
-//    through distributed shared memory.  Dedicated exchange warps pack this CTA's partial scores
-//    (3 bytes each) into a local staging buffer and hand them to the copy engine as one bulk copy
-//    per lane quarter into the peer's exchange buffer, while the softmax warps work on the
-//    previous tile; both CTAs then run the identical softmax.
+//    through distributed shared memory.  Dedicated exchange warps copy this CTA's partial scores
+//    (f32, as the tensor core left them) into a local staging buffer and hand them to the copy
+//    engine as one bulk copy per lane quarter into the peer's exchange buffer, while the softmax
+//    warps work on the previous tile; both CTAs add the same two f32 halves (addition commutes, so
+//    the sums are bit-identical) and run the identical softmax.
 //  * Warp roles (16 warps): 0-3 softmax and epilogue (thread = head = TMEM lane); 4-7 and 14-15
 //    row gather, plus 8-11 when d is not split; 8-11 score exchange when it is; 12 index
 //    compaction; 13 TMEM allocation + single-thread MMA issue, in whatever order its inputs
@@ -36,7 +37,7 @@
 //    path while every exponent stays <= 2^8.
 //  * Every wait is bounded: past a time limit the kernel flags DS_DEV_TIMEOUT, drains its own
 //    copies and MMAs, frees TMEM and returns.
-#include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -82,14 +83,12 @@ struct Cfg {
     // memory and hands it to the copy engine as one bulk copy into the peer's exchange buffer, so
     // the slow cluster-network traffic never sits in the warps' memory instruction queues
     // (where it delays every shared-memory access of the softmax warps on the same sub-core).
-    // PACKED: each partial score crosses as the top three bytes of its f32 (see pack3 below),
-    // which makes room for a third exchange buffer next to the staging buffer.
-    static constexpr bool PACKED = true;
-    static constexpr int XB = PACKED ? 3 : 4;       // bytes per exchanged score
+    // Each partial score crosses as its full f32, so the summed score is an f32 evaluation.
+    static constexpr int XB = 4;                    // bytes per exchanged score
     // exchange buffers (tiles of the peer's partial scores).  With the d split, P of tile J is
     // written into exchange buffer J % NX once its scores have been read, and the peer may send
     // tile J + NX there once this CTA's P V of tile J is done.
-    static constexpr int NX = CL == 2 ? (PACKED ? 3 : 2) : 0;
+    static constexpr int NX = CL == 2 ? 2 : 0;
     static constexpr int NXD = NX > 0 ? NX : 1;     // divisor for buffer arithmetic
     // separate P buffers (no d split): the softmax writes P of tile J into buffer J % NP without
     // waiting, because the MMA thread issues S(J) only after P V of tile J - NP (so S(J)'s
@@ -113,7 +112,6 @@ struct Cfg {
     // is 512 contiguous bytes.  P of the tile (128 rows of 128 bytes) is later written over it.
     static constexpr int XQ = 32 * BN * XB;
     static constexpr int X_STRIDE = 4 * XQ;         // one exchange buffer
-    static constexpr int XU = BN * XB / 16;         // 16-byte units per row
     // shared address of P of tile J (relative to the 1024-aligned base)
     __device__ static uint32_t p_off(int J) {
         return NX > 0 ? (uint32_t)(SM_X + (J % NXD) * X_STRIDE) : (uint32_t)(SM_P + (J % NPD) * P_BYTES);
@@ -189,7 +187,7 @@ struct Params {
     int G;            // clusters
     float scale_log2; // softmax scale * log2(e)
     unsigned int *status;
-    // test switch for the timeout path (DSATTN_TEST_STALL): the gather warps withhold their
+    // test switch for the timeout path (ds_test_set_stall): the gather warps withhold their
     // arrivals for the first tile, so a bounded wait runs out
     int stall_first_tile;
 };
@@ -208,29 +206,6 @@ __host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t ntok,
     const int64_t tok = x / TK, r = x - tok * TK;
     return tok * T + (r > K ? r - K : 0);
 }
-
-// Exchange encoding of partial scores (d split): a score crosses the cluster as the top three
-// bytes of its f32 (sign, exponent, 15 mantissa bits) and is rebuilt with byte 0 a copy of byte 1,
-// i.e. within 2^-15 relative of the original; infinities and NaNs stay what they were.  Each CTA
-// applies the same rounding to its own half (round3) before the two halves are added, so both
-// CTAs compute bit-identical scores and take identical softmax decisions.
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-// four scores -> three words: the high halves of a, b; of c, d; then byte 1 of a, b, c, d
-__device__ __forceinline__ void pack3(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t &w0, uint32_t &w1,
-                                      uint32_t &w2) {
-    w0 = prmt(a, b, 0x7632);
-    w1 = prmt(c, d, 0x7632);
-    w2 = prmt(prmt(a, b, 0x0051), prmt(c, d, 0x0051), 0x5410);
-}
-__device__ __forceinline__ float4 unpack3(uint32_t w0, uint32_t w1, uint32_t w2) {
-    return make_float4(__uint_as_float(prmt(w0, w2, 0x1044)), __uint_as_float(prmt(w0, w2, 0x3255)),
-                       __uint_as_float(prmt(w1, w2, 0x1066)), __uint_as_float(prmt(w1, w2, 0x3277)));
-}
-__device__ __forceinline__ float round3(uint32_t x) { return __uint_as_float(prmt(x, x, 0x3211)); }
 
 // Every lane waits for the phase itself (acquire) and the warp proceeds together or not at all,
 // so warp-collective tcgen05 instructions never diverge.  (Measured on this path: one polling
@@ -704,30 +679,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
             if (live_q) {
+                // row i of the quarter: 16-byte unit k at (k * 32 + i) * 16
                 const uint32_t srow = stage_q + lane * 16;
-                if constexpr (C::PACKED) {
-                    // 16 scores -> 12 words -> three 16-byte units, four times
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t w[12];
+                for (int k = 0; k < 8; ++k)
+                    st_shared_v4(srow + k * 512, r0[4 * k], r0[4 * k + 1], r0[4 * k + 2], r0[4 * k + 3]);
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int j = 16 * c + 4 * g;
-                            const uint32_t *v = j < 32 ? r0 + j : r1 + (j - 32);
-                            pack3(v[0], v[1], v[2], v[3], w[3 * g], w[3 * g + 1], w[3 * g + 2]);
-                        }
-#pragma unroll
-                        for (int u = 0; u < 3; ++u)
-                            st_shared_v4(srow + (3 * c + u) * 512, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_shared_v4(srow + k * 512, r0[4 * k], r0[4 * k + 1], r0[4 * k + 2], r0[4 * k + 3]);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_shared_v4(srow + (8 + k) * 512, r1[4 * k], r1[4 * k + 1], r1[4 * k + 2], r1[4 * k + 3]);
-                }
+                for (int k = 0; k < 8; ++k)
+                    st_shared_v4(srow + (8 + k) * 512, r1[4 * k], r1[4 * k + 1], r1[4 * k + 2], r1[4 * k + 3]);
                 fence_proxy_async_smem();                // the copy engine reads what was written here
             }
             // the peer's exchange buffer for tile J is free (its P V of tile J - NX is done)
@@ -737,8 +696,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 bulk_commit_group();
             }
         }
-        // the staging buffer must stay valid until the copy engine has read it
-        if (lane == 0) bulk_wait_read_all();
+        // every copy to the peer must have landed before either CTA of the cluster may exit (the
+        // final cluster barrier comes after this), and the staging buffer must stay valid until
+        // the copy engine has read it: wait for the bulk group to complete, not just its reads
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     } else if (warp < 4) {
         // ============================ softmax + epilogue (warps 0-3) ============================
         setmaxnreg_inc<REG_SOFTMAX>();
@@ -847,9 +809,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     float s[BN];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        // with the d split this CTA's half is rounded exactly as the peer sees it
-                        s[j] = C::CL == 2 && C::PACKED ? round3(r0[j]) : __uint_as_float(r0[j]);
-                        s[32 + j] = C::CL == 2 && C::PACKED ? round3(r1[j]) : __uint_as_float(r1[j]);
+                        s[j] = __uint_as_float(r0[j]);
+                        s[32 + j] = __uint_as_float(r1[j]);
                     }
                     if constexpr (C::CL == 2) {
                         const int xs = J % C::NXD;
@@ -863,37 +824,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                             mbar_arrive_expect_tx(BAR(B_XFULL + xs), (uint32_t)((p.h < 128 ? p.h : 128) + 31) / 32 * C::XQ);
                         const uint32_t xbuf = base + C::SM_X + xs * XSTRIDE + warp * C::XQ + lane * 16;
                         if (live) {
-                            if constexpr (C::PACKED) {
+                            // own half + peer half: the peer adds the same two f32 values
 #pragma unroll
-                                for (int c = 0; c < 4; ++c) {
-                                    uint32_t w[12];
-#pragma unroll
-                                    for (int u = 0; u < 3; ++u) {
-                                        const uint4 q4 = ld_shared_u4(xbuf + (3 * c + u) * 512);
-                                        w[4 * u] = q4.x;
-                                        w[4 * u + 1] = q4.y;
-                                        w[4 * u + 2] = q4.z;
-                                        w[4 * u + 3] = q4.w;
-                                    }
-#pragma unroll
-                                    for (int g = 0; g < 4; ++g) {
-                                        const float4 v = unpack3(w[3 * g], w[3 * g + 1], w[3 * g + 2]);
-                                        const int j = 16 * c + 4 * g;
-                                        s[j] += v.x;
-                                        s[j + 1] += v.y;
-                                        s[j + 2] += v.z;
-                                        s[j + 3] += v.w;
-                                    }
-                                }
-                            } else {
-#pragma unroll
-                                for (int k = 0; k < BN / 4; ++k) {
-                                    const float4 v = ld_shared_v4(xbuf + k * 512);
-                                    s[4 * k] += v.x;
-                                    s[4 * k + 1] += v.y;
-                                    s[4 * k + 2] += v.z;
-                                    s[4 * k + 3] += v.w;
-                                }
+                            for (int k = 0; k < BN / 4; ++k) {
+                                const float4 v = ld_shared_v4(xbuf + k * 512);
+                                s[4 * k] += v.x;
+                                s[4 * k + 1] += v.y;
+                                s[4 * k + 2] += v.z;
+                                s[4 * k + 3] += v.w;
                             }
                         }
                         // the exchange warps tell the peer when this buffer is free again (after
@@ -1093,16 +1031,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if constexpr (C::CL == 2) {
-        // after an abort the peer's score stores may still be on their way into this CTA's
-        // shared memory (a normal run has received every byte): give them time to land
-        if (*abort_flag) {
-            const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < 50000ull) {
-            }
-        }
-        cluster_sync();
-    }
+    // the exchange warps of both CTAs have waited for their copies into the peer to complete, so
+    // after this barrier nothing is on its way into either CTA's shared memory
+    if constexpr (C::CL == 2) cluster_sync();
 }
 
 // Merge the partials of every token that a range boundary cut, add the sink once, write bf16.
@@ -1215,6 +1146,8 @@ struct DeviceInfo {
 constexpr int kMaxDev = 64;
 DeviceInfo g_dev[kMaxDev];
 std::mutex g_dev_mutex;
+// test switch of the bounded-wait path (ds_test_set_stall)
+std::atomic<int> g_test_stall{0};
 
 template <int D, bool F8>
 constexpr int dvar() { return F8 ? 4 : D == 64 ? 0 : D == 128 ? 1 : D == 256 ? 2 : 3; }
@@ -1276,15 +1209,29 @@ bool splits_tokens(int64_t ntok, int topk, int64_t G) {
     return false;
 }
 
-template <int D>
-size_t workspace_bytes_for(int64_t ntok, int topk) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-    const int gmax = max_clusters<D>(dev);
+// Workspace of one kernel variant for a problem on `dev` (0 when no token is cut).
+template <int D, bool F8>
+size_t variant_workspace_bytes(int dev, int64_t ntok, int topk) {
+    const int gmax = max_clusters<D, F8>(dev);
     if (gmax <= 0 || ntok == 0 || topk == 0) return 0;
     const int64_t G = choose_clusters(ntok, topk, gmax);
     if (!splits_tokens(ntok, topk, G)) return 0;
     return (size_t)G * 2 * ((size_t)SLOT_HEADS * D + 2 * SLOT_HEADS) * sizeof(float);
+}
+
+// The workspace query serves every kernel that reads rows of width D: at d = 512 that is the bf16
+// gather and the fp8 row store, whose co-resident cluster counts could differ, so the larger need
+// is returned and either call accepts it.
+template <int D>
+size_t workspace_bytes_for(int64_t ntok, int topk) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    size_t need = variant_workspace_bytes<D, false>(dev, ntok, topk);
+    if constexpr (D == 512) {
+        const size_t f8 = variant_workspace_bytes<D, true>(dev, ntok, topk);
+        if (f8 > need) need = f8;
+    }
+    return need;
 }
 
 template <int D, bool F8 = false>
@@ -1332,8 +1279,7 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     p.G = (int)G;
     p.scale_log2 = a.scale * kLog2e;
     p.status = a.status;
-    const char *stall = std::getenv("DSATTN_TEST_STALL");
-    p.stall_first_tile = stall != nullptr && stall[0] == '1';
+    p.stall_first_tile = g_test_stall.load(std::memory_order_relaxed) != 0 ? 1 : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(C::CL * G), 1, 1);
@@ -1377,6 +1323,8 @@ size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk) {
         default: return 0;
     }
 }
+
+void set_test_stall(bool on) { tc::g_test_stall.store(on ? 1 : 0, std::memory_order_relaxed); }
 
 int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream) {
     if (a.kv8) return a.d == 512 ? tc::launch<512, true>(a, stream) : DS_EUNSUPPORTED;

@@ -58,6 +58,8 @@ _lib.ds_sparse_attn_fp8kv.argtypes = [_P, _P, _P, _i64, _P, _P, _i32, _f32, _P, 
 _lib.ds_sparse_attn_fp8kv.restype = _i32
 _lib.ds_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint)]
 _lib.ds_device_status.restype = _i32
+_lib.ds_test_set_stall.argtypes = [_i32]
+_lib.ds_test_set_stall.restype = None
 _lib.ds_status_string.argtypes = [_i32]
 _lib.ds_status_string.restype = ctypes.c_char_p
 
@@ -289,6 +291,11 @@ def device_status(stream=None) -> int:
     if st not in (DS_OK, DS_EDEVICE):
         raise DsError("ds_device_status", st)
     return bits.value
+
+
+def test_set_stall(on: bool) -> None:
+    """Test hook: while on, every sparse_attn launch has a bounded wait run out (DS_DEV_TIMEOUT)."""
+    _lib.ds_test_set_stall(1 if on else 0)
 
 
 def status_string(status: int) -> str:

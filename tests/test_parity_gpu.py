@@ -272,11 +272,11 @@ def test_attn_edge_shapes(ds, case):
 @pytest.mark.parametrize("qscale", [8.0, 32.0])
 def test_attn_peaked_scores_on_the_split_path(ds, qscale):
     """Large logits on the d = 512 path, where each CTA of the cluster adds the peer's partial
-    scores carried in three bytes (relative error <= 2^-15 per partial score).  q is scaled so
-    the partial logits reach tens to hundreds of log2 units: attention that is nearly one-hot,
-    where a score error shows up directly in the weights.  Also a workload where the two halves'
-    partials cancel: q's second half is minus its first half and kv's halves are equal, so every
-    full score is 0 and the output is the plain mean of the rows (with the sink)."""
+    scores (f32) to its own.  q is scaled so the partial logits reach tens to hundreds of log2
+    units: attention that is nearly one-hot, where a score error shows up directly in the
+    weights.  Also a workload where the two halves' partials cancel: q's second half is minus its
+    first half and kv's halves are equal, so every full score is 0 and the output is the plain
+    mean of the rows (with the sink)."""
     q, kv, sink, idx = _case(30, 2, 2, 128, 512, 1500, 700, 0.02)
     q = (q.float() * qscale).to(torch.bfloat16)
     _check_case(ds, q, kv, sink, idx, 512 ** -0.5)
@@ -296,6 +296,42 @@ def test_attn_stream_k_every_token(ds, d, h, ntok, topk):
     kernel merges every cut token.  Every token is checked, cut or whole."""
     q, kv, sink, idx = _case(50 + topk, ntok // 2, 2, h, d, 3 * topk, topk, 0.05)
     _check_case(ds, q, kv, sink, idx, d ** -0.5)
+    assert ds.device_status() == 0
+
+
+def _out_of_tolerance(got: np.ndarray, ref64: np.ndarray) -> int:
+    """Elements of got (f32 values) outside |got - ref| <= 1e-2 + 1.6e-2 |ref| of the f64 result."""
+    return int((np.abs(got.astype(np.float64) - ref64) > 1e-2 + 1.6e-2 * np.abs(ref64)).sum())
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("d,h,b,m,topk", [(512, 64, 100, 2, 300), (512, 128, 2, 2, 1500), (256, 32, 3, 2, 500)])
+def test_attn_wide_range_rows_as_accurate_as_f32(ds, fp8, d, h, b, m, topk):
+    """Rows whose 32-blocks span 2^-20 .. 2^20 (a range the fp8 round trip keeps): logits reach
+    about 10^6, where an f32 evaluation itself is no longer within the bf16 tolerance everywhere
+    (its rounding of a logit near 7e5 is 0.06, which moves a near-tie's weights by percent).
+    Scores, softmax and accumulation are f32 ("Module attn", Precision paragraph), so measured
+    against the f64 evaluation the kernel may miss the tolerance only where f32 arithmetic does:
+    it must have no more elements out of tolerance than the f32 oracle on the same input (a
+    score carried with fewer bits than f32 across the d split shows up here as many more)."""
+    if fp8 and d != 512:
+        pytest.skip("the fp8 row store is read by the d = 512 kernel")
+    q, _, sink, idx = _case(500 + d + b, b, m, h, d, 2 * topk, topk, 0.05)
+    kv = _spread_rows(500 + b, b * 2 * topk, d).view(b, 2 * topk, d)
+    kv_rt = _bf16_from_bits(oracle.act_quant_inplace(bits(kv).copy().reshape(-1)).reshape(kv.shape))
+    if fp8:
+        codes, exps = ds.kv_quantize_fp8(kv.cuda())
+        o = ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), d ** -0.5)
+    else:
+        o = ds.sparse_attn(q.cuda(), kv_rt.cuda(), sink.cuda(), idx.cuda(), d ** -0.5)
+    ref64 = oracle.sparse_attn(bits(q), bits(kv_rt), sink.numpy(), idx.numpy(), d ** -0.5, f64=True)
+    ref32 = oracle.bf16_bits_to_f32(oracle.sparse_attn(bits(q), bits(kv_rt), sink.numpy(), idx.numpy(), d ** -0.5))
+    got = oracle.bf16_bits_to_f32(bits(o))
+    assert np.isfinite(got).all()
+    n_gpu, n_f32 = _out_of_tolerance(got, ref64), _out_of_tolerance(ref32, ref64)
+    print(f"\nwide-range rows d={d} h={h} fp8={fp8}: out of tolerance against f64: kernel {n_gpu}, "
+          f"f32 oracle {n_f32} of {got.size}")
+    assert n_gpu <= n_f32
     assert ds.device_status() == 0
 
 
@@ -375,19 +411,21 @@ def test_repeated_calls_finish_without_timeouts(ds):
 
 
 @pytest.mark.parametrize("d,h,b,topk", [(512, 64, 4, 700), (64, 8, 2, 300)])
-def test_timed_out_wait_is_reported_and_context_stays_usable(ds, monkeypatch, d, h, b, topk):
-    """The kernel's bounded waits, made to run out without any GPU fault: with the test switch
-    DSATTN_TEST_STALL the gather warps withhold the first tile's arrivals, so the MMA thread's
+def test_timed_out_wait_is_reported_and_context_stays_usable(ds, d, h, b, topk):
+    """The kernel's bounded waits, made to run out without any GPU fault: with the test hook
+    ds_test_set_stall on, the gather warps withhold the first tile's arrivals, so the MMA thread's
     wait gives up after its time limit.  The call must end (no hang), raise DS_DEV_TIMEOUT, and
     leave the context usable: the next call without the switch is clean and agrees with the
     oracle.  Covers the 2-CTA cluster path (d = 512) and the single-CTA path (d = 64)."""
     q, kv, sink, idx = _case(40 + d, b, 1, h, d, 2048, topk)
     scale = d ** -0.5
     assert ds.device_status() == 0
-    monkeypatch.setenv("DSATTN_TEST_STALL", "1")
-    ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
-    bits_after = ds.device_status()
-    monkeypatch.delenv("DSATTN_TEST_STALL")
+    ds.test_set_stall(True)
+    try:
+        ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
+        bits_after = ds.device_status()
+    finally:
+        ds.test_set_stall(False)
     assert bits_after & ds.DS_DEV_TIMEOUT, f"expected a timeout, status bits {bits_after}"
     _check_case(ds, q, kv, sink, idx, scale)
     assert ds.device_status() == 0
@@ -503,16 +541,18 @@ def test_attn_fp8kv_ring_then_attend(ds):
     assert ds.device_status() == 0
 
 
-def test_attn_fp8kv_timed_out_wait_is_reported(ds, monkeypatch):
+def test_attn_fp8kv_timed_out_wait_is_reported(ds):
     """The bounded-wait abort on the fp8 gather path (see the bf16 test above)."""
     q, _, sink, idx = _case(90, 4, 1, 64, 512, 2048, 700)
     kv = _spread_rows(90, 4 * 2048, 512).view(4, 2048, 512)
     codes, exps = ds.kv_quantize_fp8(kv.cuda())
     assert ds.device_status() == 0
-    monkeypatch.setenv("DSATTN_TEST_STALL", "1")
-    ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), 512 ** -0.5)
-    bits_after = ds.device_status()
-    monkeypatch.delenv("DSATTN_TEST_STALL")
+    ds.test_set_stall(True)
+    try:
+        ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), 512 ** -0.5)
+        bits_after = ds.device_status()
+    finally:
+        ds.test_set_stall(False)
     assert bits_after & ds.DS_DEV_TIMEOUT, f"expected a timeout, status bits {bits_after}"
     o = ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), 512 ** -0.5)
     dec = oracle.kv_dequantize_fp8(codes.cpu().numpy(), exps.cpu().numpy())
@@ -597,7 +637,8 @@ def test_writes_stay_inside_o_and_workspace(ds, fp8, d, h, b, m, topk):
     ws_big = torch.full((need + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
     ws = ws_big[:need] if need else None
     if fp8:
-        kv = _spread_rows(300 + b, b * 2 * topk, d).view(b, 2 * topk, d)
+        # the same N(0,1) rows, kept as the fp8 row store (this test is about where writes land;
+        # wide-range rows are the subject of test_attn_wide_range_rows_as_accurate_as_f32)
         codes, exps = ds.kv_quantize_fp8(kv.cuda())
         ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), d ** -0.5, o=o, workspace=ws)
         kv_ref = oracle.kv_dequantize_fp8(codes.cpu().numpy(), exps.cpu().numpy())
