@@ -139,6 +139,27 @@ int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float
                    void *workspace, size_t workspace_bytes, ds_stream_t stream);
 
 /*
+ * ds_sparse_attn_rope -- ds_sparse_attn with the inverse RoPE of its output fused in.
+ * Sources: "DeepSeek V4.1", attention/query-latent, Attention.forward (the attention output is
+ * rotated back, apply_rotary_emb(o, inverse=True), before the output projection); "Module attn",
+ * apply_rotary and freqs_cis.
+ *
+ * The result is bit-identical to ds_sparse_attn followed by
+ *     ds_apply_rotary(o, b * m * h, d, rd, h, m, start_pos, table, table_rows, 1)
+ * i.e. the last rd values of o[bi][t][hh] are rotated back by the angle of position start_pos + t
+ * (the stored bf16 pair, f32 products, bf16 result), in the attention kernel's epilogue and in the
+ * combine of tokens split across CTAs, without a second pass over o.
+ * Arguments before rd are those of ds_sparse_attn (same workspace); rd, table and table_rows are
+ * those of ds_apply_rotary: rd a multiple of 8 and <= d, table f32 [table_rows][rd / 2][2] of
+ * (cos, sin), 8-byte aligned, start_pos + m - 1 < table_rows.
+ * Errors: those of ds_sparse_attn, and DS_EINVAL for rd, table or start_pos outside the above.
+ */
+int ds_sparse_attn_rope(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink,
+                        const int32_t *idx, int topk, float scale, uint16_t *o, int b, int m, int h, int d,
+                        void *workspace, size_t workspace_bytes, int rd, const float *table,
+                        int64_t table_rows, int64_t start_pos, ds_stream_t stream);
+
+/*
  * ds_apply_rotary -- RoPE (or its inverse) on the last rd values of rows of bf16 values, in place.
  * Sources: "Module attn", apply_rotary, freqs_cis and the Precision paragraph; "DeepSeek V4.1",
  * attention/query-latent, precompute_freqs_cis, apply_rotary_emb and Attention.forward (RoPE on

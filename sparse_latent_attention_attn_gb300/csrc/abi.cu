@@ -41,6 +41,31 @@ struct Range {
 };
 
 }  // namespace
+
+// ds_sparse_attn and ds_sparse_attn_rope (rope == nullptr: no rotation of the output).
+int sparse_attn_bf16(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink, const int32_t *idx, int topk,
+                     float scale, uint16_t *o, int b, int m, int h, int d, void *workspace, size_t workspace_bytes,
+                     const float *rope, int rd, int64_t rope_pos0, int64_t table_rows, ds_stream_t stream) {
+    if (b < 0 || m < 0 || n < 0 || topk < 0 || h < 1) return DS_EINVAL;
+    if (!supported_head_dim(d) || h > 128) return DS_EUNSUPPORTED;
+    if ((int64_t)b * m == 0) return DS_OK;
+    if (!q || !o || !sink || (topk > 0 && (!idx || !kv))) return DS_EINVAL;
+    if (!aligned16(q) || !aligned16(o) || (kv && !aligned16(kv))) return DS_EINVAL;
+    const size_t need = ds_sparse_attn_workspace_bytes(b, m, h, d, topk);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return DS_EWORKSPACE;
+    AttnArgs a{q, kv, nullptr, nullptr, n, sink, idx, topk, scale, o, b, m, h, d, workspace, workspace_bytes,
+               status_word(), rope, rd, rope_pos0};
+    if (!a.status) return DS_ECUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (topk == 0) {   // nothing to attend to: every output is 0 (then rotated, as a separate pass would)
+        if (cudaMemsetAsync(o, 0, (size_t)b * m * h * d * sizeof(uint16_t), st) != cudaSuccess) return DS_ECUDA;
+        if (!rope) return DS_OK;
+        (void)table_rows;
+        return launch_apply_rotary(o, (int64_t)b * m * h, d, rd, h, m, rope_pos0, rope, true, st);
+    }
+    return launch_sparse_attn_tc(a, st);
+}
+
 }  // namespace dsattn
 
 using namespace dsattn;
@@ -78,21 +103,20 @@ int ds_sparse_attn(const uint16_t *q, const uint16_t *kv, int64_t n, const float
                    int topk, float scale, uint16_t *o, int b, int m, int h, int d, void *workspace,
                    size_t workspace_bytes, ds_stream_t stream) {
     const Range range("ds_sparse_attn");
-    if (b < 0 || m < 0 || n < 0 || topk < 0 || h < 1) return DS_EINVAL;
-    if (!supported_head_dim(d) || h > 128) return DS_EUNSUPPORTED;
-    if ((int64_t)b * m == 0) return DS_OK;
-    if (!q || !o || !sink || (topk > 0 && (!idx || !kv))) return DS_EINVAL;
-    if (!aligned16(q) || !aligned16(o) || (kv && !aligned16(kv))) return DS_EINVAL;
-    const size_t need = ds_sparse_attn_workspace_bytes(b, m, h, d, topk);
-    if (workspace_bytes < need || (need > 0 && !workspace)) return DS_EWORKSPACE;
-    AttnArgs a{q, kv, nullptr, nullptr, n, sink, idx, topk, scale, o, b, m, h, d, workspace, workspace_bytes,
-               status_word()};
-    if (!a.status) return DS_ECUDA;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (topk == 0) {   // nothing to attend to: every output is 0
-        return cudaMemsetAsync(o, 0, (size_t)b * m * h * d * sizeof(uint16_t), st) == cudaSuccess ? DS_OK : DS_ECUDA;
-    }
-    return launch_sparse_attn_tc(a, st);
+    return sparse_attn_bf16(q, kv, n, sink, idx, topk, scale, o, b, m, h, d, workspace, workspace_bytes, nullptr, 0,
+                            0, 0, stream);
+}
+
+int ds_sparse_attn_rope(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink, const int32_t *idx,
+                        int topk, float scale, uint16_t *o, int b, int m, int h, int d, void *workspace,
+                        size_t workspace_bytes, int rd, const float *table, int64_t table_rows, int64_t start_pos,
+                        ds_stream_t stream) {
+    const Range range("ds_sparse_attn_rope");
+    if (rd <= 0 || rd % 8 != 0 || rd > d || start_pos < 0 || table_rows < 0) return DS_EINVAL;
+    if (!table || (reinterpret_cast<uintptr_t>(table) & 7u) != 0) return DS_EINVAL;
+    if (m > 0 && start_pos + m - 1 >= table_rows) return DS_EINVAL;   // a position outside the table
+    return sparse_attn_bf16(q, kv, n, sink, idx, topk, scale, o, b, m, h, d, workspace, workspace_bytes, table, rd,
+                            start_pos, table_rows, stream);
 }
 
 int ds_apply_rotary(uint16_t *x, int64_t rows, int row_len, int rd, int64_t rows_per_pos, int64_t positions_per_seq,

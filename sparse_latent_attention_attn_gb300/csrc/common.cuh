@@ -19,6 +19,19 @@ __device__ __forceinline__ void flag_status(unsigned int *status, unsigned int b
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// RoPE of one pair of bf16 values (low half first) by the table entry cs = (cos, sin), negated
+// angle when inverse ("Module attn", apply_rotary: adjacent pairs as complex numbers, f32 products,
+// bf16 result): a' = a c - b s, b' = a s + b c, each product and sum rounded to f32 on its own
+// (no fused multiply-add), then each result rounded to bf16, nearest even.
+__device__ __forceinline__ uint32_t rope_rotate_bf16x2(uint32_t w, float2 cs, bool inverse) {
+    const float a = bf16_lo(w), b = bf16_hi(w);
+    const float sn = inverse ? -cs.y : cs.y;
+    const float re = __fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, sn));
+    const float im = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, cs.x));
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(re)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(im)) << 16);
+}
+
 // ------------------------------------------------------------------------------------------
 // Kernel entry points (defined in the per-kernel translation units).
 // ------------------------------------------------------------------------------------------
@@ -52,6 +65,11 @@ struct AttnArgs {
     void *workspace;
     size_t workspace_bytes;
     unsigned int *status;
+    // inverse RoPE of the output, fused (rope == nullptr: none): the last rd values of o[bi][t][hh]
+    // rotated back by the angle of position rope_pos0 + t, table rows of rd / 2 (cos, sin) pairs
+    const float *rope = nullptr;
+    int rd = 0;
+    int64_t rope_pos0 = 0;
 };
 
 int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream);

@@ -32,15 +32,7 @@ __global__ void __launch_bounds__(256) apply_rotary_kernel(uint16_t *__restrict_
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
         const float2 *cs = table + pos * (rd / 2) + q * 4;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float a = bf16_lo(w[i]), b = bf16_hi(w[i]);
-            const float2 t = cs[i];
-            const float sn = inverse ? -t.y : t.y;
-            const float re = __fsub_rn(__fmul_rn(a, t.x), __fmul_rn(b, sn));
-            const float im = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, t.x));
-            w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(re)) |
-                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(im)) << 16);
-        }
+        for (int i = 0; i < 4; ++i) w[i] = rope_rotate_bf16x2(w[i], cs[i], inverse);
         *p4 = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }

@@ -190,7 +190,21 @@ struct Params {
     // test switch for the timeout path (ds_test_set_stall): the gather warps withhold their
     // arrivals for the first tile, so a bounded wait runs out
     int stall_first_tile;
+    // fused inverse RoPE of the output (rope == nullptr: none), see AttnArgs
+    const float2 *rope;
+    int rd;
+    int64_t rope_pos0;
 };
+
+// A bf16 pair of output columns (col, col + 1) of token tok: the normalised values, and when the
+// inverse RoPE is fused and the pair lies in the last rd columns, rotated back exactly as
+// ds_apply_rotary would rotate the stored bf16 pair.  cs_row: the token's table row (or nullptr).
+template <int D>
+__device__ __forceinline__ uint32_t out_pair(float x0, float x1, int col, const float2 *cs_row, int rd) {
+    uint32_t v = pack_bf16x2(x0, x1);
+    if (cs_row != nullptr && col >= D - rd) v = rope_rotate_bf16x2(v, __ldg(cs_row + ((col - (D - rd)) >> 1)), true);
+    return v;
+}
 
 // Start of cluster c's range of the flattened entry space (token t holds entries [t T, t T + T)).
 // The G ranges split a cost line evenly, on which each token costs its T entries plus K: the fixed
@@ -942,6 +956,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 const float w = any ? ex2(m_used - top) : 0.0f;
                 const float inv = w / (l * w + ex2(sink2 - top));
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (tok * p.h + t) * (int64_t)D + crank * C::DH);
+                const float2 *cs_row = p.rope != nullptr ? p.rope + (p.rope_pos0 + tok % p.m) * (p.rd / 2) : nullptr;
+                const int col0 = (int)crank * C::DH;
 #pragma unroll 1
                 for (int c0 = 0; c0 < C::DH / 32; c0 += EG) {
                     uint32_t r[EG][32];
@@ -965,7 +981,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                                 for (int i = 0; i < 8; ++i) {
                                     const float x0 = __uint_as_float(r[g][16 * k + 2 * i]) * inv;
                                     const float x1 = __uint_as_float(r[g][16 * k + 2 * i + 1]) * inv;
-                                    w8[i] = pack_bf16x2(x0, x1);
+                                    w8[i] = out_pair<D>(x0, x1, col0 + (c0 + g) * 32 + 16 * k + 2 * i, cs_row, p.rd);
                                 }
                                 st_global_v8(dst + (c0 + g) * 4 + 2 * k, w8);
                             }
@@ -979,7 +995,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                                 for (int i = 0; i < 4; ++i) {
                                     const float x0 = __uint_as_float(r[g][8 * k + 2 * i]) * inv;
                                     const float x1 = __uint_as_float(r[g][8 * k + 2 * i + 1]) * inv;
-                                    w4[i] = pack_bf16x2(x0, x1);
+                                    w4[i] = out_pair<D>(x0, x1, col0 + (c0 + g) * 32 + 8 * k + 2 * i, cs_row, p.rd);
                                 }
                                 dst[(c0 + g) * 4 + k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
@@ -1048,9 +1064,12 @@ struct CombineParams {
     const float *sink;
     const float *ws;
     uint16_t *o;
+    const float2 *rope;           // fused inverse RoPE (nullptr: none), see AttnArgs
+    int64_t rope_pos0;
+    int rd;
+    int m;
     int h;
     int ncut;
-    float pad_;
     int4 cut[kMaxCut];            // {token, first part, parts, slot bits}
 };
 
@@ -1096,10 +1115,13 @@ __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const C
         }
     }
     uint4 *dst = reinterpret_cast<uint4 *>(cp.o + (tok * cp.h + hh) * (int64_t)D + c0);
+    const float2 *cs_row = cp.rope != nullptr ? cp.rope + (cp.rope_pos0 + tok % cp.m) * (cp.rd / 2) : nullptr;
 #pragma unroll
     for (int k = 0; k < COLS / 8; ++k)
-        dst[k] = make_uint4(pack_bf16x2(acc[8 * k], acc[8 * k + 1]), pack_bf16x2(acc[8 * k + 2], acc[8 * k + 3]),
-                            pack_bf16x2(acc[8 * k + 4], acc[8 * k + 5]), pack_bf16x2(acc[8 * k + 6], acc[8 * k + 7]));
+        dst[k] = make_uint4(out_pair<D>(acc[8 * k], acc[8 * k + 1], c0 + 8 * k, cs_row, cp.rd),
+                            out_pair<D>(acc[8 * k + 2], acc[8 * k + 3], c0 + 8 * k + 2, cs_row, cp.rd),
+                            out_pair<D>(acc[8 * k + 4], acc[8 * k + 5], c0 + 8 * k + 4, cs_row, cp.rd),
+                            out_pair<D>(acc[8 * k + 6], acc[8 * k + 7], c0 + 8 * k + 6, cs_row, cp.rd));
 }
 
 // The cut tokens of a launch (host): every token that some range boundary falls inside.
@@ -1254,8 +1276,11 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
         cpar.sink = a.sink;
         cpar.ws = static_cast<const float *>(a.workspace);
         cpar.o = a.o;
+        cpar.rope = reinterpret_cast<const float2 *>(a.rope);
+        cpar.rope_pos0 = a.rope_pos0;
+        cpar.rd = a.rd;
+        cpar.m = a.m;
         cpar.h = a.h;
-        cpar.pad_ = 0.0f;
         cpar.ncut = cut_tokens(ntok, a.topk, K, G, cpar.cut);
         if (cpar.ncut <= 0) return DS_EUNSUPPORTED;
     }
@@ -1280,6 +1305,9 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     p.scale_log2 = a.scale * kLog2e;
     p.status = a.status;
     p.stall_first_tile = g_test_stall.load(std::memory_order_relaxed) != 0 ? 1 : 0;
+    p.rope = reinterpret_cast<const float2 *>(a.rope);
+    p.rd = a.rd;
+    p.rope_pos0 = a.rope_pos0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(C::CL * G), 1, 1);

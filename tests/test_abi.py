@@ -120,6 +120,22 @@ def test_rope_argument_checks(lib):
     assert k(fake, 64, None, 0, 1, 1, 64, 0, 8, 32, None, 10, None) == -1
 
 
+def test_sparse_attn_rope_argument_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)   # never dereferenced: every call below fails its checks first
+    f = lib.ds_sparse_attn_rope
+    f.argtypes = [P, P, ctypes.c_int64, P, P, ctypes.c_int, ctypes.c_float, P, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, P, ctypes.c_size_t, ctypes.c_int, P, ctypes.c_int64, ctypes.c_int64, P]
+    args = lambda rd, table, rows, pos, m=1: (fake, fake, 10, fake, fake, 4, 0.1, fake, 1, m, 4, 64, None, 0, rd,
+                                               table, rows, pos, None)
+    assert f(*args(12, fake, 100, 0)) == -1          # rd not a multiple of 8
+    assert f(*args(128, fake, 100, 0)) == -1         # rd > d
+    assert f(*args(16, None, 100, 0)) == -1          # no table
+    assert f(*args(16, P(4100), 100, 0)) == -1       # table not 8-byte aligned
+    assert f(*args(16, fake, 100, 98, m=3)) == -1    # positions 98..100: 100 is past the table
+    assert f(*args(16, fake, 100, -1)) == -1
+
+
 def test_workspace_query_is_host_only(lib):
     f = lib.ds_sparse_attn_workspace_bytes
     f.argtypes = [ctypes.c_int] * 5

@@ -316,8 +316,8 @@ def test_attn_wide_range_rows_as_accurate_as_f32(ds, fp8, d, h, b, m, topk):
     score carried with fewer bits than f32 across the d split shows up here as many more)."""
     if fp8 and d != 512:
         pytest.skip("the fp8 row store is read by the d = 512 kernel")
-    q, _, sink, idx = _case(500 + d + b, b, m, h, d, 2 * topk, topk, 0.05)
-    kv = _spread_rows(500 + b, b * 2 * topk, d).view(b, 2 * topk, d)
+    q, _, sink, idx = _case(300 + d + b, b, m, h, d, 2 * topk, topk, 0.05)
+    kv = _spread_rows(300 + b, b * 2 * topk, d).view(b, 2 * topk, d)
     kv_rt = _bf16_from_bits(oracle.act_quant_inplace(bits(kv).copy().reshape(-1)).reshape(kv.shape))
     if fp8:
         codes, exps = ds.kv_quantize_fp8(kv.cuda())
@@ -592,6 +592,43 @@ def test_kv_rope_ring_write_bit_exact(ds, b, s, d, W, p0, rd):
     ds.kv_rope_quant_ring_write(kv, ring, p0, W, rd, torch.from_numpy(table).cuda())
     assert np.array_equal(bits(kv), kv_o)
     assert np.array_equal(bits(ring), ring_o)
+
+
+@pytest.mark.parametrize("d,h,b,m,topk,rd,p0", [(512, 64, 100, 2, 300, 64, 4000),    # cut tokens: the combine
+                                                 (512, 128, 3, 1, 2176, 64, 131072),  # whole tokens, decode
+                                                 (512, 16, 1, 5, 200, 512, 0),        # every column rotated
+                                                 (64, 4, 1, 12, 8, 16, 0),            # the ratio-0 fixture's shape
+                                                 (256, 32, 60, 3, 129, 32, 77)])
+def test_sparse_attn_rope_equals_attention_then_inverse_rotation(ds, d, h, b, m, topk, rd, p0):
+    """The inverse RoPE of the output fused into the attention epilogue and the combine
+    ("DeepSeek V4.1", attention/query-latent, Attention.forward rotates o back by its position):
+    bit-identical to ds_sparse_attn followed by ds_apply_rotary(inverse), and to the oracle's
+    rotation of that attention output; the attention itself matches the oracle within the
+    tolerance."""
+    q, kv, sink, idx = _case(700 + d + m, b, m, h, d, 2 * topk, topk, 0.05)
+    table = oracle.rope_table(p0 + m, rd, 10000.0)
+    tg = torch.from_numpy(table).cuda()
+    qg, kvg, sg, ig = q.cuda(), kv.cuda(), sink.cuda(), idx.cuda()
+    fused = ds.sparse_attn_rope(qg, kvg, sg, ig, d ** -0.5, rd, tg, p0)
+    plain = ds.sparse_attn(qg, kvg, sg, ig, d ** -0.5)
+    ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), idx.numpy(), d ** -0.5)
+    assert_close_bf16(bits(plain), ref)
+    want = oracle.apply_rotary(bits(plain).copy(), rd, table, p0, h, m, True)
+    assert np.array_equal(bits(fused), want)
+    ds.apply_rotary(plain, rd, tg, p0, h, m, True)
+    assert torch.equal(fused, plain)
+    assert ds.device_status() == 0
+
+
+def test_sparse_attn_rope_empty_topk_rotates_zeros(ds):
+    """No index entries: o is zero, then rotated like any other output (the sign of a rotated
+    zero follows the table, exactly as the separate rotation pass gives it)."""
+    q, kv, sink, idx = _case(710, 2, 3, 8, 64, 10, 0)
+    table = oracle.rope_table(40, 16, 10000.0)
+    fused = ds.sparse_attn_rope(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), 0.125, 16, torch.from_numpy(table).cuda(),
+                                30)
+    want = oracle.apply_rotary(np.zeros((2, 3, 8, 64), dtype=np.uint16), 16, table, 30, 8, 3, True)
+    assert np.array_equal(bits(fused), want)
 
 
 def test_apply_rotary_rate(ds):
