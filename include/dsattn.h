@@ -271,6 +271,51 @@ int ds_sparse_attn_static_scratch(const uint16_t *q, const uint16_t *kv, int64_t
 size_t ds_sparse_attn_static_scratch_capacity(void);
 
 /*
+ * The Indexer: scores of compressed positions and the top-k kept per query.
+ * Source: "DeepSeek V4.1", attention/query-latent, Indexer.forward (index_score = einsum of the
+ * query's index heads with the shared index keys, relu, times weights_proj's per-head weights,
+ * summed over heads; the causal compress_lens mask; topk = min(index_topk, end_pos // ratio); the
+ * positions re-sorted ascending; -1 where a kept position is not visible, the others + offset).
+ *
+ * For query i (0 <= i < s) of sequence bi, at position start_pos + i, with
+ *     lens_i = (start_pos + i + 1) / ratio      (compressed positions the query can see)
+ *     Tv     = (start_pos + s) / ratio          (positions scored; end_pos // ratio)
+ * the score of position t < Tv is
+ *     score[t] = sum_h relu(dot(q[bi][i][h], k[bi][t])) * w[bi][i][h]    for t < lens_i
+ *     score[t] = -inf                                                      for t >= lens_i
+ * computed in f32 (dot products of bf16 values accumulated in f32, the head sum in f32).
+ * The kk = min(topk, Tv) positions with the largest scores are kept (equal scores at the cut: the
+ * smaller position first), written in ascending position order, t + offset, or -1 for t >= lens_i.
+ * Layouts: q bf16 [b][s][H][D]; k bf16 [b][T][D] (T >= Tv rows per sequence); w f32 [b][s][H];
+ * idx int32 [b][s][kk]; all contiguous, q and k 16-byte aligned, w 4-byte aligned.
+ * Supported: D in {64, 128}; H a multiple of 16, <= 256 (DS_EUNSUPPORTED otherwise).
+ * The q and k values are used as given (the pages' fp4 rounding of both is outside this call).
+ */
+
+/* ds_indexer_workspace_bytes -- scratch that ds_indexer_topk needs: the f32 scores of every query,
+ * b * s * round_up(Tv, 4) * 4 bytes (pure host function; 0 for invalid arguments). */
+size_t ds_indexer_workspace_bytes(int b, int s, int64_t start_pos, int ratio);
+
+/* ds_indexer_scores -- the scores alone: scores[(bi * s + i) * ld + t] for t < Tv (f32, -inf where
+ * t >= lens_i); ld >= Tv, scores 4-byte aligned.  Errors: DS_EINVAL, DS_EUNSUPPORTED, DS_ECUDA. */
+int ds_indexer_scores(const uint16_t *q, const uint16_t *k, const float *w, int b, int s, int H, int D, int64_t T,
+                      int64_t start_pos, int ratio, float *scores, int64_t ld, ds_stream_t stream);
+
+/* ds_indexer_select -- the selection alone, from scores laid out as ds_indexer_scores writes them
+ * (only t < lens_i of each row is read; the rest counts as -inf).  Exact: for the same scores the
+ * kept positions and their order are fully determined.  offset + Tv must fit in int32.
+ * Errors: DS_EINVAL, DS_ECUDA. */
+int ds_indexer_select(const float *scores, int64_t ld, int b, int s, int64_t start_pos, int ratio, int topk,
+                      int64_t offset, int32_t *idx, ds_stream_t stream);
+
+/* ds_indexer_topk -- scores then selection, the scores kept in the caller's workspace
+ * (>= ds_indexer_workspace_bytes, 16-byte aligned; DS_EWORKSPACE otherwise).
+ * Errors: DS_EINVAL, DS_EUNSUPPORTED, DS_EWORKSPACE, DS_ECUDA. */
+int ds_indexer_topk(const uint16_t *q, const uint16_t *k, const float *w, int b, int s, int H, int D, int64_t T,
+                    int64_t start_pos, int ratio, int topk, int64_t offset, int32_t *idx, void *workspace,
+                    size_t workspace_bytes, ds_stream_t stream);
+
+/*
  * ds_device_status -- synchronise `stream`, then read and clear the current device's status word
  * (DS_DEV_* bits set by kernels since the last read).  Returns DS_OK when the word was 0,
  * DS_EDEVICE when a bit was set (the bits are stored to *bits_out when it is not NULL), or

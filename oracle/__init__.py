@@ -75,6 +75,8 @@ def _load():
         lib.oracle_kv_rope_quant_ring_write.restype = i32
         lib.oracle_indexer_topk.argtypes = [P, P, P, i32, i32, i32, i32, i64, i64, i32, i32, i64, P, P]
         lib.oracle_indexer_topk.restype = i32
+        lib.oracle_indexer_select.argtypes = [P, i64, i32, i32, i64, i32, i32, i64, P]
+        lib.oracle_indexer_select.restype = i32
         attn_args = [P, P, i64, P, P, i32, f32, P, i32, i32, i32, i32, P, i64, i32]
         lib.oracle_sparse_attn.argtypes = attn_args
         lib.oracle_sparse_attn.restype = i32
@@ -221,6 +223,19 @@ def indexer_topk(q_bits: np.ndarray, k_bits: np.ndarray, w: np.ndarray, start_po
     if got != kk:
         raise ValueError("indexer_topk: bad arguments (fewer compressed keys than the top-k needs?)")
     return (idx, scores) if return_scores else idx
+
+
+def indexer_select(scores: np.ndarray, start_pos: int, ratio: int, topk: int, offset: int = 0) -> np.ndarray:
+    """The Indexer's selection from given f32 scores ``[b][s][>= Tv]``: idx ``[b][s][kk]`` int32."""
+    assert scores.dtype == np.float32 and scores.ndim == 3
+    b, s, ld = scores.shape
+    kk = min(topk, (start_pos + s) // ratio)
+    idx = np.empty((b, s, max(kk, 0)), dtype=np.int32)
+    got = _load().oracle_indexer_select(_ptr(np.ascontiguousarray(scores)), ld, b, s, start_pos, ratio, topk, offset,
+                                        _ptr(idx))
+    if got != kk:
+        raise ValueError("indexer_select: bad arguments")
+    return idx
 
 
 def sparse_attn(q_bits: np.ndarray, kv_bits: np.ndarray, sink: np.ndarray, idx: np.ndarray, scale: float,

@@ -404,6 +404,15 @@ static void sort_ctx(int64_t *v, int64_t n, int (*cmp)(const void *, const void 
     }
 }
 
+/* kk entries of one row of T scores: the kk largest (ties: smaller position first), by position */
+static void select_row(const float *sc, int64_t *ord, int64_t T, int64_t lens, int64_t kk, int64_t offset,
+                       int32_t *out) {
+    for (int64_t t = 0; t < T; ++t) ord[t] = t;
+    sort_ctx(ord, T, cmp_desc_score, (void *)sc);
+    qsort(ord, (size_t)kk, sizeof(int64_t), cmp_i64);
+    for (int64_t j = 0; j < kk; ++j) out[j] = ord[j] < lens ? (int32_t)(ord[j] + offset) : -1;
+}
+
 int oracle_indexer_topk(const uint16_t *q, const uint16_t *k, const float *w, int b, int s, int H, int D, int64_t T,
                         int64_t start_pos, int ratio, int topk, int64_t offset, float *scores_out, int32_t *idx_out) {
     if (b < 0 || s < 1 || H < 1 || D < 1 || T < 0 || start_pos < 0 || ratio < 1 || topk < 0) return -1;
@@ -433,13 +442,39 @@ int oracle_indexer_topk(const uint16_t *q, const uint16_t *k, const float *w, in
                 sc[t] = t < lens ? acc : -INFINITY;
                 if (scores_out) scores_out[((int64_t)bi * s + i) * T + t] = sc[t];
             }
-            for (int64_t t = 0; t < T; ++t) ord[t] = t;
-            sort_ctx(ord, T, cmp_desc_score, sc);
-            qsort(ord, (size_t)kk, sizeof(int64_t), cmp_i64);
-            int32_t *out = idx_out + ((int64_t)bi * s + i) * kk;
-            for (int64_t j = 0; j < kk; ++j) out[j] = ord[j] < lens ? (int32_t)(ord[j] + offset) : -1;
+            select_row(sc, ord, T, lens, kk, offset, idx_out + ((int64_t)bi * s + i) * kk);
         }
     }
+    free(sc);
+    free(ord);
+    return (int)kk;
+}
+
+/*
+ * The selection alone, from given scores: row (bi, i) is scores[(bi * s + i) * ld + t] for
+ * t < Tv = (start_pos + s) / ratio; positions t >= compress_lens count as -inf whatever the row
+ * holds there.  The kept entries follow the rule above.  Returns kk, or -1.
+ */
+int oracle_indexer_select(const float *scores, int64_t ld, int b, int s, int64_t start_pos, int ratio, int topk,
+                          int64_t offset, int32_t *idx_out) {
+    if (b < 0 || s < 1 || start_pos < 0 || ratio < 1 || topk < 0) return -1;
+    const int64_t Tv = (start_pos + s) / ratio;
+    if (ld < Tv) return -1;
+    const int64_t kk = topk < Tv ? topk : Tv;
+    float *sc = (float *)malloc(sizeof(float) * (size_t)(Tv > 0 ? Tv : 1));
+    int64_t *ord = (int64_t *)malloc(sizeof(int64_t) * (size_t)(Tv > 0 ? Tv : 1));
+    if (!sc || !ord) {
+        free(sc);
+        free(ord);
+        return -1;
+    }
+    for (int bi = 0; bi < b; ++bi)
+        for (int i = 0; i < s; ++i) {
+            const int64_t lens = (start_pos + i + 1) / ratio;
+            const float *row = scores + ((int64_t)bi * s + i) * ld;
+            for (int64_t t = 0; t < Tv; ++t) sc[t] = t < lens ? row[t] : -INFINITY;
+            select_row(sc, ord, Tv, lens, kk, offset, idx_out + ((int64_t)bi * s + i) * kk);
+        }
     free(sc);
     free(ord);
     return (int)kk;

@@ -188,6 +188,77 @@ int ds_sparse_attn_fp8kv(const uint16_t *q, const uint8_t *kv_codes, const int8_
     return launch_sparse_attn_tc(a, st);
 }
 
+// ---- the Indexer --------------------------------------------------------------------------------
+
+namespace {
+int64_t indexer_visible(int s, int64_t start_pos, int ratio) { return (start_pos + s) / ratio; }
+
+int indexer_check(const uint16_t *q, const uint16_t *k, const float *w, int b, int s, int H, int D, int64_t T,
+                  int64_t start_pos, int ratio) {
+    if (b < 0 || s < 1 || H < 1 || T < 0 || start_pos < 0 || ratio < 1) return DS_EINVAL;
+    if ((D != 64 && D != 128) || H % 16 != 0 || H > 256) return DS_EUNSUPPORTED;
+    if (T < indexer_visible(s, start_pos, ratio)) return DS_EINVAL;          // keys the queries can see
+    if (b == 0 || indexer_visible(s, start_pos, ratio) == 0) return DS_OK;   // nothing to score
+    if (!q || !k || !w || !aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(w) & 3u) != 0)
+        return DS_EINVAL;
+    return DS_OK;
+}
+}  // namespace
+
+size_t ds_indexer_workspace_bytes(int b, int s, int64_t start_pos, int ratio) {
+    if (b < 0 || s < 1 || start_pos < 0 || ratio < 1) return 0;
+    const int64_t Tv = indexer_visible(s, start_pos, ratio);
+    return (size_t)b * s * (size_t)((Tv + 3) / 4 * 4) * sizeof(float);
+}
+
+int ds_indexer_scores(const uint16_t *q, const uint16_t *k, const float *w, int b, int s, int H, int D, int64_t T,
+                      int64_t start_pos, int ratio, float *scores, int64_t ld, ds_stream_t stream) {
+    const Range range("ds_indexer_scores");
+    int st = indexer_check(q, k, w, b, s, H, D, T, start_pos, ratio);
+    const int64_t Tv = indexer_visible(s, start_pos, ratio);
+    if (st != DS_OK || b == 0 || Tv == 0) return st;
+    if (!scores || ld < Tv || (reinterpret_cast<uintptr_t>(scores) & 3u) != 0) return DS_EINVAL;
+    IndexerArgs a{q, k, w, b, s, H, D, T, start_pos, ratio, 0, 0, status_word()};
+    if (!a.status) return DS_ECUDA;
+    return launch_indexer_scores(a, scores, ld, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ds_indexer_select(const float *scores, int64_t ld, int b, int s, int64_t start_pos, int ratio, int topk,
+                      int64_t offset, int32_t *idx, ds_stream_t stream) {
+    const Range range("ds_indexer_select");
+    if (b < 0 || s < 1 || start_pos < 0 || ratio < 1 || topk < 0) return DS_EINVAL;
+    const int64_t Tv = indexer_visible(s, start_pos, ratio);
+    const int64_t kk = topk < Tv ? topk : Tv;
+    if (b == 0 || kk == 0) return DS_OK;
+    if (!scores || !idx || ld < Tv || (reinterpret_cast<uintptr_t>(scores) & 3u) != 0) return DS_EINVAL;
+    if (offset + Tv > INT32_MAX || offset < INT32_MIN) return DS_EINVAL;      // shifted positions fit int32
+    IndexerArgs a{nullptr, nullptr, nullptr, b, s, 0, 0, 0, start_pos, ratio, topk, offset, nullptr};
+    return launch_indexer_select(scores, ld, a, idx, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ds_indexer_topk(const uint16_t *q, const uint16_t *k, const float *w, int b, int s, int H, int D, int64_t T,
+                    int64_t start_pos, int ratio, int topk, int64_t offset, int32_t *idx, void *workspace,
+                    size_t workspace_bytes, ds_stream_t stream) {
+    const Range range("ds_indexer_topk");
+    if (topk < 0) return DS_EINVAL;
+    int st = indexer_check(q, k, w, b, s, H, D, T, start_pos, ratio);
+    const int64_t Tv = indexer_visible(s, start_pos, ratio);
+    const int64_t kk = topk < Tv ? topk : Tv;
+    if (st != DS_OK || b == 0 || kk == 0) return st;
+    if (!idx) return DS_EINVAL;
+    if (offset + Tv > INT32_MAX || offset < INT32_MIN) return DS_EINVAL;
+    const size_t need = ds_indexer_workspace_bytes(b, s, start_pos, ratio);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return DS_EWORKSPACE;
+    const int64_t ld = (Tv + 3) / 4 * 4;
+    IndexerArgs a{q, k, w, b, s, H, D, T, start_pos, ratio, topk, offset, status_word()};
+    if (!a.status) return DS_ECUDA;
+    cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
+    float *scores = static_cast<float *>(workspace);
+    st = launch_indexer_scores(a, scores, ld, strm);
+    if (st != DS_OK) return st;
+    return launch_indexer_select(scores, ld, a, idx, strm);
+}
+
 void ds_test_set_stall(int on) { set_test_stall(on != 0); }
 
 int ds_device_status(ds_stream_t stream, unsigned int *bits_out) {

@@ -73,6 +73,21 @@ struct AttnArgs {
 };
 
 int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream);
+
+struct IndexerArgs {
+    const uint16_t *q;     // [b][s][H][D] bf16
+    const uint16_t *k;     // [b][T][D] bf16
+    const float *w;        // [b][s][H]
+    int b, s, H, D;
+    int64_t T;
+    int64_t start_pos;
+    int ratio;
+    int topk;
+    int64_t offset;
+    unsigned int *status;
+};
+int launch_indexer_scores(const IndexerArgs &a, float *scores, int64_t ld, cudaStream_t stream);
+int launch_indexer_select(const float *scores, int64_t ld, const IndexerArgs &a, int32_t *idx, cudaStream_t stream);
 void set_test_stall(bool on);
 size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk);
 

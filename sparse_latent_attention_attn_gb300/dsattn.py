@@ -61,6 +61,14 @@ _lib.ds_sparse_attn_fp8kv.argtypes = [_P, _P, _P, _i64, _P, _P, _i32, _f32, _P, 
 _lib.ds_sparse_attn_fp8kv.restype = _i32
 _lib.ds_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint)]
 _lib.ds_device_status.restype = _i32
+_lib.ds_indexer_workspace_bytes.argtypes = [_i32, _i32, _i64, _i32]
+_lib.ds_indexer_workspace_bytes.restype = _sz
+_lib.ds_indexer_scores.argtypes = [_P, _P, _P, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _P, _i64, _P]
+_lib.ds_indexer_scores.restype = _i32
+_lib.ds_indexer_select.argtypes = [_P, _i64, _i32, _i32, _i64, _i32, _i32, _i64, _P, _P]
+_lib.ds_indexer_select.restype = _i32
+_lib.ds_indexer_topk.argtypes = [_P, _P, _P, _i32, _i32, _i32, _i32, _i64, _i64, _i32, _i32, _i64, _P, _P, _sz, _P]
+_lib.ds_indexer_topk.restype = _i32
 _lib.ds_test_set_stall.argtypes = [_i32]
 _lib.ds_test_set_stall.restype = None
 _lib.ds_status_string.argtypes = [_i32]
@@ -328,6 +336,84 @@ def device_status(stream=None) -> int:
     if st not in (DS_OK, DS_EDEVICE):
         raise DsError("ds_device_status", st)
     return bits.value
+
+
+def _indexer_inputs(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor):
+    _need(q, torch.bfloat16, "q")
+    _need(k, torch.bfloat16, "k")
+    _need(w, torch.float32, "w")
+    b, s, H, D = q.shape
+    T = k.shape[1]
+    if k.shape != (b, T, D) or w.shape != (b, s, H):
+        raise ValueError("shape mismatch: q [b][s][H][D], k [b][T][D], w [b][s][H]")
+    for t, name in ((q, "q"), (k, "k"), (w, "w")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    return b, s, H, D, T
+
+
+def indexer_visible(s: int, start_pos: int, ratio: int) -> int:
+    """Compressed positions scored for a step of s queries at start_pos: (start_pos + s) // ratio."""
+    return (start_pos + s) // ratio
+
+
+def indexer_scores(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, start_pos: int, ratio: int,
+                   scores: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """f32 scores [b][s][Tv] of the Indexer (-inf where a position is not visible yet)."""
+    b, s, H, D, T = _indexer_inputs(q, k, w)
+    Tv = indexer_visible(s, start_pos, ratio)
+    if scores is None:
+        scores = torch.empty((b, s, Tv), dtype=torch.float32, device=q.device)
+    _need(scores, torch.float32, "scores")
+    if scores.shape[:2] != (b, s) or scores.shape[2] < Tv or scores.stride(2) != 1 or scores.stride(1) != scores.shape[2] \
+            or scores.stride(0) != s * scores.shape[2]:
+        raise ValueError("scores must be a contiguous f32 [b][s][>= Tv]")
+    _check("ds_indexer_scores",
+           _lib.ds_indexer_scores(_ptr(q), _ptr(k), _ptr(w), b, s, H, D, T, start_pos, ratio, _ptr(scores),
+                                  scores.shape[2], _stream(stream)))
+    return scores
+
+
+def indexer_select(scores: torch.Tensor, start_pos: int, ratio: int, topk: int, offset: int = 0,
+                   idx: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Top-k positions per query from scores [b][s][>= Tv] (contiguous f32): int32 [b][s][kk]."""
+    _need(scores, torch.float32, "scores")
+    if not scores.is_contiguous():
+        raise ValueError("scores must be contiguous")
+    b, s, ld = scores.shape
+    kk = min(topk, indexer_visible(s, start_pos, ratio))
+    if idx is None:
+        idx = torch.empty((b, s, kk), dtype=torch.int32, device=scores.device)
+    _need(idx, torch.int32, "idx")
+    if idx.shape != (b, s, kk) or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous int32 [b][s][kk]")
+    _check("ds_indexer_select",
+           _lib.ds_indexer_select(_ptr(scores), ld, b, s, start_pos, ratio, topk, offset, _ptr(idx), _stream(stream)))
+    return idx
+
+
+def indexer_workspace_bytes(b: int, s: int, start_pos: int, ratio: int) -> int:
+    return int(_lib.ds_indexer_workspace_bytes(b, s, start_pos, ratio))
+
+
+def indexer_topk(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, start_pos: int, ratio: int, topk: int,
+                 offset: int = 0, idx: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """The Indexer's kept positions: int32 [b][s][min(topk, Tv)], ascending, + offset, -1 if unseen."""
+    b, s, H, D, T = _indexer_inputs(q, k, w)
+    kk = min(topk, indexer_visible(s, start_pos, ratio))
+    if idx is None:
+        idx = torch.empty((b, s, kk), dtype=torch.int32, device=q.device)
+    _need(idx, torch.int32, "idx")
+    if idx.shape != (b, s, kk) or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous int32 [b][s][kk]")
+    need = indexer_workspace_bytes(b, s, start_pos, ratio)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check("ds_indexer_topk",
+           _lib.ds_indexer_topk(_ptr(q), _ptr(k), _ptr(w), b, s, H, D, T, start_pos, ratio, topk, offset, _ptr(idx),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return idx
 
 
 def test_set_stall(on: bool) -> None:

@@ -99,6 +99,56 @@ WORKLOADS = {
 FIXTURE_DECODE_STEPS = (12, 13)
 
 
+@dataclass(frozen=True)
+class IndexerWorkload:
+    """The Indexer step that produces a workload's compressed indices ("DeepSeek V4.1",
+    attention/query-latent, Indexer.forward): H index heads of width D per query, one shared key
+    per compressed position, compress ratio 4, index_topk kept, shifted past the window rows."""
+    index: int
+    name: str
+    b: int
+    s: int
+    H: int
+    D: int
+    start_pos: int
+    ratio: int
+    topk: int
+    offset: int
+
+    @property
+    def Tv(self) -> int:
+        return (self.start_pos + self.s) // self.ratio
+
+    @property
+    def seed(self) -> int:
+        return 2000 + self.index
+
+
+# The pages name the Indexer's head count and width (index_n_heads, index_head_dim) without
+# values; these workloads take 64 heads of 128.  The compressed positions, top-k and window offset
+# are those of the attention workload with the same number.
+INDEXER_WORKLOADS = {
+    2: IndexerWorkload(2, "indexer_prefill", b=1, s=4096, H=64, D=128, start_pos=0, ratio=4, topk=512, offset=4096),
+    3: IndexerWorkload(3, "indexer_decode_comp", b=32, s=1, H=64, D=128, start_pos=16384, ratio=4, topk=512,
+                       offset=128),
+    4: IndexerWorkload(4, "indexer_decode_large", b=256, s=1, H=64, D=128, start_pos=131072, ratio=4, topk=2048,
+                       offset=128),
+}
+
+
+def indexer_inputs(w: IndexerWorkload, device="cpu", seed: int | None = None):
+    """q [b][s][H][D] and k [b][Tv][D] ~ N(0,1) bf16; w [b][s][H] f32 ~ N(0,1) * D^-0.5 * H^-0.5
+    (weights_proj's output times the softmax scale and n_heads^-0.5, rounded to bf16 first)."""
+    g = _gen(device, w.seed if seed is None else seed)
+    q = torch.empty((w.b, w.s, w.H, w.D), dtype=torch.bfloat16, device=device)
+    _fill_rows_bf16(q, g)
+    k = torch.empty((w.b, w.Tv, w.D), dtype=torch.bfloat16, device=device)
+    _fill_rows_bf16(k, g)
+    wt = torch.randn((w.b, w.s, w.H), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16).float()
+    wt = wt * (w.D ** -0.5 * w.H ** -0.5)
+    return q, k, wt
+
+
 def _gen(device, seed: int) -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed(seed)

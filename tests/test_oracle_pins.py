@@ -506,6 +506,40 @@ def test_indexer_properties(oracle_mod):
             assert 1 in got[:, i].tolist()[0] and 1 in got[:, i].tolist()[1]
 
 
+def _brute_select(scores, start_pos, ratio, topk, offset):
+    """Textbook selection: order positions by (score descending, position ascending), keep the
+    first kk, list them ascending, -1 for an unseen position."""
+    b, s, _ = scores.shape
+    Tv = (start_pos + s) // ratio
+    kk = min(topk, Tv)
+    out = np.empty((b, s, kk), dtype=np.int32)
+    for bi in range(b):
+        for i in range(s):
+            lens = (start_pos + i + 1) // ratio
+            vals = [(-(float(scores[bi, i, t]) if t < lens else -math.inf), t) for t in range(Tv)]
+            keep = sorted(t for _, t in sorted(vals)[:kk])
+            out[bi, i] = [t + offset if t < lens else -1 for t in keep]
+    return out
+
+
+@pytest.mark.parametrize("start_pos,s,topk,offset", [(0, 40, 6, 0), (0, 40, 64, 128), (99, 1, 7, 3), (400, 2, 30, 0)])
+def test_indexer_select_is_the_ordered_cut(oracle_mod, start_pos, s, topk, offset):
+    """The selection from given scores, with many exact ties (scores on a coarse grid, and +0 next
+    to -0), against a brute-force ordering by (score, position)."""
+    g = torch.Generator().manual_seed(34 + s)
+    Tv = (start_pos + s) // 4
+    sc = (torch.randint(-4, 5, (2, s, Tv + 3), generator=g).float() * 0.5).numpy()
+    sc[0, :, ::7] = -0.0
+    got = oracle_mod.indexer_select(sc, start_pos, 4, topk, offset)
+    assert np.array_equal(got, _brute_select(sc, start_pos, 4, topk, offset))
+
+
+def test_indexer_select_agrees_with_topk_on_its_own_scores(oracle_mod):
+    q, k, w = _indexer_case(35, s=40)
+    idx, sc = oracle_mod.indexer_topk(to_bits(q), to_bits(k), w.numpy(), 0, 4, 5, 7, return_scores=True)
+    assert np.array_equal(oracle_mod.indexer_select(sc, 0, 4, 5, 7), idx)
+
+
 def test_indexer_prefill_row_equals_decode_step(oracle_mod):
     q, k, w = _indexer_case(33, b=1, s=40, H=3)
     pre = oracle_mod.indexer_topk(to_bits(q), to_bits(k), w.numpy(), 0, 4, 6)
