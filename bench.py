@@ -378,6 +378,87 @@ def run_reference(args):
     return 0
 
 
+def run_indexer(args):
+    """The Indexer step of a workload (its scores and top-k) timed alone: CUDA events around K
+    calls on the launching stream after W warm-ups, two input sets alternating so consecutive
+    calls read different keys.  Unit: one (query, visible compressed position) pair scored."""
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    from sparse_latent_attention_attn_gb300 import dsattn
+    iw = wl.INDEXER_WORKLOADS[args.config]
+    peaks = load_peaks()
+    kk = min(iw.topk, iw.Tv)
+    sets = []
+    for k_ in range(2):
+        q, k, w = wl.indexer_inputs(iw, device=device, seed=iw.seed + 7919 * k_ + 104729 * rank)
+        idx = torch.empty((iw.b, iw.s, kk), dtype=torch.int32, device=device)
+        ws = torch.empty(dsattn.indexer_workspace_bytes(iw.b, iw.s, iw.start_pos, iw.ratio), dtype=torch.uint8,
+                         device=device)
+        sets.append((q, k, w, idx, ws))
+
+    def call(st):
+        q, k, w, idx, ws = st
+        dsattn.indexer_topk(q, k, w, iw.start_pos, iw.ratio, iw.topk, iw.offset, idx=idx, workspace=ws)
+
+    for j in range(args.warmup):
+        call(sets[j % 2])
+    torch.cuda.synchronize()
+    dsattn.device_status()
+    lens = [min((iw.start_pos + i + 1) // iw.ratio, iw.Tv) for i in range(iw.s)]
+    units = iw.b * sum(lens)                                   # (query, visible position) pairs
+    flops = 2 * iw.H * iw.D * units
+    key_bytes = iw.b * iw.Tv * iw.D * 2                        # every key row read once per call
+    alg_bytes = key_bytes + iw.b * iw.s * (iw.H * iw.D * 2 + iw.H * 4 + kk * 4)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(SLEEP_CYCLES)
+    for j in range(args.steps):
+        ev[j][0].record()
+        call(sets[j % 2])
+        ev[j][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    status = dsattn.device_status()
+    per = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    elapsed = sum(per)
+    units_all, slowest = aggregate(float(units) * args.steps, elapsed, world, device)
+    if rank == 0:
+        t = statistics.mean(per)
+        t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+        if t_hbm >= t_tc:
+            roof = {"bound": "hbm", "achieved": alg_bytes / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        else:
+            roof = {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof.update({"traffic": None, "peak_source": peaks["source"], "kernel": "indexer scores + select",
+                     "kernel_ms": t * 1e3, "roofline_ms": max(t_hbm, t_tc) * 1e3, "algorithmic_bytes": alg_bytes,
+                     "algorithmic_flops": flops})
+        out = {"metric": "Indexer (query·visible position)/s scored and selected", "value": units_all / slowest,
+               "unit": "(query·position)/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+               "ms_per_step": 1e3 * slowest / args.steps, "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "bf16 q/k, f32 weights and scores",
+               "data": "synthetic (seeded, N(0,1) bf16 q/k, N(0,1)/sqrt(D H) weights)",
+               "config": {"workload": f"{iw.name}: b={iw.b} s={iw.s} H={iw.H} D={iw.D} start_pos={iw.start_pos} "
+                                      f"ratio={iw.ratio} topk={iw.topk} ({iw.Tv} positions)",
+                          "l2": "two input sets alternating; decode keys exceed the L2"},
+               "roofline": roof, "clocks": clk, "device_status": status, "gpu_launches": 2 * args.steps}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
@@ -569,6 +650,8 @@ def main(argv=None):
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate through (0 = automatic)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--path", choices=["attn", "indexer"], default="attn",
+                    help="attn: the sparse_attn step (the bench line); indexer: the Indexer step of --config 2-4")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="kv rows as bf16, or as the fp8 row store (decode, head_dim 512)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
@@ -580,6 +663,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.path == "indexer":
+        return run_indexer(args)
     return run_ours(args)
 
 

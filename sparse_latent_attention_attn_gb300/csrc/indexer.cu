@@ -247,8 +247,6 @@ __global__ void __launch_bounds__(NTHREADS)
 // ------------------------------------------------------------------------------------------------
 // selection
 // ------------------------------------------------------------------------------------------------
-constexpr int ST = 512;   // threads of the select kernel
-
 // Order-preserving key of an f32 score: larger score, larger key; -0 and +0 are one value.
 __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
@@ -256,7 +254,8 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive prefix sum of one int per thread (ST threads); also returns the total.
+// Block-wide exclusive prefix sum of one int per thread (NT threads); also returns the total.
+template <int NT>
 __device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int x = v;
@@ -268,19 +267,50 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int &total
     if (lane == 31) warp_sums[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int s = lane < ST / 32 ? warp_sums[lane] : 0;
+        int s = lane < NT / 32 ? warp_sums[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, s, o);
             if (lane >= o) s += y;
         }
-        if (lane < ST / 32) warp_sums[lane] = s;   // inclusive
+        if (lane < NT / 32) warp_sums[lane] = s;   // inclusive
     }
     __syncthreads();
-    total = warp_sums[ST / 32 - 1];
+    total = warp_sums[NT / 32 - 1];
     const int before = warp > 0 ? warp_sums[warp - 1] : 0;
     __syncthreads();                                 // warp_sums may be reused right after
     return before + x - v;
+}
+
+// The digit of the rem-th largest key from a histogram of NBINS digits (digit NBINS - 1 largest):
+// each thread sums NBINS / NT bins from the top, a block scan finds the thread whose bins hold the
+// rank, and that thread walks them.  Writes the digit and the rank within it to *digit, *rank.
+template <int NT, int NBINS>
+__device__ __forceinline__ void find_digit(const int *hist, int rem, int *warp_sums, uint32_t *digit, int *rank) {
+    constexpr int B = NBINS / NT;
+    static_assert(B >= 1 && NBINS % NT == 0, "bins per thread");
+    const int top = NBINS - 1 - threadIdx.x * B;     // this thread's bins: top, top - 1, ..., top - B + 1
+    int c[B], sum = 0;
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+        c[k] = hist[top - k];
+        sum += c[k];
+    }
+    int total = 0;
+    const int above = block_excl_scan<NT>(sum, warp_sums, total);
+    if (above < rem && rem <= above + sum) {
+        int acc = above;
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            if (acc + c[k] >= rem) {
+                *digit = (uint32_t)(top - k);
+                *rank = rem - acc;
+                break;
+            }
+            acc += c[k];
+        }
+    }
+    __syncthreads();
 }
 
 struct SelectParams {
@@ -291,11 +321,18 @@ struct SelectParams {
     int s, ratio, kk;
 };
 
-__global__ void __launch_bounds__(ST) indexer_select_kernel(const SelectParams p) {
-    __shared__ int hist[256];
-    __shared__ int warp_sums[ST / 32];
-    __shared__ uint32_t s_prefix;
-    __shared__ int s_rem;
+// Rows up to this many positions keep their order keys in shared memory (192 KB) for every pass;
+// longer rows are read again from L2 in each pass.
+constexpr int64_t kKeysInSmemMax = 49152;
+
+template <int NT, bool SMEM>
+__global__ void __launch_bounds__(NT) indexer_select_kernel(const SelectParams p) {
+    extern __shared__ uint32_t keys_s[];   // SMEM: the order keys of positions [0, lens)
+    __shared__ int hist[4096];
+    __shared__ int warp_sums[NT / 32];
+    __shared__ uint32_t s_digit;
+    __shared__ int s_rank;
+    constexpr int NW = NT / 32;
     grid_dependency_wait();   // the scores come from the previous kernel on the stream
     const int64_t row = blockIdx.x;
     const int i = (int)(row % p.s);
@@ -303,79 +340,88 @@ __global__ void __launch_bounds__(ST) indexer_select_kernel(const SelectParams p
     if (lens > p.Tv) lens = p.Tv;
     const float *sc = p.scores + row * p.ld;
     int32_t *out = p.idx + row * p.kk;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (p.kk == 0) return;
     if (lens <= p.kk) {
         // every position the query sees is kept (the others score -inf and become -1)
-        for (int j = tid; j < p.kk; j += ST) out[j] = j < lens ? (int32_t)(j + p.offset) : -1;
+        for (int j = tid; j < p.kk; j += NT) out[j] = j < lens ? (int32_t)(j + p.offset) : -1;
         return;
     }
-    // radix select of the kk-th largest key among positions [0, lens), 8 bits at a time
+    if constexpr (SMEM) {
+        // sixteen loads in flight per thread before any store (a store right after its load would
+        // make every element wait out a whole L2 round trip)
+        constexpr int U = 16;
+        for (int64_t t0 = 0; t0 < lens; t0 += (int64_t)NT * U) {
+            float v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t t = t0 + (int64_t)u * NT + tid;
+                v[u] = t < lens ? __ldg(sc + t) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t t = t0 + (int64_t)u * NT + tid;
+                if (t < lens) keys_s[t] = order_key(v[u]);
+            }
+        }
+        __syncthreads();
+    }
+    auto key_at = [&](int64_t t) -> uint32_t {
+        if constexpr (SMEM) return keys_s[t];
+        else return order_key(__ldg(sc + t));
+    };
+    // Radix select of the kk-th largest key among positions [0, lens) in three digits: bits 31-20
+    // (sign, exponent and three mantissa bits: enough distinct values that the histogram atomics
+    // seldom collide), bits 19-8, bits 7-0.  Only keys that match the digits found so far count.
     uint32_t prefix = 0, pmask = 0;
     int rem = p.kk;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int j = tid; j < 256; j += ST) hist[j] = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 20 : pass == 1 ? 8 : 0;
+        const uint32_t dmask = pass == 2 ? 255u : 4095u;
+        for (int j = tid; j < 4096; j += NT) hist[j] = 0;
         __syncthreads();
-        for (int64_t t = tid; t < lens; t += ST) {
-            const uint32_t key = order_key(__ldg(sc + t));
-            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+        for (int64_t t = tid; t < lens; t += NT) {
+            const uint32_t key = key_at(t);
+            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1);
         }
         __syncthreads();
-        if (tid < 32) {
-            // lane l holds digits 255 - 8 l - 7 .. 255 - 8 l (high digits first)
-            int c[8], tot = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                c[k] = hist[255 - 8 * tid - k];
-                tot += c[k];
-            }
-            int incl = tot;   // keys with digits above this lane's lowest, inclusive scan from the top
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o) incl += y;
-            }
-            const int above = incl - tot;                 // keys with a digit above this lane's range
-            const bool here = above < rem && rem <= incl;
-            const uint32_t bal = __ballot_sync(0xffffffffu, here);
-            if (tid == __ffs(bal) - 1) {
-                int acc = above;
-                for (int k = 0; k < 8; ++k) {
-                    if (acc + c[k] >= rem) {
-                        s_prefix = prefix | ((uint32_t)(255 - 8 * tid - k) << shift);
-                        s_rem = rem - acc;
-                        break;
-                    }
-                    acc += c[k];
-                }
-            }
-        }
-        __syncthreads();
-        prefix = s_prefix;
-        rem = s_rem;
-        pmask |= 255u << shift;
+        if (pass < 2) find_digit<NT, 4096>(hist, rem, warp_sums, &s_digit, &s_rank);
+        else find_digit<NT, (NT > 256 ? NT : 256)>(hist, rem, warp_sums, &s_digit, &s_rank);
+        prefix |= s_digit << shift;
+        pmask |= dmask << shift;
+        rem = s_rank;
         __syncthreads();
     }
     // prefix is the key of the kk-th largest score; rem of the positions with exactly that key
-    // are kept, the first ones in position order.  Each thread owns a contiguous segment.
-    const int64_t seg = (lens + ST - 1) / ST;
-    const int64_t a = min((int64_t)tid * seg, lens), z = min(a + seg, lens);
+    // are kept, the first ones in position order.  Warp w owns a contiguous range of positions,
+    // read 32 at a time (one per lane); ballots give each lane its rank among the kept ones.
+    const int64_t segw = ((lens + NW - 1) / NW + 31) / 32 * 32;
+    const int64_t a = min((int64_t)warp * segw, lens), z = min(a + segw, lens);
     int gt = 0, eq = 0;
-    for (int64_t t = a; t < z; ++t) {
-        const uint32_t key = order_key(__ldg(sc + t));
-        gt += key > prefix;
-        eq += key == prefix;
+    for (int64_t c = a; c < z; c += 32) {
+        const int64_t t = c + lane;
+        const uint32_t key = t < z ? key_at(t) : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, t < z && key > prefix));
+        eq += __popc(__ballot_sync(0xffffffffu, t < z && key == prefix));
     }
     int total = 0;
-    const int tie0 = block_excl_scan(eq, warp_sums, total);
+    // one value per warp (lane 0 carries it, the others 0) through the block scan
+    const int tie0 = __shfl_sync(0xffffffffu, block_excl_scan<NT>(lane == 0 ? eq : 0, warp_sums, total), 0);
     const int take_eq = max(0, min(eq, rem - tie0));
-    int pos = block_excl_scan(gt + take_eq, warp_sums, total);
+    int pos = __shfl_sync(0xffffffffu, block_excl_scan<NT>(lane == 0 ? gt + take_eq : 0, warp_sums, total), 0);
     int tie = tie0;
-    for (int64_t t = a; t < z; ++t) {
-        const uint32_t key = order_key(__ldg(sc + t));
-        bool keep = key > prefix;
-        if (key == prefix) keep = tie++ < rem;
-        if (keep) out[pos++] = (int32_t)(t + p.offset);
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int64_t c = a; c < z; c += 32) {
+        const int64_t t = c + lane;
+        const uint32_t key = t < z ? key_at(t) : 0u;
+        const bool is_gt = t < z && key > prefix, is_eq = t < z && key == prefix;
+        const uint32_t eqm = __ballot_sync(0xffffffffu, is_eq);
+        const bool keep = is_gt || (is_eq && tie + __popc(eqm & lt) < rem);
+        const uint32_t km = __ballot_sync(0xffffffffu, keep);
+        if (keep) out[pos + __popc(km & lt)] = (int32_t)(t + p.offset);
+        pos += __popc(km);
+        tie += __popc(eqm);
     }
 }
 
@@ -467,6 +513,26 @@ int launch_scores(const IndexerArgs &a, float *scores, int64_t ld, cudaStream_t 
     return DS_OK;
 }
 
+template <int NT, bool SMEM>
+int launch_select_variant(const SelectParams &p, int64_t rows, cudaStream_t stream) {
+    const size_t smem = SMEM ? (size_t)p.Tv * sizeof(uint32_t) : 0;
+    if (SMEM && smem > 48 * 1024 &&
+        cudaFuncSetAttribute(indexer_select_kernel<NT, SMEM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kKeysInSmemMax * sizeof(uint32_t))) != cudaSuccess)
+        return DS_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, indexer_select_kernel<NT, SMEM>, p) == cudaSuccess ? DS_OK : DS_ECUDA;
+}
+
 int launch_select(const float *scores, int64_t ld, const IndexerArgs &a, int32_t *idx, cudaStream_t stream) {
     const int64_t Tv = (a.start_pos + a.s) / a.ratio;
     SelectParams p;
@@ -482,17 +548,10 @@ int launch_select(const float *scores, int64_t ld, const IndexerArgs &a, int32_t
     const int64_t rows = (int64_t)a.b * a.s;
     if (rows == 0 || p.kk == 0) return DS_OK;
     if (rows > 0x7fffffff) return DS_EUNSUPPORTED;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)rows, 1, 1);
-    cfg.blockDim = dim3(ST, 1, 1);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, indexer_select_kernel, p) != cudaSuccess) return DS_ECUDA;
-    return DS_OK;
+    // short rows: a small block per row; longer rows: 512 threads, keys in shared memory when they fit
+    if (Tv <= 1024) return launch_select_variant<128, true>(p, rows, stream);
+    if (Tv <= kKeysInSmemMax) return launch_select_variant<512, true>(p, rows, stream);
+    return launch_select_variant<512, false>(p, rows, stream);
 }
 
 }  // namespace ix

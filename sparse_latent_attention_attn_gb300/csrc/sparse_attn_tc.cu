@@ -198,11 +198,14 @@ struct Params {
 
 // A bf16 pair of output columns (col, col + 1) of token tok: the normalised values, and when the
 // inverse RoPE is fused and the pair lies in the last rd columns, rotated back exactly as
-// ds_apply_rotary would rotate the stored bf16 pair.  cs_row: the token's table row (or nullptr).
-template <int D>
+// ds_apply_rotary would rotate the stored bf16 pair.  cs_row: the token's table row.  The rotation
+// is a separate kernel instantiation (ROPE), so the plain kernel carries none of its code.
+template <int D, bool ROPE>
 __device__ __forceinline__ uint32_t out_pair(float x0, float x1, int col, const float2 *cs_row, int rd) {
     uint32_t v = pack_bf16x2(x0, x1);
-    if (cs_row != nullptr && col >= D - rd) v = rope_rotate_bf16x2(v, __ldg(cs_row + ((col - (D - rd)) >> 1)), true);
+    if constexpr (ROPE) {
+        if (col >= D - rd) v = rope_rotate_bf16x2(v, __ldg(cs_row + ((col - (D - rd)) >> 1)), true);
+    }
     return v;
 }
 
@@ -221,6 +224,23 @@ __host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t ntok,
     return tok * T + (r > K ? r - K : 0);
 }
 
+// Four packed entries kept in registers: a loop over constant indices selects the slot.
+struct PvRing {
+    uint32_t e[4];
+    __device__ __forceinline__ void put(int q, uint32_t v) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i == q) e[i] = v;
+    }
+    __device__ __forceinline__ uint32_t get(int q) const {
+        uint32_t v = e[0];
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+            if (i == q) v = e[i];
+        return v;
+    }
+};
+
 // Every lane waits for the phase itself (acquire) and the warp proceeds together or not at all,
 // so warp-collective tcgen05 instructions never diverge.  (Measured on this path: one polling
 // lane plus a broadcast costs about twice as much per wait, and a wake-up three times as long.)
@@ -231,7 +251,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, bool ROPE = false>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Params p) {
     using C = Cfg<D>;
     static_assert(!F8 || C::CL == 2, "the fp8 row store is read by the d-split (d = 512) kernel");
@@ -532,9 +552,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             int64_t tok = tok_begin;
             int it = 0, J = 0, seg = 0;
             bool first = true, s_more = has_work;
-            // pending P V, oldest at pq_head; at most three can be outstanding
-            int pq_J[4], pq_stage[4], pq_seg[4];
-            bool pq_first[4];
+            // pending P V, oldest at pq_head; at most three can be outstanding.  Entry pq_tail holds
+            // tile J = pq_tail (every S pushes one); its stage, first flag and segment are packed in
+            // a register ring (an indexed array would live in local memory)
+            PvRing pq;
             int pq_head = 0, pq_tail = 0;
             uint64_t idle_since = 0;
             uint32_t idle = 0;
@@ -573,11 +594,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                                             k > 0 ? 1u : 0u);
                             }
                             mma_commit(BAR(B_SFULL + (J & 1)));
-                            const int q = pq_tail & 3;
-                            pq_J[q] = J;
-                            pq_stage[q] = stage;
-                            pq_seg[q] = seg;
-                            pq_first[q] = first;
+                            pq.put(pq_tail & 3, (uint32_t)stage | (first ? 8u : 0u) | ((uint32_t)seg << 4));
                             ++pq_tail;
                             ++J;
                             ++it;
@@ -593,14 +610,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     }
                 }
                 if (pq_head != pq_tail) {
-                    const int q = pq_head & 3;
-                    const int Jp = pq_J[q];
+                    const uint32_t ent = pq.get(pq_head & 3);
+                    const int Jp = pq_head;
+                    const int pq_stage = (int)(ent & 7u), pq_seg = (int)(ent >> 4);
+                    const bool pq_first = (ent & 8u) != 0;
                     if (mbar_test_wait(BAR(B_PFULL + (Jp & 3)), (Jp >> 2) & 1) &&
-                        (!pq_first[q] || pq_seg[q] == 0 || mbar_test_wait(BAR(B_OFREE), (pq_seg[q] - 1) & 1))) {
+                        (!pq_first || pq_seg == 0 || mbar_test_wait(BAR(B_OFREE), (pq_seg - 1) & 1))) {
                         // P was written by st.shared (generic proxy) and fenced by its writers
                         tc_fence_after();
                         const uint32_t pbase = base + C::p_off(Jp);
-                        const uint32_t vbase = base + C::SM_KV + pq_stage[q] * C::TILE_BYTES;
+                        const uint32_t vbase = base + C::SM_KV + pq_stage * C::TILE_BYTES;
 #pragma unroll
                         for (int k = 0; k < BN / 16; ++k) {
                             // P: K-major A operand, 16 columns = 32 bytes of each 128-byte row.
@@ -608,9 +627,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                             // groups 1024 B apart, 64-column chunks CHUNK_BYTES apart
                             const uint64_t adesc = smem_desc_sw128(pbase + k * 32, 16, 1024);
                             const uint64_t bdesc = smem_desc_sw128(vbase + k * 2048, C::CHUNK_BYTES, 1024);
-                            mma_bf16_ss(tmem + C::O_COL, adesc, bdesc, IDESC_PV, (pq_first[q] && k == 0) ? 0u : 1u);
+                            mma_bf16_ss(tmem + C::O_COL, adesc, bdesc, IDESC_PV, (pq_first && k == 0) ? 0u : 1u);
                         }
-                        mma_commit(BAR(B_EMPTY + pq_stage[q]));
+                        mma_commit(BAR(B_EMPTY + pq_stage));
                         mma_commit(BAR(B_PVDONE + (Jp & 3)));
                         ++pq_head;
                         progressed = true;
@@ -956,7 +975,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 const float w = any ? ex2(m_used - top) : 0.0f;
                 const float inv = w / (l * w + ex2(sink2 - top));
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (tok * p.h + t) * (int64_t)D + crank * C::DH);
-                const float2 *cs_row = p.rope != nullptr ? p.rope + (p.rope_pos0 + tok % p.m) * (p.rd / 2) : nullptr;
+                const float2 *cs_row = nullptr;
+                if constexpr (ROPE) cs_row = p.rope + (p.rope_pos0 + tok % p.m) * (p.rd / 2);
                 const int col0 = (int)crank * C::DH;
 #pragma unroll 1
                 for (int c0 = 0; c0 < C::DH / 32; c0 += EG) {
@@ -981,7 +1001,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                                 for (int i = 0; i < 8; ++i) {
                                     const float x0 = __uint_as_float(r[g][16 * k + 2 * i]) * inv;
                                     const float x1 = __uint_as_float(r[g][16 * k + 2 * i + 1]) * inv;
-                                    w8[i] = out_pair<D>(x0, x1, col0 + (c0 + g) * 32 + 16 * k + 2 * i, cs_row, p.rd);
+                                    w8[i] = out_pair<D, ROPE>(x0, x1, col0 + (c0 + g) * 32 + 16 * k + 2 * i, cs_row, p.rd);
                                 }
                                 st_global_v8(dst + (c0 + g) * 4 + 2 * k, w8);
                             }
@@ -995,7 +1015,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                                 for (int i = 0; i < 4; ++i) {
                                     const float x0 = __uint_as_float(r[g][8 * k + 2 * i]) * inv;
                                     const float x1 = __uint_as_float(r[g][8 * k + 2 * i + 1]) * inv;
-                                    w4[i] = out_pair<D>(x0, x1, col0 + (c0 + g) * 32 + 8 * k + 2 * i, cs_row, p.rd);
+                                    w4[i] = out_pair<D, ROPE>(x0, x1, col0 + (c0 + g) * 32 + 8 * k + 2 * i, cs_row, p.rd);
                                 }
                                 dst[(c0 + g) * 4 + k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
@@ -1073,7 +1093,7 @@ struct CombineParams {
     int4 cut[kMaxCut];            // {token, first part, parts, slot bits}
 };
 
-template <int D>
+template <int D, bool ROPE>
 __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const CombineParams cp) {
     grid_dependency_wait();   // launched as a programmatic dependent of the attention kernel
     const int hh = threadIdx.x;
@@ -1115,13 +1135,14 @@ __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const C
         }
     }
     uint4 *dst = reinterpret_cast<uint4 *>(cp.o + (tok * cp.h + hh) * (int64_t)D + c0);
-    const float2 *cs_row = cp.rope != nullptr ? cp.rope + (cp.rope_pos0 + tok % cp.m) * (cp.rd / 2) : nullptr;
+    const float2 *cs_row = nullptr;
+    if constexpr (ROPE) cs_row = cp.rope + (cp.rope_pos0 + tok % cp.m) * (cp.rd / 2);
 #pragma unroll
     for (int k = 0; k < COLS / 8; ++k)
-        dst[k] = make_uint4(out_pair<D>(acc[8 * k], acc[8 * k + 1], c0 + 8 * k, cs_row, cp.rd),
-                            out_pair<D>(acc[8 * k + 2], acc[8 * k + 3], c0 + 8 * k + 2, cs_row, cp.rd),
-                            out_pair<D>(acc[8 * k + 4], acc[8 * k + 5], c0 + 8 * k + 4, cs_row, cp.rd),
-                            out_pair<D>(acc[8 * k + 6], acc[8 * k + 7], c0 + 8 * k + 6, cs_row, cp.rd));
+        dst[k] = make_uint4(out_pair<D, ROPE>(acc[8 * k], acc[8 * k + 1], c0 + 8 * k, cs_row, cp.rd),
+                            out_pair<D, ROPE>(acc[8 * k + 2], acc[8 * k + 3], c0 + 8 * k + 2, cs_row, cp.rd),
+                            out_pair<D, ROPE>(acc[8 * k + 4], acc[8 * k + 5], c0 + 8 * k + 4, cs_row, cp.rd),
+                            out_pair<D, ROPE>(acc[8 * k + 6], acc[8 * k + 7], c0 + 8 * k + 6, cs_row, cp.rd));
 }
 
 // The cut tokens of a launch (host): every token that some range boundary falls inside.
@@ -1183,6 +1204,10 @@ int max_clusters(int dev) {
     if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     if (cudaFuncSetAttribute(sparse_attn_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    // the instantiation with the output rotation has the same resources and residency
+    if (!F8 && cudaFuncSetAttribute(sparse_attn_tc_kernel<D, F8, !F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::SMEM_BYTES) != cudaSuccess)
         return 0;
     int nclusters = di.sms;
     if (C::CL > 1) {
@@ -1325,7 +1350,11 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = C::CL > 1 ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<D, F8>, p) != cudaSuccess) return DS_ECUDA;
+    const bool rope = a.rope != nullptr;
+    if (rope && F8) return DS_EUNSUPPORTED;
+    if (cudaLaunchKernelEx(&cfg, rope ? sparse_attn_tc_kernel<D, F8, !F8> : sparse_attn_tc_kernel<D, F8, false>, p) !=
+        cudaSuccess)
+        return DS_ECUDA;
     if (split) {
         cudaLaunchConfig_t ccfg = {};
         ccfg.gridDim = dim3((unsigned)cpar.ncut, (unsigned)((D + kCombineCols - 1) / kCombineCols), 1);
@@ -1333,7 +1362,9 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
         ccfg.stream = stream;
         ccfg.attrs = attr;   // programmatic serialization only
         ccfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&ccfg, sparse_attn_combine_kernel<D>, cpar) != cudaSuccess) return DS_ECUDA;
+        if (cudaLaunchKernelEx(&ccfg, rope ? sparse_attn_combine_kernel<D, true> : sparse_attn_combine_kernel<D, false>,
+                               cpar) != cudaSuccess)
+            return DS_ECUDA;
     }
     return DS_OK;
 }
