@@ -42,6 +42,9 @@ ATTN_KERNEL_SOURCES = ["sparse_latent_attention_attn_gb300/csrc/sparse_attn_tc.c
                        "sparse_latent_attention_attn_gb300/csrc/ptx.cuh",
                        "sparse_latent_attention_attn_gb300/csrc/common.cuh"]
 PROFILE_SUMMARY = "profiles/sparse_attn_{workload}.txt"
+INDEXER_KERNEL_SOURCES = ["sparse_latent_attention_attn_gb300/csrc/indexer.cu",
+                          "sparse_latent_attention_attn_gb300/csrc/ptx.cuh",
+                          "sparse_latent_attention_attn_gb300/csrc/common.cuh"]
 
 
 # ----------------------------------------------------------------------------------------------
@@ -135,17 +138,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in ATTN_KERNEL_SOURCES:
+    for rel in (ATTN_KERNEL_SOURCES if sources is None else sources):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, launches_units: float):
+def profiled_traffic(workload: str, launches_units: float, summary: str = PROFILE_SUMMARY, sources=None):
     """dram bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
-    path = os.path.join(ROOT, PROFILE_SUMMARY.format(workload=workload))
+    path = os.path.join(ROOT, summary.format(workload=workload))
     if not os.path.exists(path):
         return None
     src_hash, traffic = None, None
@@ -155,7 +158,7 @@ def profiled_traffic(workload: str, launches_units: float):
                 src_hash = line.split(":", 1)[1].strip()
             if line.startswith("dram_bytes_per_launch:"):
                 traffic = float(line.split(":", 1)[1].strip())
-    if src_hash != kernel_source_hash():
+    if src_hash != kernel_source_hash(sources):
         return None
     return traffic
 
@@ -441,7 +444,9 @@ def run_indexer(args):
         else:
             roof = {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
         roof["frac"] = roof["achieved"] / roof["peak"]
-        roof.update({"traffic": None, "peak_source": peaks["source"], "kernel": "indexer scores + select",
+        roof.update({"traffic": profiled_traffic(iw.name, 1, "profiles/{workload}.txt", INDEXER_KERNEL_SOURCES),
+                     "kernel_source_sha256_16": kernel_source_hash(INDEXER_KERNEL_SOURCES),
+                     "peak_source": peaks["source"], "kernel": "indexer scores + select",
                      "kernel_ms": t * 1e3, "roofline_ms": max(t_hbm, t_tc) * 1e3, "algorithmic_bytes": alg_bytes,
                      "algorithmic_flops": flops})
         out = {"metric": "Indexer (query·visible position)/s scored and selected", "value": units_all / slowest,
