@@ -168,10 +168,11 @@ def profiled_traffic(workload: str, launches_units: float, summary: str = PROFIL
 # ----------------------------------------------------------------------------------------------
 
 class StepSet:
-    def __init__(self, w: wl.Workload, device, seed: int, kv_mode: str = "bf16"):
+    def __init__(self, w: wl.Workload, device, seed: int, kv_mode: str = "bf16", pairs: bool = False):
         from sparse_latent_attention_attn_gb300 import dsattn
         self.w = w
         self.fp8 = kv_mode == "fp8"
+        self.pairs = pairs
         inp = wl.make_step_inputs(w, device=device, seed=seed)
         self.q, self.kv, self.sink = inp.q, inp.kv, inp.sink
         self.cidx = inp.cidx
@@ -191,10 +192,15 @@ class StepSet:
             # compressed rows, all kept quantised); self.kv becomes its bf16 decode (the round trip)
             self.codes, self.exps = dsattn.kv_quantize_fp8(self.kv)
             dsattn.kv_quant_ring_write(self.kv, None, 0, 1)
-        need = dsattn.sparse_attn_workspace_bytes(w.b, w.m, w.h, w.d, w.topk)
+        need = (dsattn.sparse_attn_prefill_workspace_bytes(w.b, w.m, w.h, w.d, w.topk) if pairs
+                else dsattn.sparse_attn_workspace_bytes(w.b, w.m, w.h, w.d, w.topk))
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         # library kernels per step: ring write, window rows, sparse_attn (+ combine when tokens are cut)
-        self.launches = 3 + (1 if need > 0 else 0)
+        if pairs:   # ring write, window rows, the pair union, attention, and the combine when pairs are cut
+            union = (w.b * ((w.m + 1) // 2) * 2 * w.topk * 4 + 255) // 256 * 256
+            self.launches = 4 + (1 if need > union else 0)
+        else:
+            self.launches = 3 + (1 if need > 0 else 0)
 
     def attend(self, ev=None):
         """sparse_attn alone on the step's inputs; events (start, end) around it when given."""
@@ -206,7 +212,9 @@ class StepSet:
             ev[1].record()
 
     def _attn(self, dsattn):
-        if self.fp8:
+        if self.pairs:
+            dsattn.sparse_attn_prefill(self.q, self.kv, self.sink, self.idx, self.w.scale, o=self.o, workspace=self.ws)
+        elif self.fp8:
             dsattn.sparse_attn_fp8kv(self.q, self.codes, self.exps, self.sink, self.idx, self.w.scale, o=self.o,
                                      workspace=self.ws)
         else:
@@ -488,7 +496,11 @@ def run_ours(args):
     nsets = args.sets or max(1, min(24, -(-4 * L2_BYTES // max(per_set_bytes, 1))))
     if w.n_comp * w.b * w.d * 2 > 4 * L2_BYTES:
         nsets = args.sets or 2
-    sets = [StepSet(w, device, seed=w.seed + 7919 * k + 104729 * rank, kv_mode=args.kv) for k in range(nsets)]
+    if args.prefill_pairs and w.decode:
+        print(json.dumps({"error": "--prefill-pairs needs the prefill workload"}))
+        return 1
+    sets = [StepSet(w, device, seed=w.seed + 7919 * k + 104729 * rank, kv_mode=args.kv, pairs=args.prefill_pairs)
+            for k in range(nsets)]
     torch.cuda.synchronize()
 
     # one CUDA graph per input set holds a whole step (the three library calls); replaying graphs
@@ -555,7 +567,8 @@ def run_ours(args):
         # timed-loop sets is made for it when needed
         pipe = list(sets[:3])
         while len(pipe) < 3:
-            pipe.append(StepSet(w, device, seed=w.seed + 7919 * len(pipe) + 104729 * rank, kv_mode=args.kv))
+            pipe.append(StepSet(w, device, seed=w.seed + 7919 * len(pipe) + 104729 * rank, kv_mode=args.kv,
+                                pairs=args.prefill_pairs))
         host = []
         for st_ in pipe:
             host.append({"q": st_.q.cpu().pin_memory(), "c": st_.cidx.cpu().pin_memory(),
@@ -657,6 +670,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--path", choices=["attn", "indexer"], default="attn",
                     help="attn: the sparse_attn step (the bench line); indexer: the Indexer step of --config 2-4")
+    ap.add_argument("--prefill-pairs", action="store_true",
+                    help="prefill workload: neighbouring queries share one gather (ds_sparse_attn_prefill)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="kv rows as bf16, or as the fp8 row store (decode, head_dim 512)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")

@@ -160,6 +160,31 @@ int ds_sparse_attn_rope(const uint16_t *q, const uint16_t *kv, int64_t n, const 
                         int64_t table_rows, int64_t start_pos, ds_stream_t stream);
 
 /*
+ * ds_sparse_attn_prefill -- ds_sparse_attn for a prefill chunk, two neighbouring queries per
+ * gather.  Sources: "DeepSeek V4.1", attention/attend, get_window_topk_idxs (prefill branch:
+ * query q's causal window max(0, q - W + 1) .. q) and attention/query-latent (the Indexer's
+ * compressed positions, re-sorted ascending); the operation is that of ds_sparse_attn.
+ *
+ * Queries 2j and 2j + 1 of every sequence are processed together: the sorted union of the valid
+ * entries of their two index rows is gathered once and multiplied against the heads of both
+ * queries (2 h rows of the tensor-core tile), each query's softmax keeping only the rows its own
+ * index row lists.  Neighbouring prefill queries share all but one of their window rows and many
+ * compressed rows, so the gathers and the MMA work per query shrink.
+ * The result equals ds_sparse_attn's (same tolerance to an f32 evaluation) when the valid
+ * entries of each index row are distinct, as window rows and the Indexer's positions are; a row
+ * listed twice by one query counts once here, and DS_DEV_BAD_INDEX is raised for it.
+ * Arguments and layouts are those of ds_sparse_attn; the workspace is
+ * ds_sparse_attn_prefill_workspace_bytes(b, m, h, d, topk) bytes, 256-byte aligned (the union
+ * rows, then the partials of pairs split across CTAs).
+ * Supported: d in {64, 512}; 1 <= h <= 64; topk <= 8192; n <= 2^29 (DS_EUNSUPPORTED otherwise).
+ * Errors: DS_EINVAL, DS_EUNSUPPORTED, DS_EWORKSPACE, DS_ECUDA.
+ */
+size_t ds_sparse_attn_prefill_workspace_bytes(int b, int m, int h, int d, int topk);
+int ds_sparse_attn_prefill(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink,
+                           const int32_t *idx, int topk, float scale, uint16_t *o, int b, int m, int h, int d,
+                           void *workspace, size_t workspace_bytes, ds_stream_t stream);
+
+/*
  * ds_apply_rotary -- RoPE (or its inverse) on the last rd values of rows of bf16 values, in place.
  * Sources: "Module attn", apply_rotary, freqs_cis and the Precision paragraph; "DeepSeek V4.1",
  * attention/query-latent, precompute_freqs_cis, apply_rotary_emb and Attention.forward (RoPE on

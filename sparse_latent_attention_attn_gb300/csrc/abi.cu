@@ -119,6 +119,50 @@ int ds_sparse_attn_rope(const uint16_t *q, const uint16_t *kv, int64_t n, const 
                             start_pos, table_rows, stream);
 }
 
+// ---- prefill: two neighbouring queries per gather ------------------------------------------------
+
+namespace {
+constexpr int kPrefillMaxTopk = 8192;          // index rows the union kernel sorts in shared memory
+constexpr int64_t kPrefillMaxRows = (int64_t)1 << 29;   // rows addressable beside the listing bits
+
+size_t prefill_union_bytes(int b, int m, int topk) {
+    const size_t bytes = (size_t)b * ((m + 1) / 2) * (size_t)(2 * topk) * sizeof(int32_t);
+    return (bytes + 255) & ~(size_t)255;
+}
+}  // namespace
+
+size_t ds_sparse_attn_prefill_workspace_bytes(int b, int m, int h, int d, int topk) {
+    if (b < 0 || m < 0 || h < 1 || h > 64 || topk < 1 || topk > kPrefillMaxTopk || (d != 64 && d != 512)) return 0;
+    if ((int64_t)b * m == 0) return 0;
+    return prefill_union_bytes(b, m, topk) + sparse_attn_tc_workspace_bytes(b, m, h, d, topk, true);
+}
+
+int ds_sparse_attn_prefill(const uint16_t *q, const uint16_t *kv, int64_t n, const float *sink, const int32_t *idx,
+                           int topk, float scale, uint16_t *o, int b, int m, int h, int d, void *workspace,
+                           size_t workspace_bytes, ds_stream_t stream) {
+    const Range range("ds_sparse_attn_prefill");
+    if (b < 0 || m < 0 || n < 0 || topk < 0 || h < 1) return DS_EINVAL;
+    if ((d != 64 && d != 512) || h > 64 || topk > kPrefillMaxTopk || n > kPrefillMaxRows) return DS_EUNSUPPORTED;
+    if ((int64_t)b * m == 0) return DS_OK;
+    if (!q || !o || !sink || (topk > 0 && (!idx || !kv))) return DS_EINVAL;
+    if (!aligned16(q) || !aligned16(o) || (kv && !aligned16(kv))) return DS_EINVAL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (topk == 0)
+        return cudaMemsetAsync(o, 0, (size_t)b * m * h * d * sizeof(uint16_t), st) == cudaSuccess ? DS_OK : DS_ECUDA;
+    const size_t need = ds_sparse_attn_prefill_workspace_bytes(b, m, h, d, topk);
+    if (workspace_bytes < need || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return DS_EWORKSPACE;
+    unsigned int *status = status_word();
+    if (!status) return DS_ECUDA;
+    int32_t *uidx = static_cast<int32_t *>(workspace);
+    const size_t ub = prefill_union_bytes(b, m, topk);
+    int rc = launch_pair_union(idx, b, m, topk, n, uidx, status, st);
+    if (rc != DS_OK) return rc;
+    AttnArgs a{q, kv, nullptr, nullptr, n, sink, uidx, 2 * topk, scale, o, b, m, h, d,
+               static_cast<char *>(workspace) + ub, workspace_bytes - ub, status, nullptr, 0, 0, true};
+    return launch_sparse_attn_tc(a, st);
+}
+
 int ds_apply_rotary(uint16_t *x, int64_t rows, int row_len, int rd, int64_t rows_per_pos, int64_t positions_per_seq,
                     int64_t start_pos, const float *table, int64_t table_rows, int inverse, ds_stream_t stream) {
     const Range range("ds_apply_rotary");

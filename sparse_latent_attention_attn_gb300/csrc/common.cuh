@@ -70,6 +70,10 @@ struct AttnArgs {
     const float *rope = nullptr;
     int rd = 0;
     int64_t rope_pos0 = 0;
+    // pair mode (prefill): idx holds the union rows of the query pairs (2j, 2j + 1), each 2 topk
+    // wide with the listing queries in bits 29-30 of every entry (launch_pair_union); topk is
+    // that width
+    bool pair = false;
 };
 
 int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream);
@@ -89,6 +93,9 @@ struct IndexerArgs {
 int launch_indexer_scores(const IndexerArgs &a, float *scores, int64_t ld, cudaStream_t stream);
 int launch_indexer_select(const float *scores, int64_t ld, const IndexerArgs &a, int32_t *idx, cudaStream_t stream);
 void set_test_stall(bool on);
-size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk);
+size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk, bool pair = false);
+int pair_union_cap(int topk);
+int launch_pair_union(const int32_t *idx, int b, int m, int topk, int64_t n, int32_t *uidx, unsigned int *status,
+                      cudaStream_t stream);
 
 }  // namespace dsattn

@@ -121,7 +121,7 @@ struct Cfg {
     static constexpr int SM_LIST = SM_X + X_BYTES;
     static constexpr int LIST_BYTES = LR * BN * 4;  // the index ring
     static constexpr int SM_BAR = SM_LIST + LIST_BYTES;
-    static constexpr int SM_END = SM_BAR + 512;
+    static constexpr int SM_END = SM_BAR + 1024;
     static constexpr int SMEM_BYTES = SM_END + 1024;
     static_assert(Q_COL + DH / 2 <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -166,7 +166,12 @@ constexpr int LMETA_OFF = (META_OFF + 8 * 5 + 15) & ~15;   // [LR] int4 {count, 
 constexpr int TMEM_ADDR_OFF = LMETA_OFF + 16 * LR;
 constexpr int ABORT_OFF = TMEM_ADDR_OFF + 4;
 constexpr int SEND_OFF = ABORT_OFF + 4;
-static_assert(SEND_OFF + 4 <= 512, "barrier block");
+// pair mode: per stage, the 64-bit masks of the tile's rows listed by the pair's first and second
+// query {A lo, A hi, B lo, B hi}
+constexpr int META2_OFF = 512;
+static_assert(SEND_OFF + 4 <= META2_OFF && META2_OFF + 16 * 5 <= 1024, "barrier block");
+// pair mode: an index entry carries its row in the low 29 bits and the queries listing it above
+constexpr int32_t kRowMask = (1 << 29) - 1, kPairA = 1 << 29, kPairB = 1 << 30;
 
 struct Params {
     const uint16_t *q;
@@ -178,8 +183,11 @@ struct Params {
     uint16_t *o;
     float *ws;
     int64_t n;
-    int64_t ntok;     // b * m tokens of topk entries each
+    int64_t ntok;     // work units of topk entries each: b * m tokens, or (pair mode) b * ceil(m / 2) pairs
     int topk;
+    int useq;         // work units per sequence (m, or ceil(m / 2) in pair mode)
+    int hm;           // TMEM lanes (rows of M) in use: h, or 2 h in pair mode
+    bool interleave;  // unit order (unit_at): several units per sequence
     int seg_cost;     // K of range_start, in entries
     int wide;         // q and o 32-byte aligned: their rows move in 32-byte accesses
     int m;
@@ -251,9 +259,40 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool F8 = false, bool ROPE = false>
+// Lane t of unit u (a token, or in pair mode the queries 2j, 2j + 1 of a sequence): the token it
+// serves, its head and whether that token exists.  In pair mode lanes [0, h) serve the first
+// query and [h, 2 h) the second.
+struct LaneRow {
+    int64_t tok;
+    int head;
+    bool live;
+};
+
+// The work unit a cluster's position u in the unit order stands for.  With several queries per
+// sequence (prefill) the cost of a query grows with its position (its window and its visible
+// compressed rows fill up), so the order interleaves the units from both ends, 0, N-1, 1, N-2, ...:
+// any contiguous range of positions then holds light and heavy units alike and the clusters'
+// equal shares of the index entries become equal shares of the work.  The results do not depend
+// on the order.
+__host__ __device__ __forceinline__ int64_t unit_at(int64_t u, int64_t nunits, bool interleave) {
+    return interleave ? ((u & 1) ? nunits - 1 - (u >> 1) : (u >> 1)) : u;
+}
+template <bool PAIR>
+__device__ __forceinline__ LaneRow lane_row(int64_t u, int t, int h, int m, int useq) {
+    if constexpr (!PAIR) {
+        return LaneRow{u, t, t < h};
+    } else {
+        const int k = t >= h ? 1 : 0;
+        const int64_t bi = u / useq;
+        const int qi = (int)(u - bi * useq) * 2 + k;
+        return LaneRow{bi * m + qi, t - k * h, t < 2 * h && qi < m};
+    }
+}
+
+template <int D, bool F8 = false, bool ROPE = false, bool PAIR = false>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Params p) {
     using C = Cfg<D>;
+    static_assert(!(PAIR && (F8 || ROPE)), "pair mode reads bf16 rows and writes the plain output");
     static_assert(!F8 || C::CL == 2, "the fp8 row store is read by the d-split (d = 512) kernel");
     constexpr int NSTAGE = C::NSTAGE;
     extern __shared__ uint8_t smem_raw[];
@@ -263,6 +302,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     const uint32_t bars = base + C::SM_BAR;
     auto BAR = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
     int2 *meta = reinterpret_cast<int2 *>(sbase + C::SM_BAR + META_OFF);
+    uint4 *meta2 = reinterpret_cast<uint4 *>(sbase + C::SM_BAR + META2_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + ABORT_OFF);
     volatile int *s_end = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + SEND_OFF);
     int4 *lmeta = reinterpret_cast<int4 *>(sbase + C::SM_BAR + LMETA_OFF);
@@ -308,7 +348,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         fence_mbar_init();
         if constexpr (C::CL == 2) {
             // the exchange buffers expect the peer's quarters with live rows, tiles 0 .. NX-1
-            const uint32_t xbytes = (uint32_t)((p.h < 128 ? p.h : 128) + 31) / 32 * C::XQ;
+            const uint32_t xbytes = (uint32_t)((p.hm < 128 ? p.hm : 128) + 31) / 32 * C::XQ;
             for (int i = 0; i < C::NX; ++i) mbar_arrive_expect_tx(BAR(B_XFULL + i), xbytes);
         }
     }
@@ -358,12 +398,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
             const int a = (int)((e0 > tok * T ? e0 : tok * T) - tok * T);
             const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
-            const int seq = (int)(tok / p.m);
-            const int32_t *irow = p.idx + tok * T;
+            const int64_t utok = unit_at(tok, p.ntok, p.interleave);
+            const int seq = (int)(utok / p.useq);
+            const int32_t *irow = p.idx + utok * T;
             {   // warm L2 with the next token's index row
                 const int64_t nt = tok + 1;
                 if (nt * T < e1)
-                    for (int j = lane * 32; j < T; j += 32 * 32) prefetch_l2(p.idx + nt * T + j);
+                    for (int j = lane * 32; j < T; j += 32 * 32)
+                        prefetch_l2(p.idx + unit_at(nt, p.ntok, p.interleave) * T + j);
             }
             if (!acquire()) {
                 ok = false;
@@ -388,8 +430,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 for (int g = 0; g < 8 && ok; ++g) {
                     if (j0 + g * 32 >= z) break;
                     const int v = v8[g];
-                    const bool valid = v >= 0 && (int64_t)v < p.n;
-                    bad |= (int64_t)v >= p.n;
+                    const int64_t row = PAIR ? (int64_t)(v & kRowMask) : (int64_t)v;
+                    const bool valid = v >= 0 && row < p.n;
+                    bad |= v >= 0 && row >= p.n;
                     const uint32_t bal = __ballot_sync(0xffffffffu, valid);
                     const int c = __popc(bal), pos = __popc(bal & lanemask_lt());
                     const int space = BN - fill;
@@ -433,7 +476,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         int it = 0;
         bool ok = true;
         for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
-            const int64_t row0 = (tok / p.m) * p.n;
+            const int64_t row0 = (unit_at(tok, p.ntok, p.interleave) / p.useq) * p.n;
             const uint8_t *cb = p.kv8 + row0 * (int64_t)D + crank * C::DH + unit * 16;
             const int8_t *xb = p.kexp + row0 * (int64_t)(D / 32) + crank * (C::DH / 32) + unit / 2;
             for (;; ++it) {
@@ -502,7 +545,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         int it = 0;
         bool ok = true;
         for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok) {
-            const uint16_t *kvb = p.kv + ((tok / p.m) * p.n) * (int64_t)D + crank * C::DH + unit * 8;
+            const uint16_t *kvb =
+                p.kv + ((unit_at(tok, p.ntok, p.interleave) / p.useq) * p.n) * (int64_t)D + crank * C::DH + unit * 8;
             for (;; ++it) {
                 // index tile it, then its stage
                 if (!warp_wait(BAR(B_LTFULL + it % LR), (uint32_t)(it / LR) & 1u, abort_flag)) {
@@ -521,8 +565,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
 #pragma unroll 4
                 for (int r = pw * RPW + rsub; r < cnt; r += C::NPROD_WARPS * RPW) {
                     // row r, 16-byte unit u8 of its 128-byte chunk: swizzled to unit u8 ^ (r % 8)
-                    const int v = tile[r];
+                    const int v = PAIR ? (tile[r] & kRowMask) : tile[r];
                     cp_async_16(dst0 + r * 128 + ((u8 ^ (r & 7)) << 4), kvb + (int64_t)v * D);
+                }
+                if constexpr (PAIR) {
+                    // the rows of this tile that each query of the pair listed (warp 0 of the gather)
+                    if (pw == 0) {
+                        const int e0 = lane < cnt ? tile[lane] : 0, e1 = lane + 32 < cnt ? tile[lane + 32] : 0;
+                        const uint32_t alo = __ballot_sync(0xffffffffu, (e0 & kPairA) != 0);
+                        const uint32_t ahi = __ballot_sync(0xffffffffu, (e1 & kPairA) != 0);
+                        const uint32_t blo = __ballot_sync(0xffffffffu, (e0 & kPairB) != 0);
+                        const uint32_t bhi = __ballot_sync(0xffffffffu, (e1 & kPairB) != 0);
+                        if (lane == 0) meta2[stage] = make_uint4(alo, ahi, blo, bhi);
+                    }
                 }
                 if (!(p.stall_first_tile && it == 0)) {
                     cp_async_arrive_noinc(BAR(B_FULL + stage));
@@ -677,7 +732,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         // peer's exchange buffer, so the softmax warps never wait on the cluster network to send.
         // Quarters without a live head are not sent (the receiver expects only the others).
         const int quarter = warp & 3;
-        const bool live_q = quarter * 32 < p.h;
+        const bool live_q = quarter * 32 < p.hm;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         constexpr uint32_t XSTRIDE = C::X_STRIDE;
         const uint32_t xpeer = mapa(base + C::SM_X, peer) + quarter * C::XQ;
@@ -739,18 +794,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         setmaxnreg_inc<REG_SOFTMAX>();
         const int t = threadIdx.x;                       // head row = TMEM lane
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const bool live = t < p.h;
-        const float sink2 = live ? p.sink[t] * kLog2e : 0.0f;
+        // live: this lane is a row of the MMA (a head of the token, or of one query of the pair);
+        // whether that query exists is per unit (lane_row)
+        const bool live = t < p.hm;
+        const int head = PAIR && t >= p.h ? t - p.h : t;
+        const float sink2 = live ? p.sink[head] * kLog2e : 0.0f;
         constexpr uint32_t XSTRIDE = C::X_STRIDE;
-        auto q_row = [&](int64_t tok) {
-            return reinterpret_cast<const uint4 *>(p.q + (tok * p.h + t) * (int64_t)D + crank * C::DH);
+        auto q_row = [&](const LaneRow &lr) {
+            return reinterpret_cast<const uint4 *>(p.q + (lr.tok * p.h + lr.head) * (int64_t)D + crank * C::DH);
         };
         auto load_q = [&](int64_t tok) {
             // this CTA's DH columns of q[tok][t] into TMEM columns [Q_COL, Q_COL + DH/2) of lane t.
             // Every load of the row is in flight at once (DH <= 256: at most 128 registers), so a
             // token change costs one memory latency, not one per 64 columns.  These loads queue
             // behind the row gathers in the SM's memory pipeline, so fewer, wider ones issue sooner.
-            const uint4 *src = q_row(tok);
+            const LaneRow lr = lane_row<PAIR>(unit_at(tok, p.ntok, p.interleave), t, p.h, p.m, p.useq);
+            const bool live = lr.live;
+            const uint4 *src = q_row(lr);
             uint32_t r[C::NCHUNK][32];
             if (p.wide) {
 #pragma unroll
@@ -786,10 +846,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         for (int64_t tok = tok_begin; has_work && ok && tok * T < e1; ++tok, ++seg) {
             const int a = (int)((e0 > tok * T ? e0 : tok * T) - tok * T);
             const int z = (int)((e1 < (tok + 1) * T ? e1 : (tok + 1) * T) - tok * T);
-            if (live && (tok + 1) * T < e1) {
+            const LaneRow next = lane_row<PAIR>(unit_at(tok + 1, p.ntok, p.interleave), t, p.h, p.m, p.useq);
+            if (next.live && (tok + 1) * T < e1) {
                 // the next token's q row is read as soon as this segment's scores are all read:
                 // ask for it in L2 now, so that read does not wait on HBM
-                const char *nq = reinterpret_cast<const char *>(q_row(tok + 1));
+                const char *nq = reinterpret_cast<const char *>(q_row(next));
 #pragma unroll
                 for (int i = 0; i < C::DH * 2 / 128; ++i) prefetch_l2(nq + i * 128);
             }
@@ -801,6 +862,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 break;
             }
             int2 cur = meta[it % NSTAGE];
+            uint4 cur2 = make_uint4(0, 0, 0, 0);
+            if constexpr (PAIR) cur2 = meta2[it % NSTAGE];
             if (cur.x == 0) {
                 // a segment without a single valid row: its only tile loads nothing; once all
                 // 128 threads and the MMA thread have seen it, thread 0 hands the stage back
@@ -854,7 +917,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         // arm the buffer for tile J + NX (its bytes cannot come before every
                         // softmax warp has released tile J below)
                         if (t == 0)
-                            mbar_arrive_expect_tx(BAR(B_XFULL + xs), (uint32_t)((p.h < 128 ? p.h : 128) + 31) / 32 * C::XQ);
+                            mbar_arrive_expect_tx(BAR(B_XFULL + xs), (uint32_t)((p.hm < 128 ? p.hm : 128) + 31) / 32 * C::XQ);
                         const uint32_t xbuf = base + C::SM_X + xs * XSTRIDE + warp * C::XQ + lane * 16;
                         if (live) {
                             // own half + peer half: the peer adds the same two f32 values
@@ -875,6 +938,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
 #pragma unroll
                         for (int j = 0; j < BN; ++j)
                             if (j >= cnt) s[j] = -INFINITY;
+                    }
+                    if constexpr (PAIR) {
+                        // only the rows this lane's query listed (the tile holds the pair's union)
+                        const uint32_t mlo = t < p.h ? cur2.x : cur2.z, mhi = t < p.h ? cur2.y : cur2.w;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (!((mlo >> j) & 1u)) s[j] = -INFINITY;
+                            if (!((mhi >> j) & 1u)) s[32 + j] = -INFINITY;
+                        }
                     }
                     // row max of the raw scores (the scale is positive), as a tree
                     float mx[8];
@@ -897,7 +969,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         }
                         tc_fence_after();
                         const float m_new = fmaxf(m_used, tmax);
-                        const float f = ex2(m_used - m_new);
+                        // pair mode: a lane whose query has listed no row yet keeps m = -inf
+                        const float f = PAIR && m_new == -INFINITY ? 1.0f : ex2(m_used - m_new);
                         l *= f;
 #pragma unroll 1
                         for (int c = 0; c < C::DH / 32; ++c) {
@@ -915,7 +988,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     // p = 2^(s * scale_log2 - m); P goes to the MMA in bf16, the row sum stays f32
                     uint32_t pk[32];
                     float ls[4] = {0.f, 0.f, 0.f, 0.f};
-                    const float neg_m = -m_used;
+                    // pair mode: with m = -inf every score of the tile is -inf, and p must be 0
+                    const float neg_m = PAIR && m_used == -INFINITY ? 0.0f : -m_used;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float p0 = ex2(fmaf(s[2 * j], p.scale_log2, neg_m));
@@ -946,6 +1020,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         break;
                     }
                     cur = meta[it % NSTAGE];
+                    if constexpr (PAIR) cur2 = meta2[it % NSTAGE];
                 }
                 if (!ok) break;
             }
@@ -974,9 +1049,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 const float top = fmaxf(m_used, sink2);
                 const float w = any ? ex2(m_used - top) : 0.0f;
                 const float inv = w / (l * w + ex2(sink2 - top));
-                uint4 *dst = reinterpret_cast<uint4 *>(p.o + (tok * p.h + t) * (int64_t)D + crank * C::DH);
+                const LaneRow lr = lane_row<PAIR>(unit_at(tok, p.ntok, p.interleave), t, p.h, p.m, p.useq);
+                const bool live = lr.live;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + (lr.tok * p.h + lr.head) * (int64_t)D + crank * C::DH);
                 const float2 *cs_row = nullptr;
-                if constexpr (ROPE) cs_row = p.rope + (p.rope_pos0 + tok % p.m) * (p.rd / 2);
+                if constexpr (ROPE) cs_row = p.rope + (p.rope_pos0 + lr.tok % p.m) * (p.rd / 2);
                 const int col0 = (int)crank * C::DH;
 #pragma unroll 1
                 for (int c0 = 0; c0 < C::DH / 32; c0 += EG) {
@@ -1077,7 +1154,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
 // partial slot it wrote (0: the part's first segment, 1: its last).  Block (i, y) merges columns
 // [y * kCombineCols, (y + 1) * kCombineCols) of cut token i for every head, one thread per head,
 // so each of its loads from the slots is 512 contiguous bytes per warp.
-constexpr int kCombineCols = 64;
+constexpr int kCombineCols = 16;   // columns per block: many small blocks read the partials in parallel
 constexpr int kMaxCut = 160;      // cut tokens: at most one per range boundary, G <= SM count
 
 struct CombineParams {
@@ -1089,17 +1166,23 @@ struct CombineParams {
     int rd;
     int m;
     int h;
+    int hm;                       // lanes in use (h, or 2 h in pair mode)
+    int useq;                     // work units per sequence
+    int interleave;               // unit order (unit_at)
+    int64_t nunits;
     int ncut;
-    int4 cut[kMaxCut];            // {token, first part, parts, slot bits}
+    int4 cut[kMaxCut];            // {unit, first part, parts, slot bits}
 };
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool PAIR>
 __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const CombineParams cp) {
     grid_dependency_wait();   // launched as a programmatic dependent of the attention kernel
     const int hh = threadIdx.x;
-    if (hh >= cp.h || (int)blockIdx.x >= cp.ncut) return;
+    if (hh >= cp.hm || (int)blockIdx.x >= cp.ncut) return;
     const int4 c = cp.cut[blockIdx.x];
-    const int64_t tok = c.x;
+    const LaneRow lr = lane_row<PAIR>(unit_at(c.x, cp.nunits, cp.interleave != 0), hh, cp.h, cp.m, cp.useq);
+    if (!lr.live) return;
+    const int64_t tok = lr.tok;
     const int kf = c.y, np = c.z;
     const uint32_t slots = (uint32_t)c.w;
     constexpr size_t SLOT = (size_t)SLOT_HEADS * D + 2 * SLOT_HEADS;
@@ -1107,7 +1190,7 @@ __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const C
     auto part = [&](int i) -> const float * {
         return cp.ws + ((size_t)(kf + i) * 2 + ((slots >> i) & 1u)) * SLOT;
     };
-    const float sink2 = cp.sink[hh] * kLog2e;
+    const float sink2 = cp.sink[lr.head] * kLog2e;
     float top = sink2;
     for (int i = 0; i < np; ++i) top = fmaxf(top, part(i)[SLOT_HEADS * D + hh]);
     float den = exp2f(sink2 - top);
@@ -1134,7 +1217,7 @@ __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const C
             acc[4 * k + 3] += w * x.w;
         }
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(cp.o + (tok * cp.h + hh) * (int64_t)D + c0);
+    uint4 *dst = reinterpret_cast<uint4 *>(cp.o + (tok * cp.h + lr.head) * (int64_t)D + c0);
     const float2 *cs_row = nullptr;
     if constexpr (ROPE) cs_row = cp.rope + (cp.rope_pos0 + tok % cp.m) * (cp.rd / 2);
 #pragma unroll
@@ -1192,6 +1275,10 @@ std::mutex g_dev_mutex;
 // test switch of the bounded-wait path (ds_test_set_stall)
 std::atomic<int> g_test_stall{0};
 
+// pair mode is built for the fixture's and the model's head_dim
+template <int D>
+constexpr bool kPairBuilt = D == 64 || D == 512;
+
 template <int D, bool F8>
 constexpr int dvar() { return F8 ? 4 : D == 64 ? 0 : D == 128 ? 1 : D == 256 ? 2 : 3; }
 
@@ -1205,10 +1292,16 @@ int max_clusters(int dev) {
     if (cudaFuncSetAttribute(sparse_attn_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
         return 0;
-    // the instantiation with the output rotation has the same resources and residency
+    // the instantiations with the output rotation and in pair mode have the same resources and
+    // residency
     if (!F8 && cudaFuncSetAttribute(sparse_attn_tc_kernel<D, F8, !F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::SMEM_BYTES) != cudaSuccess)
         return 0;
+    if constexpr (!F8 && kPairBuilt<D>) {
+        if (cudaFuncSetAttribute(sparse_attn_tc_kernel<D, false, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+            return 0;
+    }
     int nclusters = di.sms;
     if (C::CL > 1) {
         cudaLaunchConfig_t cfg = {};
@@ -1288,7 +1381,10 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return DS_ECUDA;
     const int gmax = max_clusters<D, F8>(dev);
     if (gmax <= 0) return DS_ECUDA;
-    const int64_t ntok = (int64_t)a.b * a.m;
+    // work units: tokens, or in pair mode the query pairs (2j, 2j + 1) of each sequence, whose
+    // index rows (a.idx) are the pairs' union rows
+    const int useq = a.pair ? (a.m + 1) / 2 : a.m;
+    const int64_t ntok = (int64_t)a.b * useq;
     const int64_t G = choose_clusters(ntok, a.topk, gmax);
     const int64_t K = seg_cost(ntok, G);
     if (a.topk > 0 && ntok > (INT64_MAX / (G + 1)) / (a.topk + K)) return DS_EUNSUPPORTED;   // G * ntok * (T + K) < 2^63
@@ -1306,6 +1402,10 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
         cpar.rd = a.rd;
         cpar.m = a.m;
         cpar.h = a.h;
+        cpar.hm = a.pair ? 2 * a.h : a.h;
+        cpar.useq = useq;
+        cpar.interleave = useq > 1 ? 1 : 0;
+        cpar.nunits = ntok;
         cpar.ncut = cut_tokens(ntok, a.topk, K, G, cpar.cut);
         if (cpar.ncut <= 0) return DS_EUNSUPPORTED;
     }
@@ -1326,6 +1426,9 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     p.wide = (((uintptr_t)a.q | (uintptr_t)a.o) & 31u) == 0;
     p.m = a.m;
     p.h = a.h;
+    p.useq = useq;
+    p.hm = a.pair ? 2 * a.h : a.h;
+    p.interleave = useq > 1;
     p.G = (int)G;
     p.scale_log2 = a.scale * kLog2e;
     p.status = a.status;
@@ -1351,10 +1454,18 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = C::CL > 1 ? 2 : 1;
     const bool rope = a.rope != nullptr;
-    if (rope && F8) return DS_EUNSUPPORTED;
-    if (cudaLaunchKernelEx(&cfg, rope ? sparse_attn_tc_kernel<D, F8, !F8> : sparse_attn_tc_kernel<D, F8, false>, p) !=
-        cudaSuccess)
-        return DS_ECUDA;
+    if ((rope && F8) || (a.pair && (F8 || rope || 2 * a.h > SLOT_HEADS))) return DS_EUNSUPPORTED;
+    auto kernel = rope ? sparse_attn_tc_kernel<D, F8, !F8> : sparse_attn_tc_kernel<D, F8, false>;
+    auto combine = rope ? sparse_attn_combine_kernel<D, true, false> : sparse_attn_combine_kernel<D, false, false>;
+    if (a.pair) {
+        if constexpr (!F8 && kPairBuilt<D>) {
+            kernel = sparse_attn_tc_kernel<D, false, false, true>;
+            combine = sparse_attn_combine_kernel<D, false, true>;
+        } else {
+            return DS_EUNSUPPORTED;
+        }
+    }
+    if (cudaLaunchKernelEx(&cfg, kernel, p) != cudaSuccess) return DS_ECUDA;
     if (split) {
         cudaLaunchConfig_t ccfg = {};
         ccfg.gridDim = dim3((unsigned)cpar.ncut, (unsigned)((D + kCombineCols - 1) / kCombineCols), 1);
@@ -1362,18 +1473,17 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
         ccfg.stream = stream;
         ccfg.attrs = attr;   // programmatic serialization only
         ccfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&ccfg, rope ? sparse_attn_combine_kernel<D, true> : sparse_attn_combine_kernel<D, false>,
-                               cpar) != cudaSuccess)
-            return DS_ECUDA;
+        if (cudaLaunchKernelEx(&ccfg, combine, cpar) != cudaSuccess) return DS_ECUDA;
     }
     return DS_OK;
 }
 
 }  // namespace tc
 
-size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk) {
+size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk, bool pair) {
     (void)h;
-    const int64_t ntok = (int64_t)b * m;
+    const int64_t ntok = pair ? (int64_t)b * ((m + 1) / 2) : (int64_t)b * m;
+    if (pair) topk *= 2;
     switch (d) {
         case 64: return tc::workspace_bytes_for<64>(ntok, topk);
         case 128: return tc::workspace_bytes_for<128>(ntok, topk);

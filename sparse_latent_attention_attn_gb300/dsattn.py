@@ -46,6 +46,10 @@ _lib.ds_sparse_attn_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.ds_sparse_attn_workspace_bytes.restype = _sz
 _lib.ds_sparse_attn.argtypes = [_P, _P, _i64, _P, _P, _i32, _f32, _P, _i32, _i32, _i32, _i32, _P, _sz, _P]
 _lib.ds_sparse_attn.restype = _i32
+_lib.ds_sparse_attn_prefill_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
+_lib.ds_sparse_attn_prefill_workspace_bytes.restype = _sz
+_lib.ds_sparse_attn_prefill.argtypes = [_P, _P, _i64, _P, _P, _i32, _f32, _P, _i32, _i32, _i32, _i32, _P, _sz, _P]
+_lib.ds_sparse_attn_prefill.restype = _i32
 _lib.ds_sparse_attn_rope.argtypes = [_P, _P, _i64, _P, _P, _i32, _f32, _P, _i32, _i32, _i32, _i32, _P, _sz, _i32, _P,
                                     _i64, _i64, _P]
 _lib.ds_sparse_attn_rope.restype = _i32
@@ -170,6 +174,41 @@ def sparse_attn(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor, idx: torc
     _check("ds_sparse_attn",
            _lib.ds_sparse_attn(_ptr(q), _ptr(kv), n, _ptr(sink), _ptr(idx), topk, float(scale), _ptr(o), b, m, h, d,
                                _ptr(workspace), ws_bytes, _stream(stream)))
+    return o
+
+
+def sparse_attn_prefill_workspace_bytes(b: int, m: int, h: int, d: int, topk: int) -> int:
+    return int(_lib.ds_sparse_attn_prefill_workspace_bytes(b, m, h, d, topk))
+
+
+def sparse_attn_prefill(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor, idx: torch.Tensor, scale: float,
+                        o: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """``sparse_attn`` for a prefill chunk, queries 2j and 2j + 1 sharing one gather of the union
+    of their index rows (valid entries of a row must be distinct)."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv, torch.bfloat16, "kv")
+    _need(sink, torch.float32, "sink")
+    _need(idx, torch.int32, "idx")
+    b, m, h, d = q.shape
+    n = kv.shape[1]
+    topk = idx.shape[2]
+    if kv.shape != (b, n, d) or idx.shape[:2] != (b, m) or sink.shape != (h,):
+        raise ValueError("shape mismatch")
+    for t, name in ((q, "q"), (kv, "kv"), (idx, "idx"), (sink, "sink")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if o is None:
+        o = torch.empty_like(q)
+    elif o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous bf16 tensor shaped like q")
+    need = sparse_attn_prefill_workspace_bytes(b, m, h, d, topk)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("ds_sparse_attn_prefill",
+           _lib.ds_sparse_attn_prefill(_ptr(q), _ptr(kv), n, _ptr(sink), _ptr(idx), topk, float(scale), _ptr(o), b, m,
+                                       h, d, _ptr(workspace), ws_bytes, _stream(stream)))
     return o
 
 

@@ -34,10 +34,13 @@ def decode_step(q: torch.Tensor, kv: torch.Tensor, new_kv: torch.Tensor, sink: t
 
 def prefill_step(q: torch.Tensor, kv: torch.Tensor, ring: torch.Tensor, sink: torch.Tensor, idx: torch.Tensor,
                  window: int, scale: float, o: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                 stream=None) -> torch.Tensor:
+                 stream=None, pairs: bool = False) -> torch.Tensor:
     """q [b][s][h][d]; kv [b][s + C][d] (the raw chunk first, rounded in place); ring [b][window][d];
-    idx [b][s][min(s, window) + K] with the compressed columns already filled."""
+    idx [b][s][min(s, window) + K] with the compressed columns already filled.  pairs: neighbouring
+    queries share one gather (ds_sparse_attn_prefill; its own workspace size)."""
     b, s = q.shape[0], q.shape[1]
     dsattn.kv_quant_ring_write(kv[:, :s], ring, 0, window, stream=stream)
     dsattn.window_topk_idxs(idx, b, s, 0, window, stream=stream)
+    if pairs:
+        return dsattn.sparse_attn_prefill(q, kv, sink, idx, scale, o=o, workspace=workspace, stream=stream)
     return dsattn.sparse_attn(q, kv, sink, idx, scale, o=o, workspace=workspace, stream=stream)

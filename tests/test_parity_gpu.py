@@ -689,3 +689,116 @@ def test_writes_stay_inside_o_and_workspace(ds, fp8, d, h, b, m, topk):
     ref = oracle.sparse_attn(bits(q), kv_ref, sink.numpy(), idx.numpy(), d ** -0.5)
     assert_close_bf16(bits(o), ref)
     assert ds.device_status() == 0
+
+
+# ----------------------------------------------------------------------------------------------
+# prefill in pairs: queries 2j and 2j + 1 share one gather of the union of their rows
+# ----------------------------------------------------------------------------------------------
+
+def _prefill_rows(seed, b, m, n, window, K, ncomp, neg_tail=True):
+    """Index rows shaped like a prefill chunk's: query q's causal window rows (chunk positions
+    max(0, q - window + 1) .. q, -1 before the chunk start) then K compressed positions drawn
+    without replacement from the first q // 4 of ncomp (shifted past the chunk), ascending,
+    -1 padded at the tail."""
+    g = torch.Generator().manual_seed(seed)
+    W = min(m, window)
+    idx = torch.full((b, m, W + K), -1, dtype=torch.int32)
+    for qi in range(m):
+        lo = max(0, qi - window + 1)
+        win = torch.arange(lo, lo + W)
+        idx[:, qi, :W] = torch.where(win <= qi, win, -1).to(torch.int32)
+        avail = min(qi // 4, ncomp)
+        for bi in range(b):
+            if avail:
+                sel = torch.sort(torch.randperm(avail, generator=g)[:min(K, avail)]).values
+                idx[bi, qi, W:W + len(sel)] = (sel + m).to(torch.int32)
+    return idx
+
+
+PAIR_CASES = [
+    # seed, b, m, h, d, window, K, ncomp
+    (1, 1, 12, 4, 64, 8, 0, 0),            # the ratio-0 fixture's prefill shape
+    (2, 2, 37, 8, 64, 16, 24, 40),         # odd query count: the last pair has one query
+    (3, 1, 300, 64, 512, 128, 64, 200),    # more pairs than clusters: pairs cut across CTAs
+    (4, 3, 21, 64, 512, 128, 512, 1024),   # wide rows, few queries
+    (5, 1, 130, 32, 512, 128, 40, 60),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=[f"p{c[0]}" for c in PAIR_CASES])
+def test_prefill_pairs_match_oracle(ds, case):
+    seed, b, m, h, d, window, K, ncomp = case
+    n = m + ncomp
+    g = torch.Generator().manual_seed(600 + seed)
+    q = torch.randn((b, m, h, d), generator=g).to(torch.bfloat16)
+    kv = torch.randn((b, n, d), generator=g).to(torch.bfloat16)
+    sink = torch.randn((h,), generator=g)
+    idx = _prefill_rows(seed, b, m, n, window, K, ncomp)
+    o = ds.sparse_attn_prefill(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), d ** -0.5)
+    ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), idx.numpy(), d ** -0.5)
+    assert_close_bf16(bits(o), ref)
+    assert ds.device_status() == 0
+    # the same rows in any order (the union is sorted on the GPU), and repeatable bit for bit
+    perm = torch.randperm(idx.shape[-1], generator=torch.Generator().manual_seed(seed))
+    o2 = ds.sparse_attn_prefill(q.cuda(), kv.cuda(), sink.cuda(), idx[..., perm].contiguous().cuda(), d ** -0.5)
+    assert torch.equal(o, o2)
+
+
+def test_prefill_pairs_empty_and_shared_rows(ds):
+    """Pairs whose rows are all -1 (zeros out), pairs where only one query lists anything, and
+    pairs listing exactly the same rows."""
+    b, m, h, d, n = 2, 8, 16, 512, 200
+    g = torch.Generator().manual_seed(620)
+    q = torch.randn((b, m, h, d), generator=g).to(torch.bfloat16)
+    kv = torch.randn((b, n, d), generator=g).to(torch.bfloat16)
+    sink = torch.randn((h,), generator=g)
+    idx = torch.stack([torch.randperm(n, generator=g)[:90] for _ in range(b * m)]).view(b, m, 90).to(torch.int32)
+    idx[0, 0:2] = -1                  # pair 0 of sequence 0: nothing at all
+    idx[0, 3] = -1                    # pair 1: only its first query lists rows
+    idx[1, 5] = idx[1, 4]             # pair 2 of sequence 1: the same rows twice
+    o = ds.sparse_attn_prefill(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), d ** -0.5)
+    ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), idx.numpy(), d ** -0.5)
+    assert_close_bf16(bits(o), ref)
+    assert (o[0, 0:2].float() == 0).all() and (o[0, 3].float() == 0).all()
+    assert ds.device_status() == 0
+
+
+def test_prefill_pairs_flag_a_row_listed_twice(ds):
+    """This path counts a row once per query: a row listed twice by one query raises
+    DS_DEV_BAD_INDEX, and the output is that of the row listed once."""
+    b, m, h, d, n = 1, 4, 8, 64, 50
+    g = torch.Generator().manual_seed(630)
+    q = torch.randn((b, m, h, d), generator=g).to(torch.bfloat16)
+    kv = torch.randn((b, n, d), generator=g).to(torch.bfloat16)
+    sink = torch.randn((h,), generator=g)
+    idx = torch.stack([torch.randperm(n, generator=g)[:20] for _ in range(m)]).view(b, m, 20).to(torch.int32)
+    dup = idx.clone()
+    dup[0, 2, 5] = dup[0, 2, 4]
+    o = ds.sparse_attn_prefill(q.cuda(), kv.cuda(), sink.cuda(), dup.cuda(), 0.125)
+    assert ds.device_status() & ds.DS_DEV_BAD_INDEX
+    once = dup.clone()
+    once[0, 2, 5] = -1
+    ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), once.numpy(), 0.125)
+    assert_close_bf16(bits(o), ref)
+    assert ds.device_status() == 0
+
+
+def test_prefill_workload_in_pairs(ds):
+    """The prefill workload at full size (4096 queries, 64 heads, 512 wide, 128 window + 512
+    compressed rows) through the pair path, sampled tokens against the oracle, repeatable."""
+    w = wl.WORKLOADS[2]
+    gs = GpuStep(w)
+    need = ds.sparse_attn_prefill_workspace_bytes(w.b, w.m, w.h, w.d, w.topk)
+    gs.workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    from sparse_latent_attention_attn_gb300 import path
+    inp = gs.inp
+    path.prefill_step(inp.q, gs.kv, gs.ring, inp.sink, gs.idx, w.window, w.scale, o=gs.o, workspace=gs.workspace,
+                      pairs=True)
+    torch.cuda.synchronize()
+    orc = OracleStep(gs, seqs=[0])
+    toks = np.array(SAMPLE_TOKENS_PREFILL, dtype=np.int64)
+    assert_close_bf16(bits(gs.o[0, torch.from_numpy(toks).cuda()]), orc.attend(tokens=toks), "prefill pairs o")
+    first = gs.o.clone()
+    ds.sparse_attn_prefill(inp.q, gs.kv, inp.sink, gs.idx, w.scale, o=gs.o, workspace=gs.workspace)
+    assert torch.equal(first, gs.o)
+    assert ds.device_status() == 0
