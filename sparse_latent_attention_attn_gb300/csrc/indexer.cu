@@ -42,7 +42,7 @@ constexpr int BM = 128;             // keys per tile: M of the MMA, TMEM lanes
 constexpr int NSTAGE_MAX = 4;       // key tiles in flight, at most (barrier slots)
 constexpr int NTHREADS = 192;       // 6 warps
 constexpr int W_TMA = 4, W_MMA = 5;
-constexpr int CHUNK_TILES = 16;     // key tiles per CTA (2048 keys)
+constexpr int CHUNK_TILES_MAX = 16; // key tiles per CTA, at most (2048 keys)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 template <int D>
@@ -76,6 +76,7 @@ struct ScoreParams {
     int b, s, H, QB, N;      // N = QB * H: MMA N, columns of one accumulator
     int ratio;
     int nchunks;             // CTAs per query block along the keys
+    int chunk_tiles;         // key tiles per CTA
     int nstage;              // key stages (stages_for(N))
     uint32_t tmem_cols;
     unsigned int *status;
@@ -125,8 +126,8 @@ __global__ void __launch_bounds__(NTHREADS)
     const int i0 = (int)(qb % nqb) * p.QB;
     const int nq = min(p.QB, p.s - i0);
     const int64_t ntiles = (p.Tv + BM - 1) / BM;
-    const int64_t j0 = (int64_t)chunk * CHUNK_TILES;
-    const int64_t j1 = min(j0 + CHUNK_TILES, ntiles);
+    const int64_t j0 = (int64_t)chunk * p.chunk_tiles;
+    const int64_t j1 = min(j0 + p.chunk_tiles, ntiles);
     // keys the block's last query can see: tiles from there on are all -inf
     int64_t lens_max = (p.start_pos + i0 + nq) / p.ratio;
     if (lens_max > p.Tv) lens_max = p.Tv;
@@ -214,14 +215,26 @@ __global__ void __launch_bounds__(NTHREADS)
             const int64_t t = (j0 + it) * BM + tid;
             for (int qi = 0; qi < nq; ++qi) {
                 float sum = 0.0f;
-                for (int h0 = 0; h0 < p.H; h0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tmem + lane_off + (uint32_t)(acc * p.N + qi * p.H + h0), r);
+                // up to 64 heads per wait: four 16-column loads in flight, then one wait
+                for (int h0 = 0; h0 < p.H; h0 += 64) {
+                    uint32_t r[4][16];
+                    const uint32_t col = tmem + lane_off + (uint32_t)(acc * p.N + qi * p.H + h0);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        if (h0 + 16 * g < p.H) tmem_ld16(col + 16 * g, r[g]);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float dot = __uint_as_float(r[j]);
-                        sum = __fadd_rn(sum, __fmul_rn(dot > 0.0f ? dot : 0.0f, w_s[qi * p.H + h0 + j]));
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) asm volatile("" : "+r"(r[g][j]));
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (h0 + 16 * g >= p.H) break;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float dot = __uint_as_float(r[g][j]);
+                            sum = __fadd_rn(sum, __fmul_rn(dot > 0.0f ? dot : 0.0f, w_s[qi * p.H + h0 + 16 * g + j]));
+                        }
                     }
                 }
                 const int64_t lens = (p.start_pos + i0 + qi + 1) / p.ratio;
@@ -373,20 +386,26 @@ __global__ void __launch_bounds__(NT) indexer_select_kernel(const SelectParams p
     // Radix select of the kk-th largest key among positions [0, lens) in three digits: bits 31-20
     // (sign, exponent and three mantissa bits: enough distinct values that the histogram atomics
     // seldom collide), bits 19-8, bits 7-0.  Only keys that match the digits found so far count.
+    // Short rows (NT = 128) take four 8-bit digits instead: zeroing and scanning 4096 bins would
+    // cost more than the extra pass over a few hundred keys.
+    constexpr bool kWide = NT > 128;
+    constexpr int kPasses = kWide ? 3 : 4;
     uint32_t prefix = 0, pmask = 0;
     int rem = p.kk;
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 20 : pass == 1 ? 8 : 0;
-        const uint32_t dmask = pass == 2 ? 255u : 4095u;
-        for (int j = tid; j < 4096; j += NT) hist[j] = 0;
+    for (int pass = 0; pass < kPasses; ++pass) {
+        const int shift = kWide ? (pass == 0 ? 20 : pass == 1 ? 8 : 0) : 24 - 8 * pass;
+        const uint32_t dmask = kWide && pass < 2 ? 4095u : 255u;
+        // the digit search reads at least max(NT, 256) bins: the unused ones must be zero too
+        const int nbins = (int)dmask + 1 > (NT > 256 ? NT : 256) ? (int)dmask + 1 : (NT > 256 ? NT : 256);
+        for (int j = tid; j < nbins; j += NT) hist[j] = 0;
         __syncthreads();
         for (int64_t t = tid; t < lens; t += NT) {
             const uint32_t key = key_at(t);
             if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1);
         }
         __syncthreads();
-        if (pass < 2) find_digit<NT, 4096>(hist, rem, warp_sums, &s_digit, &s_rank);
+        if (dmask == 4095u) find_digit<NT, 4096>(hist, rem, warp_sums, &s_digit, &s_rank);
         else find_digit<NT, (NT > 256 ? NT : 256)>(hist, rem, warp_sums, &s_digit, &s_rank);
         prefix |= s_digit << shift;
         pmask |= dmask << shift;
@@ -489,10 +508,18 @@ int launch_scores(const IndexerArgs &a, float *scores, int64_t ld, cudaStream_t 
     p.N = N;
     p.ratio = a.ratio;
     const int64_t ntiles = (Tv + BM - 1) / BM;
-    p.nchunks = (int)((ntiles + CHUNK_TILES - 1) / CHUNK_TILES);
+    // chunks short enough that the grid covers every SM twice (two CTAs share an SM in decode),
+    // long enough that a CTA's set-up is spread over several tiles
+    const int64_t nqb = (int64_t)a.b * ((a.s + QB - 1) / QB);
+    int sms = 148;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t ct = (nqb * ntiles + 2 * sms - 1) / (2 * sms);
+    ct = ct < 2 ? 2 : ct > CHUNK_TILES_MAX ? CHUNK_TILES_MAX : ct;
+    p.chunk_tiles = (int)ct;
+    p.nchunks = (int)((ntiles + ct - 1) / ct);
     p.tmem_cols = tmem_cols_for(N);
     p.status = a.status;
-    const int64_t nqb = (int64_t)a.b * ((a.s + QB - 1) / QB);
     const int64_t grid = nqb * p.nchunks;
     if (grid > 0x7fffffff) return DS_EUNSUPPORTED;
     p.nstage = stages_for(N);

@@ -640,11 +640,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                             tc_fence_after();
                             // S = Q K^T: K rows as the K-major B operand; 16 columns = 32 bytes inside
                             // the 128-byte swizzle atom of chunk k/4; 8-row groups 1024 B apart
-                            const uint32_t kbase = base + C::SM_KV + stage * C::TILE_BYTES;
+                            // the start-address field (address >> 4, 14 bits) takes the K step's
+                            // offset directly: every operand lies below 256 KB of shared memory
+                            const uint64_t kdesc0 = smem_desc_sw128(base + C::SM_KV + stage * C::TILE_BYTES, 16, 1024);
 #pragma unroll
                             for (int k = 0; k < C::DH / 16; ++k) {
                                 const uint64_t bdesc =
-                                    smem_desc_sw128(kbase + (k >> 2) * C::CHUNK_BYTES + (k & 3) * 32, 16, 1024);
+                                    kdesc0 + (uint64_t)(((k >> 2) * C::CHUNK_BYTES + (k & 3) * 32) >> 4);
                                 mma_bf16_ts(tmem + C::S_COL + (J & 1) * BN, tmem + C::Q_COL + k * 8, bdesc, IDESC_S,
                                             k > 0 ? 1u : 0u);
                             }
@@ -673,15 +675,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         (!pq_first || pq_seg == 0 || mbar_test_wait(BAR(B_OFREE), (pq_seg - 1) & 1))) {
                         // P was written by st.shared (generic proxy) and fenced by its writers
                         tc_fence_after();
-                        const uint32_t pbase = base + C::p_off(Jp);
-                        const uint32_t vbase = base + C::SM_KV + pq_stage * C::TILE_BYTES;
+                        const uint64_t pdesc0 = smem_desc_sw128(base + C::p_off(Jp), 16, 1024);
+                        const uint64_t vdesc0 =
+                            smem_desc_sw128(base + C::SM_KV + pq_stage * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
 #pragma unroll
                         for (int k = 0; k < BN / 16; ++k) {
                             // P: K-major A operand, 16 columns = 32 bytes of each 128-byte row.
                             // V rows 16k..16k+15 as the MN-major B operand (d contiguous): 8-row
                             // groups 1024 B apart, 64-column chunks CHUNK_BYTES apart
-                            const uint64_t adesc = smem_desc_sw128(pbase + k * 32, 16, 1024);
-                            const uint64_t bdesc = smem_desc_sw128(vbase + k * 2048, C::CHUNK_BYTES, 1024);
+                            const uint64_t adesc = pdesc0 + (uint64_t)((k * 32) >> 4);
+                            const uint64_t bdesc = vdesc0 + (uint64_t)((k * 2048) >> 4);
                             mma_bf16_ss(tmem + C::O_COL, adesc, bdesc, IDESC_PV, (pq_first && k == 0) ? 0u : 1u);
                         }
                         mma_commit(BAR(B_EMPTY + pq_stage));

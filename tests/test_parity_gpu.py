@@ -800,5 +800,9 @@ def test_prefill_workload_in_pairs(ds):
     assert_close_bf16(bits(gs.o[0, torch.from_numpy(toks).cuda()]), orc.attend(tokens=toks), "prefill pairs o")
     first = gs.o.clone()
     ds.sparse_attn_prefill(inp.q, gs.kv, inp.sink, gs.idx, w.scale, o=gs.o, workspace=gs.workspace)
-    assert torch.equal(first, gs.o)
+    torch.cuda.synchronize()
+    diff = (first.float() - gs.o.float()).abs()
+    where = (diff > 0).any(dim=3).any(dim=2)[0].nonzero().flatten().tolist()
+    assert not where, (f"repeated call differs at {int((diff > 0).sum())} outputs (max {diff.max().item()}) "
+                       f"of tokens {where[:16]} ({len(where)} tokens)")
     assert ds.device_status() == 0
