@@ -55,9 +55,10 @@ struct Cfg {
     static constexpr int smem_bytes(int N, int nstage) { return nstage * TILE_BYTES + N * D * 2 + N * 4 + 256 + 1024; }
 };
 
-// Stages for a query block of N rows: decode blocks (N <= 64) take two, so two CTAs share an SM
-// and one's set-up overlaps the other's stream of key tiles; wider blocks take four.
-constexpr int stages_for(int N) { return N <= 64 ? 2 : NSTAGE_MAX; }
+// Stages for a query block of N rows: blocks of up to 128 rows take two, so two CTAs share an SM
+// (shared memory and TMEM both allow it) and one's set-up and latencies overlap the other's work;
+// wider blocks take four.
+constexpr int stages_for(int N) { return N <= 128 ? 2 : NSTAGE_MAX; }
 
 // barrier slots (8 bytes each)
 enum : int { B_FULL = 0, B_EMPTY = B_FULL + NSTAGE_MAX, B_AFULL = B_EMPTY + NSTAGE_MAX, B_AFREE = B_AFULL + 2,
@@ -486,8 +487,9 @@ uint32_t tmem_cols_for(int N) {
 template <int D>
 int launch_scores(const IndexerArgs &a, float *scores, int64_t ld, cudaStream_t stream) {
     using C = Cfg<D>;
-    // queries per block: as many as fit N <= 256 (prefill); one per sequence in decode
-    const int QB = a.s < 256 / a.H ? a.s : 256 / a.H;
+    // queries per block: up to 128 rows of N (two CTAs per SM), at least one query
+    const int qcap = a.H <= 128 ? 128 / a.H : 1;
+    const int QB = a.s < qcap ? a.s : qcap;
     const int N = QB * a.H;
     const int64_t Tv = (a.start_pos + a.s) / a.ratio;
     if (Tv <= 0) return DS_OK;
