@@ -357,6 +357,18 @@ int ds_device_status(ds_stream_t stream, unsigned int *bits_out);
  */
 void ds_test_set_stall(int on);
 
+/*
+ * ds_test_set_kernel -- test hook for the choice of attention kernel (no counterpart on the
+ * pages).  ds_sparse_attn runs one of two kernels with the same operation and tolerance: the
+ * 2-CTA cluster kernel (any supported shape) or, for d = 512 and h <= 64 with fewer tokens than
+ * SMs, the one-CTA kernel with a transposed accumulator.  which = 0: that automatic choice
+ * (default); 1: always the cluster kernel; 2: the one-CTA kernel for every d = 512, h <= 64 call
+ * of ds_sparse_attn, whatever the batch.  Process-wide; nothing in the library sets it.  The
+ * workspace of ds_sparse_attn_workspace_bytes suffices for either choice.
+ * Returns DS_OK, or DS_EINVAL for another value of which.
+ */
+int ds_test_set_kernel(int which);
+
 /* ds_status_string -- static text for a status code. */
 const char *ds_status_string(int status);
 

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "sparse_attn_ot.cuh"
 
 namespace dsattn {
 namespace {
@@ -304,6 +305,12 @@ int ds_indexer_topk(const uint16_t *q, const uint16_t *k, const float *w, int b,
 }
 
 void ds_test_set_stall(int on) { set_test_stall(on != 0); }
+
+int ds_test_set_kernel(int which) {
+    if (which < 0 || which > 2) return DS_EINVAL;
+    set_test_kernel(which);
+    return DS_OK;
+}
 
 int ds_device_status(ds_stream_t stream, unsigned int *bits_out) {
     unsigned int *p = status_word();

@@ -40,13 +40,18 @@
 #include <atomic>
 #include <mutex>
 
+#include "attn_split.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
+#include "sparse_attn_ot.cuh"
 
 namespace dsattn {
 namespace tc {
 
 using namespace ptx;
+using split::range_start;
+using split::unit_at;
+using split::kMaxCut;
 
 constexpr int BN = 64;            // gathered rows per tile: N of Q K^T, K of P V
 // compacted indices travel from the compaction warp to the gather warps through a ring of LR
@@ -146,9 +151,9 @@ enum : int {
     B_EMPTY = B_FULL + 5,       // [NSTAGE] MMA -> producer: stage free
     B_SFULL = B_EMPTY + 5,      // [2] MMA -> softmax, exchange: S ready (or the end marker)
     B_SFREE = B_SFULL + 2,      // [2] softmax, exchange -> MMA: S buffer read
-    // [4] softmax -> MMA: P of tile J written (slot J % 4).  Four slots: with three exchange
-    // buffers the softmax can finish tile J + 2 before the MMA thread has seen tile J, but not
-    // tile J + 4 (its peer scores need the P V of tile J + 1)
+    // [4] softmax -> MMA: P of tile J written (slot J % 4).  Four slots: with NX (at most three)
+    // exchange buffers the softmax can finish tile J + NX - 1 before the MMA thread has seen tile
+    // J, but not tile J + NX (its peer scores need the P V of tile J, which frees the buffer)
     B_PFULL = B_SFREE + 2,
     B_PVDONE = B_PFULL + 4,     // [4] MMA -> softmax, exchange: P V of tile J done (slot J % 4)
     B_QREADY = B_PVDONE + 4,    // softmax -> MMA: Q of the segment in TMEM
@@ -217,21 +222,6 @@ __device__ __forceinline__ uint32_t out_pair(float x0, float x1, int col, const 
     return v;
 }
 
-// Start of cluster c's range of the flattened entry space (token t holds entries [t T, t T + T)).
-// The G ranges split a cost line evenly, on which each token costs its T entries plus K: the fixed
-// work of a segment (the epilogue, the next token's q, refilling the row pipeline), measured at
-// about four tiles of rows.  A cluster that starts more tokens then gets fewer entries, instead of
-// finishing last.  A cut of the cost line inside a token's K part falls on that token's first
-// entry; K = 0 is the even split of the entries.  The host guarantees G * ntok * (T + K) < 2^63,
-// so the product is exact in 64 bits (a 128-bit division is a long software routine on the GPU).
-__host__ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t ntok, int64_t T, int64_t K, int64_t G) {
-    const int64_t TK = T + K;
-    if (TK <= 0 || G <= 0) return 0;
-    const int64_t x = (int64_t)(((uint64_t)c * (uint64_t)(ntok * TK)) / (uint64_t)G);
-    const int64_t tok = x / TK, r = x - tok * TK;
-    return tok * T + (r > K ? r - K : 0);
-}
-
 // Four packed entries kept in registers: a loop over constant indices selects the slot.
 struct PvRing {
     uint32_t e[4];
@@ -268,15 +258,6 @@ struct LaneRow {
     bool live;
 };
 
-// The work unit a cluster's position u in the unit order stands for.  With several queries per
-// sequence (prefill) the cost of a query grows with its position (its window and its visible
-// compressed rows fill up), so the order interleaves the units from both ends, 0, N-1, 1, N-2, ...:
-// any contiguous range of positions then holds light and heavy units alike and the clusters'
-// equal shares of the index entries become equal shares of the work.  The results do not depend
-// on the order.
-__host__ __device__ __forceinline__ int64_t unit_at(int64_t u, int64_t nunits, bool interleave) {
-    return interleave ? ((u & 1) ? nunits - 1 - (u >> 1) : (u >> 1)) : u;
-}
 template <bool PAIR>
 __device__ __forceinline__ LaneRow lane_row(int64_t u, int t, int h, int m, int useq) {
     if constexpr (!PAIR) {
@@ -1158,7 +1139,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
 // [y * kCombineCols, (y + 1) * kCombineCols) of cut token i for every head, one thread per head,
 // so each of its loads from the slots is 512 contiguous bytes per warp.
 constexpr int kCombineCols = 16;   // columns per block: many small blocks read the partials in parallel
-constexpr int kMaxCut = 160;      // cut tokens: at most one per range boundary, G <= SM count
 
 struct CombineParams {
     const float *sink;
@@ -1231,38 +1211,6 @@ __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const C
                             out_pair<D, ROPE>(acc[8 * k + 6], acc[8 * k + 7], c0 + 8 * k + 6, cs_row, cp.rd));
 }
 
-// The cut tokens of a launch (host): every token that some range boundary falls inside.
-// Returns the number of entries written to cut (at most kMaxCut), or -1 when a token has more
-// than 32 parts or there are too many cut tokens.
-int cut_tokens(int64_t ntok, int64_t T, int64_t K, int64_t G, int4 *cut) {
-    const int64_t E = ntok * T;
-    auto start = [&](int64_t c) { return range_start(c, ntok, T, K, G); };
-    int n = 0;
-    int64_t last_tok = -1;
-    for (int64_t c = 1; c < G; ++c) {
-        const int64_t eb = start(c);
-        if (eb % T == 0 || eb >= E) continue;
-        const int64_t tok = eb / T;
-        if (tok == last_tok) continue;               // already listed through an earlier boundary
-        last_tok = tok;
-        // parts: clusters whose ranges meet [tok T, tok T + T)
-        int64_t kf = c - 1;
-        while (kf > 0 && start(kf) > tok * T) --kf;
-        int np = 0;
-        uint32_t slots = 0;
-        for (int64_t k = kf; k < G && start(k) < (tok + 1) * T; ++k) {
-            if (start(k + 1) <= start(k)) continue;   // empty range
-            if (np >= 32) return -1;
-            if (start(k) / T != tok) slots |= 1u << np;          // token is k's last segment
-            if (np == 0) kf = k;
-            ++np;
-        }
-        if (n >= kMaxCut) return -1;
-        cut[n++] = make_int4((int)tok, (int)kf, np, (int)slots);
-    }
-    return n;
-}
-
 // ---------------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------------
@@ -1275,8 +1223,10 @@ struct DeviceInfo {
 constexpr int kMaxDev = 64;
 DeviceInfo g_dev[kMaxDev];
 std::mutex g_dev_mutex;
-// test switch of the bounded-wait path (ds_test_set_stall)
+// test switches: the bounded-wait path (ds_test_set_stall) and the kernel choice
+// (ds_test_set_kernel: 0 automatic, 1 the cluster kernel, 2 the one-CTA kernel where it applies)
 std::atomic<int> g_test_stall{0};
+std::atomic<int> g_test_kernel{0};
 
 // pair mode is built for the fixture's and the model's head_dim
 template <int D>
@@ -1327,30 +1277,9 @@ int max_clusters(int dev) {
     return nclusters;
 }
 
-// Cluster count for a problem: stream-K over all clusters when there are at least as many
-// tokens as clusters; otherwise each token gets the same number of clusters (split evenly),
-// but no split shorter than two tiles.
-int64_t choose_clusters(int64_t ntok, int topk, int gmax) {
-    if (ntok >= gmax) return gmax;
-    int64_t k = gmax / ntok;
-    const int64_t kmax = topk / (2 * BN) > 1 ? topk / (2 * BN) : 1;
-    if (k > kmax) k = kmax;
-    if (k > 32) k = 32;   // the combine kernel merges at most 32 parts per token
-    if (k < 1) k = 1;
-    return ntok * k;
-}
-
-// K of range_start: the per-segment cost when clusters run several tokens each (stream-K); when
-// the clusters split tokens evenly every part has the same fixed work, so the entries split evenly.
-int64_t seg_cost(int64_t ntok, int64_t G) { return G <= ntok ? 4 * BN : 0; }
-
-bool splits_tokens(int64_t ntok, int topk, int64_t G) {
-    if (G <= 1 || topk == 0) return false;
-    const int64_t K = seg_cost(ntok, G);
-    for (int64_t c = 1; c < G; ++c)
-        if (range_start(c, ntok, topk, K, G) % topk != 0) return true;
-    return false;
-}
+int64_t choose_clusters(int64_t ntok, int topk, int gmax) { return split::choose_ranges(ntok, topk, gmax, BN); }
+int64_t seg_cost(int64_t ntok, int64_t G) { return split::seg_cost(ntok, G, 4 * BN); }
+bool splits_tokens(int64_t ntok, int topk, int64_t G) { return split::splits_units(ntok, topk, G, seg_cost(ntok, G)); }
 
 // Workspace of one kernel variant for a problem on `dev` (0 when no token is cut).
 template <int D, bool F8>
@@ -1409,7 +1338,7 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
         cpar.useq = useq;
         cpar.interleave = useq > 1 ? 1 : 0;
         cpar.nunits = ntok;
-        cpar.ncut = cut_tokens(ntok, a.topk, K, G, cpar.cut);
+        cpar.ncut = split::cut_units(ntok, a.topk, K, G, cpar.cut);
         if (cpar.ncut <= 0) return DS_EUNSUPPORTED;
     }
 
@@ -1484,21 +1413,34 @@ int launch(const AttnArgs &a, cudaStream_t stream) {
 }  // namespace tc
 
 size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk, bool pair) {
-    (void)h;
     const int64_t ntok = pair ? (int64_t)b * ((m + 1) / 2) : (int64_t)b * m;
     if (pair) topk *= 2;
+    size_t need = 0;
     switch (d) {
-        case 64: return tc::workspace_bytes_for<64>(ntok, topk);
-        case 128: return tc::workspace_bytes_for<128>(ntok, topk);
-        case 256: return tc::workspace_bytes_for<256>(ntok, topk);
-        case 512: return tc::workspace_bytes_for<512>(ntok, topk);
+        case 64: need = tc::workspace_bytes_for<64>(ntok, topk); break;
+        case 128: need = tc::workspace_bytes_for<128>(ntok, topk); break;
+        case 256: need = tc::workspace_bytes_for<256>(ntok, topk); break;
+        case 512: need = tc::workspace_bytes_for<512>(ntok, topk); break;
         default: return 0;
     }
+    // the one-CTA kernel serves some of the same calls (the query does not know which: it also
+    // answers for the fp8 row store and the fused rotation), so the larger need is returned
+    if (sparse_attn_ot_supports(h, d, false, pair, false)) {
+        const size_t ot = sparse_attn_ot_workspace_bytes(ntok, topk);
+        if (ot > need) need = ot;
+    }
+    return need;
 }
 
 void set_test_stall(bool on) { tc::g_test_stall.store(on ? 1 : 0, std::memory_order_relaxed); }
+void set_test_kernel(int which) { tc::g_test_kernel.store(which, std::memory_order_relaxed); }
 
 int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream) {
+    const int force = tc::g_test_kernel.load(std::memory_order_relaxed);
+    const int64_t ntok = (int64_t)a.b * a.m;
+    if (force != 1 && sparse_attn_ot_supports(a.h, a.d, a.kv8 != nullptr, a.pair, a.rope != nullptr) &&
+        ntok * a.h <= INT32_MAX && (force == 2 || sparse_attn_ot_preferred(ntok)))
+        return launch_sparse_attn_ot(a, stream, tc::g_test_stall.load(std::memory_order_relaxed) != 0);
     if (a.kv8) return a.d == 512 ? tc::launch<512, true>(a, stream) : DS_EUNSUPPORTED;
     switch (a.d) {
         case 64: return tc::launch<64>(a, stream);

@@ -75,6 +75,8 @@ _lib.ds_indexer_topk.argtypes = [_P, _P, _P, _i32, _i32, _i32, _i32, _i64, _i64,
 _lib.ds_indexer_topk.restype = _i32
 _lib.ds_test_set_stall.argtypes = [_i32]
 _lib.ds_test_set_stall.restype = None
+_lib.ds_test_set_kernel.argtypes = [_i32]
+_lib.ds_test_set_kernel.restype = _i32
 _lib.ds_status_string.argtypes = [_i32]
 _lib.ds_status_string.restype = ctypes.c_char_p
 
@@ -458,6 +460,15 @@ def indexer_topk(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, start_pos: i
 def test_set_stall(on: bool) -> None:
     """Test hook: while on, every sparse_attn launch has a bounded wait run out (DS_DEV_TIMEOUT)."""
     _lib.ds_test_set_stall(1 if on else 0)
+
+
+KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_ONE_CTA = 0, 1, 2
+
+
+def test_set_kernel(which: int) -> None:
+    """Test hook: the attention kernel ds_sparse_attn runs (KERNEL_AUTO, KERNEL_CLUSTER or
+    KERNEL_ONE_CTA, the latter wherever it is built for the shape)."""
+    _check("ds_test_set_kernel", _lib.ds_test_set_kernel(int(which)))
 
 
 def status_string(status: int) -> str:

@@ -1,0 +1,167 @@
+"""The one-CTA sparse_attn kernel (head_dim 512, at most 64 heads, transposed accumulator) against
+the oracle, through the C ABI.
+
+ds_sparse_attn picks this kernel by itself for decode batches (fewer tokens than SMs); the test
+switch ds_test_set_kernel forces either kernel, so every case here runs on both and each result
+is held to the attention tolerance against the oracle ("Module attn", sparse_attn and the
+Precision paragraph: |gpu - ref| <= 1e-2 + 1.6e-2 |ref|).  Cases cover whole and cut tokens
+(partials merged by the combine kernel), ragged last tiles, odd head counts, entries that are
+-1, duplicated or out of range, rows with no valid entry, many parts per token, more tokens than
+SMs (several segments per CTA, forced), and scores that grow along the index row so the running
+max moves and the accumulator is rescaled.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from pathcheck import assert_close_bf16, bits
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = {"cluster": 1, "one_cta": 2}
+
+
+@pytest.fixture(scope="module")
+def ds():
+    from sparse_latent_attention_attn_gb300 import dsattn
+    dsattn.device_status()
+    return dsattn
+
+
+@pytest.fixture(params=list(KERNELS), ids=list(KERNELS))
+def kernel(ds, request):
+    ds.test_set_kernel(KERNELS[request.param])
+    yield request.param
+    ds.test_set_kernel(ds.KERNEL_AUTO)
+
+
+def _case(seed, b, m, h, n, topk, neg=0.05, dup=False, grow=0.0, qscale=1.0, d=512):
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn((b, m, h, d), generator=g) * qscale).to(torch.bfloat16)
+    kv = torch.randn((b, n, d), generator=g)
+    if grow:
+        # row r scaled by 1 + grow * r / n: with ascending indices the later tiles score higher
+        kv = kv * (1.0 + grow * torch.arange(n, dtype=torch.float32) / n).view(1, n, 1)
+    kv = kv.to(torch.bfloat16)
+    sink = torch.randn((h,), generator=g)
+    if dup or topk > n:
+        idx = torch.randint(0, n, (b, m, topk), generator=g)
+    else:
+        idx = torch.stack([torch.randperm(n, generator=g)[:topk] for _ in range(b * m)]).view(b, m, topk)
+    if grow:
+        idx = idx.sort(dim=-1).values
+    idx = torch.where(torch.rand((b, m, topk), generator=g) < neg, -1, idx).to(torch.int32)
+    return q, kv, sink, idx
+
+
+def _check(ds, q, kv, sink, idx, what):
+    d = q.shape[-1]
+    scale = d ** -0.5
+    o = ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
+    ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), idx.numpy(), scale)
+    assert_close_bf16(bits(o), ref, what)
+    return o
+
+
+CASES = [
+    # seed, b, m, h, n, topk, neg
+    (1, 2, 2, 64, 700, 640, 0.05),       # 4 tokens, each cut over several CTAs
+    (2, 1, 1, 64, 300, 1, 0.0),          # a single entry
+    (3, 3, 1, 33, 500, 129, 0.3),        # odd head count, ragged last tile, many -1
+    (4, 4, 1, 16, 900, 300, 0.1),
+    (5, 40, 2, 64, 1000, 200, 0.05),     # 80 tokens
+    (6, 32, 1, 64, 4224, 640, 0.05),     # decode_comp's shape
+    (7, 1, 4, 64, 5000, 2176, 0.02),     # decode_large's index width, 64 heads
+    (8, 1, 1, 64, 12000, 8192, 0.02),    # one token over 32 CTAs
+    (9, 64, 1, 64, 128, 128, 0.0),       # decode_window's shape: whole tokens, no combine
+    (10, 2, 1, 8, 200, 70, 0.0),         # 8 heads, a 6-entry last tile
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{c[0]}" for c in CASES])
+def test_attn_matches_oracle_on_both_kernels(ds, kernel, case):
+    seed, b, m, h, n, topk, neg = case
+    q, kv, sink, idx = _case(seed, b, m, h, n, topk, neg)
+    _check(ds, q, kv, sink, idx, f"{kernel} c{seed}")
+    assert ds.device_status() == 0
+
+
+@pytest.mark.parametrize("ntok,h,topk", [(200, 8, 257), (300, 64, 640), (1000, 32, 130)])
+def test_more_tokens_than_sms(ds, kernel, ntok, h, topk):
+    """Several segments per CTA (stream-K ranges cut inside tokens): every token is checked."""
+    q, kv, sink, idx = _case(60 + h, ntok, 1, h, 3 * topk, topk, 0.05)
+    _check(ds, q, kv, sink, idx, f"{kernel} stream-k")
+    assert ds.device_status() == 0
+
+
+@pytest.mark.parametrize("grow,qscale", [(3.0, 4.0), (8.0, 8.0)])
+def test_running_max_moves_along_the_row(ds, kernel, grow, qscale):
+    """Index rows ascending over rows whose norms grow along kv: each tile's scores exceed the
+    running max of the earlier ones by many log2 units, so the lazy rescale of the accumulator
+    runs, on whole tokens and on cut ones."""
+    q, kv, sink, idx = _case(70, 3, 1, 64, 6000, 1500, 0.02, grow=grow, qscale=qscale)
+    _check(ds, q, kv, sink, idx, f"{kernel} rescale")
+    assert ds.device_status() == 0
+
+
+def test_invalid_duplicate_and_out_of_range_entries(ds, kernel):
+    """-1 everywhere in one token (its output is 0), duplicates counted as listed, and entries
+    >= n skipped and flagged with DS_DEV_BAD_INDEX."""
+    q, kv, sink, idx = _case(80, 4, 1, 64, 300, 400, 0.1, dup=True)
+    idx[1] = -1
+    o = _check(ds, q, kv, sink, idx, f"{kernel} dup")
+    assert (o[1].float() == 0).all()
+    assert ds.device_status() == 0
+    bad = idx.clone()
+    bad[2, 0, 5] = 300
+    bad[3, 0, 399] = 1 << 30
+    ref_idx = bad.clone()
+    ref_idx[ref_idx >= 300] = -1
+    scale = 512 ** -0.5
+    got = ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), bad.cuda(), scale)
+    ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), ref_idx.numpy(), scale)
+    assert_close_bf16(bits(got), ref, f"{kernel} out of range")
+    assert ds.device_status() & ds.DS_DEV_BAD_INDEX
+    assert ds.device_status() == 0
+
+
+def test_both_kernels_agree_and_repeat_exactly(ds):
+    """On decode_comp's shape the two kernels give results within the attention tolerance of each
+    other, and each repeats bit for bit."""
+    q, kv, sink, idx = _case(90, 32, 1, 64, 4224, 640, 0.05)
+    scale = 512 ** -0.5
+    outs = {}
+    try:
+        for name, which in KERNELS.items():
+            ds.test_set_kernel(which)
+            a = ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
+            b = ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
+            assert torch.equal(a, b), f"{name}: repeated calls differ"
+            outs[name] = bits(a)
+    finally:
+        ds.test_set_kernel(ds.KERNEL_AUTO)
+    assert_close_bf16(outs["one_cta"], outs["cluster"], "one_cta against cluster")
+    assert ds.device_status() == 0
+
+
+def test_timed_out_wait_is_reported(ds):
+    """The one-CTA kernel's bounded waits, made to run out with the stall hook (the gather warps
+    withhold the first tile's arrivals): the call ends, raises DS_DEV_TIMEOUT, and the next call
+    is clean and correct."""
+    q, kv, sink, idx = _case(95, 4, 1, 64, 2048, 700)
+    scale = 512 ** -0.5
+    assert ds.device_status() == 0
+    ds.test_set_kernel(KERNELS["one_cta"])
+    try:
+        ds.test_set_stall(True)
+        try:
+            ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
+            status_bits = ds.device_status()
+        finally:
+            ds.test_set_stall(False)
+        assert status_bits & ds.DS_DEV_TIMEOUT, f"expected a timeout, status bits {status_bits}"
+        _check(ds, q, kv, sink, idx, "after a timeout")
+    finally:
+        ds.test_set_kernel(ds.KERNEL_AUTO)
+    assert ds.device_status() == 0

@@ -5,6 +5,8 @@ outputs must satisfy |gpu - oracle| <= 1e-2 + 1.6e-2 * |oracle| elementwise ("Mo
 Precision paragraph: f32 arithmetic, bf16 result, compared at bf16 tolerance, window indices
 exactly).
 """
+from contextlib import contextmanager
+
 import numpy as np
 import pytest
 import torch
@@ -21,6 +23,16 @@ def ds():
     from sparse_latent_attention_attn_gb300 import dsattn
     dsattn.device_status()      # clear anything left over
     return dsattn
+
+
+@contextmanager
+def _kernel(ds, which):
+    """Run ds_sparse_attn on one attention kernel (ds_test_set_kernel) inside the block."""
+    ds.test_set_kernel(which)
+    try:
+        yield
+    finally:
+        ds.test_set_kernel(ds.KERNEL_AUTO)
 
 
 def _bf16_from_bits(b: np.ndarray) -> torch.Tensor:
@@ -410,24 +422,29 @@ def test_repeated_calls_finish_without_timeouts(ds):
         assert torch.equal(first, gs.o), f"cfg{cfg}: repeated calls differ"
 
 
-@pytest.mark.parametrize("d,h,b,topk", [(512, 64, 4, 700), (64, 8, 2, 300)])
+@pytest.mark.parametrize("d,h,b,topk", [(512, 64, 4, 700), (512, 128, 4, 700), (64, 8, 2, 300)])
 def test_timed_out_wait_is_reported_and_context_stays_usable(ds, d, h, b, topk):
     """The kernel's bounded waits, made to run out without any GPU fault: with the test hook
     ds_test_set_stall on, the gather warps withhold the first tile's arrivals, so the MMA thread's
     wait gives up after its time limit.  The call must end (no hang), raise DS_DEV_TIMEOUT, and
     leave the context usable: the next call without the switch is clean and agrees with the
-    oracle.  Covers the 2-CTA cluster path (d = 512) and the single-CTA path (d = 64)."""
-    q, kv, sink, idx = _case(40 + d, b, 1, h, d, 2048, topk)
+    oracle.  Covers the 2-CTA cluster kernel (d = 512, forced for 64 heads, where a decode batch
+    would otherwise take the one-CTA kernel) and its single-CTA form (d = 64)."""
+    q, kv, sink, idx = _case(40 + d + h, b, 1, h, d, 2048, topk)
     scale = d ** -0.5
     assert ds.device_status() == 0
-    ds.test_set_stall(True)
+    ds.test_set_kernel(ds.KERNEL_CLUSTER)
     try:
-        ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
-        bits_after = ds.device_status()
+        ds.test_set_stall(True)
+        try:
+            ds.sparse_attn(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), scale)
+            bits_after = ds.device_status()
+        finally:
+            ds.test_set_stall(False)
+        assert bits_after & ds.DS_DEV_TIMEOUT, f"expected a timeout, status bits {bits_after}"
+        _check_case(ds, q, kv, sink, idx, scale)
     finally:
-        ds.test_set_stall(False)
-    assert bits_after & ds.DS_DEV_TIMEOUT, f"expected a timeout, status bits {bits_after}"
-    _check_case(ds, q, kv, sink, idx, scale)
+        ds.test_set_kernel(ds.KERNEL_AUTO)
     assert ds.device_status() == 0
 
 
@@ -503,8 +520,9 @@ FP8_ATTN = [
 @pytest.mark.parametrize("case", FP8_ATTN, ids=[f"f{c[0]}" for c in FP8_ATTN])
 def test_attn_fp8kv_is_bit_identical_to_bf16_on_decoded_rows(ds, case):
     """The fp8 gather decodes each row on chip to the bf16 values of the round trip, so the MMA
-    sees identical operands: the output must equal ds_sparse_attn on the decoded rows bit for bit,
-    and match the oracle on those rows."""
+    sees identical operands: the output must equal ds_sparse_attn on the decoded rows bit for bit
+    (the same cluster kernel, which the fp8 row store always runs), and match the oracle on those
+    rows."""
     seed, b, m, h, n, topk, neg = case
     q, _, sink, idx = _case(seed, b, m, h, 512, n, topk, neg)
     kv = _spread_rows(seed, b * n, 512).view(b, n, 512)
@@ -512,7 +530,8 @@ def test_attn_fp8kv_is_bit_identical_to_bf16_on_decoded_rows(ds, case):
     dec = oracle.kv_dequantize_fp8(codes.cpu().numpy(), exps.cpu().numpy())
     assert np.array_equal(dec, oracle.act_quant_inplace(bits(kv).copy().reshape(-1)).reshape(dec.shape))
     kv_dec = _bf16_from_bits(dec)
-    o_bf16, _ = _check_case(ds, q, kv_dec, sink, idx, 512 ** -0.5)
+    with _kernel(ds, ds.KERNEL_CLUSTER):
+        o_bf16, _ = _check_case(ds, q, kv_dec, sink, idx, 512 ** -0.5)
     o_f8 = ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), 512 ** -0.5)
     assert torch.equal(o_f8, o_bf16)
     assert ds.device_status() == 0
@@ -533,7 +552,8 @@ def test_attn_fp8kv_ring_then_attend(ds):
     ds.kv_quant_ring_write(new_b, kv_bf, p0, W)
     q, _, sink, idx = _case(82, b, 1, h, d, n, 700, 0.02)
     o_f8 = ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), d ** -0.5)
-    o_bf = ds.sparse_attn(q.cuda(), kv_bf, sink.cuda(), idx.cuda(), d ** -0.5)
+    with _kernel(ds, ds.KERNEL_CLUSTER):
+        o_bf = ds.sparse_attn(q.cuda(), kv_bf, sink.cuda(), idx.cuda(), d ** -0.5)
     assert torch.equal(new_a, new_b)
     assert torch.equal(o_f8, o_bf)
     ref = oracle.sparse_attn(bits(q), bits(kv_bf), sink.numpy(), idx.numpy(), d ** -0.5)
@@ -602,15 +622,16 @@ def test_kv_rope_ring_write_bit_exact(ds, b, s, d, W, p0, rd):
 def test_sparse_attn_rope_equals_attention_then_inverse_rotation(ds, d, h, b, m, topk, rd, p0):
     """The inverse RoPE of the output fused into the attention epilogue and the combine
     ("DeepSeek V4.1", attention/query-latent, Attention.forward rotates o back by its position):
-    bit-identical to ds_sparse_attn followed by ds_apply_rotary(inverse), and to the oracle's
-    rotation of that attention output; the attention itself matches the oracle within the
-    tolerance."""
+    bit-identical to ds_sparse_attn followed by ds_apply_rotary(inverse) on the same (cluster)
+    kernel, which the fused rotation always runs, and to the oracle's rotation of that attention
+    output; the attention itself matches the oracle within the tolerance."""
     q, kv, sink, idx = _case(700 + d + m, b, m, h, d, 2 * topk, topk, 0.05)
     table = oracle.rope_table(p0 + m, rd, 10000.0)
     tg = torch.from_numpy(table).cuda()
     qg, kvg, sg, ig = q.cuda(), kv.cuda(), sink.cuda(), idx.cuda()
     fused = ds.sparse_attn_rope(qg, kvg, sg, ig, d ** -0.5, rd, tg, p0)
-    plain = ds.sparse_attn(qg, kvg, sg, ig, d ** -0.5)
+    with _kernel(ds, ds.KERNEL_CLUSTER):
+        plain = ds.sparse_attn(qg, kvg, sg, ig, d ** -0.5)
     ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), idx.numpy(), d ** -0.5)
     assert_close_bf16(bits(plain), ref)
     want = oracle.apply_rotary(bits(plain).copy(), rd, table, p0, h, m, True)
