@@ -39,6 +39,9 @@ DEFAULT_CONFIG = 4
 L2_BYTES = 129 * 1024 * 1024
 SLEEP_CYCLES = 40_000_000      # ~20 ms of device time: long enough for the host to enqueue a run
 ATTN_KERNEL_SOURCES = ["sparse_latent_attention_attn_gb300/csrc/sparse_attn_tc.cu",
+                       "sparse_latent_attention_attn_gb300/csrc/sparse_attn_ot.cu",
+                       "sparse_latent_attention_attn_gb300/csrc/sparse_attn_ot.cuh",
+                       "sparse_latent_attention_attn_gb300/csrc/attn_split.cuh",
                        "sparse_latent_attention_attn_gb300/csrc/ptx.cuh",
                        "sparse_latent_attention_attn_gb300/csrc/common.cuh"]
 PROFILE_SUMMARY = "profiles/sparse_attn_{workload}.txt"
@@ -196,11 +199,15 @@ class StepSet:
                 else dsattn.sparse_attn_workspace_bytes(w.b, w.m, w.h, w.d, w.topk))
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         # library kernels per step: ring write, window rows, sparse_attn (+ combine when tokens are cut)
+        self.attn_kernel = dsattn.KERNEL_CLUSTER
         if pairs:   # ring write, window rows, the pair union, attention, and the combine when pairs are cut
             union = (w.b * ((w.m + 1) // 2) * 2 * w.topk * 4 + 255) // 256 * 256
             self.launches = 4 + (1 if need > union else 0)
-        else:
+        elif self.fp8:
             self.launches = 3 + (1 if need > 0 else 0)
+        else:
+            n_attn, self.attn_kernel = dsattn.sparse_attn_launches(w.b, w.m, w.h, w.d, w.topk)
+            self.launches = 2 + n_attn
 
     def attend(self, ev=None):
         """sparse_attn alone on the step's inputs; events (start, end) around it when given."""
@@ -636,7 +643,9 @@ def run_ours(args):
         roof["frac"] = roof["achieved"] / roof["peak"]
         roof["traffic"] = profiled_traffic(w.name, 1)
         roof["peak_source"] = peaks["source"]
-        roof["kernel"] = "sparse_attn (tcgen05 kernel + combine)"
+        roof["kernel"] = ("sparse_attn_ot_kernel (one CTA per work range, transposed accumulator)"
+                          if sets[0].attn_kernel == dsattn.KERNEL_ONE_CTA else
+                          "sparse_attn_tc_kernel (2-CTA cluster, d split)") + " + combine when tokens are cut"
         roof["kernel_source_sha256_16"] = kernel_source_hash()
         roof["kernel_ms"] = attn_s * 1e3
         roof["roofline_ms"] = max(t_hbm, t_tc) * 1e3

@@ -358,13 +358,23 @@ int ds_device_status(ds_stream_t stream, unsigned int *bits_out);
 void ds_test_set_stall(int on);
 
 /*
+ * ds_sparse_attn_launches -- the kernels a ds_sparse_attn call of this shape enqueues on the
+ * current device (no counterpart on the pages; for accounting and tests).  Returns how many (0 for
+ * an empty batch; 1 for topk = 0, the zero fill), and stores to *kernel (may be NULL) which
+ * attention kernel runs: 1 the 2-CTA cluster kernel, 2 the one-CTA kernel (see
+ * ds_test_set_kernel).  Pure host function.  Returns DS_EINVAL for a shape ds_sparse_attn rejects.
+ */
+int ds_sparse_attn_launches(int b, int m, int h, int d, int topk, int *kernel);
+
+/*
  * ds_test_set_kernel -- test hook for the choice of attention kernel (no counterpart on the
  * pages).  ds_sparse_attn runs one of two kernels with the same operation and tolerance: the
- * 2-CTA cluster kernel (any supported shape) or, for d = 512 and h <= 64 with fewer tokens than
- * SMs, the one-CTA kernel with a transposed accumulator.  which = 0: that automatic choice
- * (default); 1: always the cluster kernel; 2: the one-CTA kernel for every d = 512, h <= 64 call
- * of ds_sparse_attn, whatever the batch.  Process-wide; nothing in the library sets it.  The
- * workspace of ds_sparse_attn_workspace_bytes suffices for either choice.
+ * 2-CTA cluster kernel (any supported shape) or, for d = 512 and h <= 64, the one-CTA kernel
+ * with a transposed accumulator (ds_sparse_attn_rope and ds_sparse_attn_fp8kv always run the
+ * cluster kernel).  which = 0: that automatic choice (default); 1: always the cluster kernel;
+ * 2: the one-CTA kernel wherever it is built for the shape (the same as 0 today).
+ * Process-wide; nothing in the library sets it.  The workspace of
+ * ds_sparse_attn_workspace_bytes suffices for either choice.
  * Returns DS_OK, or DS_EINVAL for another value of which.
  */
 int ds_test_set_kernel(int which);

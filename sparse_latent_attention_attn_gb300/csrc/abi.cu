@@ -306,6 +306,11 @@ int ds_indexer_topk(const uint16_t *q, const uint16_t *k, const float *w, int b,
 
 void ds_test_set_stall(int on) { set_test_stall(on != 0); }
 
+int ds_sparse_attn_launches(int b, int m, int h, int d, int topk, int *kernel) {
+    if (b < 0 || m < 0 || h < 1 || h > 128 || topk < 0 || !supported_head_dim(d)) return DS_EINVAL;
+    return sparse_attn_plan(b, m, h, d, topk, kernel);
+}
+
 int ds_test_set_kernel(int which) {
     if (which < 0 || which > 2) return DS_EINVAL;
     set_test_kernel(which);

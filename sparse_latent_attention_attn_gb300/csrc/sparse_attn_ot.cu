@@ -91,6 +91,8 @@ constexpr float kRescaleThreshold = 8.0f;           // log2 units
 // A partial slot (f32): O^T of the token's part, element (head h, column d) at
 // ((h / 4) * D + d) * 4 + h % 4, so a warp's stores and loads (consecutive d) are 512 contiguous
 // bytes; then the running maxima (log2 domain, -inf: no row) and the sums of the 64 heads.
+// The cluster merge uses one slot per CTA, chunk by chunk: element (h, 128 c + d) at
+// c * 128 * HM + ((h / 4) * 128 + d) * 4 + h % 4.
 constexpr int SLOT_O = HM * D;
 constexpr size_t SLOT = (size_t)SLOT_O + 2 * HM;
 
@@ -105,7 +107,8 @@ enum : int {
     B_PVDONE = B_PFULL + NPB,   // [4] MMA -> softmax: P V of tile J done (slot J % 4)
     B_OFREE = B_PVDONE + 4,     // softmax -> MMA: the epilogue has read O^T
     B_DRAIN = B_OFREE + 1,      // MMA drain on abort
-    B_COUNT = B_DRAIN + 1
+    B_XCH = B_DRAIN + 1,        // cluster merge: the other CTAs' accumulator chunks are in the workspace
+    B_COUNT = B_XCH + 1
 };
 constexpr int MASK_OFF = 256;                      // [NST] uint64: the tile's valid entries
 constexpr int TMEM_ADDR_OFF = MASK_OFF + 8 * NST;
@@ -113,7 +116,8 @@ constexpr int ABORT_OFF = TMEM_ADDR_OFF + 4;
 constexpr int VOTE_OFF = ABORT_OFF + 4;            // [2] int: tile number of a rescale request
 constexpr int FAC_OFF = 512;                       // [64] f32: rescale factors
 constexpr int INV_OFF = FAC_OFF + 4 * HM;          // [64] f32: 1 / denominator (whole tokens)
-static_assert(8 * B_COUNT <= MASK_OFF && VOTE_OFF + 8 <= FAC_OFF && INV_OFF + 4 * HM <= BAR_BYTES, "barrier block");
+constexpr int WGT_OFF = INV_OFF + 4 * HM;          // [KC][64] f32: cluster merge weights (KC <= 4)
+static_assert(8 * B_COUNT <= MASK_OFF && VOTE_OFF + 8 <= FAC_OFF && WGT_OFF + 16 * HM <= BAR_BYTES, "barrier block");
 
 struct Params {
     const uint16_t *q;
@@ -160,6 +164,16 @@ __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool pred) {
 // they complete, and are counted, like the row copies beside them.
 __device__ __forceinline__ void cp_async_zero16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster with release semantics at cluster scope:
+// the arriving thread's earlier writes (and those it has observed) are visible to a thread that
+// acquires the phase at cluster scope.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t remote_bar) {
+    asm volatile(
+        "fence.acq_rel.cluster;\n\t"
+        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+        : "memory");
 }
 
 // TMA load of a 2-D box into shared memory, completing `bar` by the bytes it writes.
@@ -210,8 +224,14 @@ struct TileIter {
 
 // qmap: q as [b m h rows][512] bf16, boxes of 64 columns x h rows, 128-byte swizzle (the MMA's
 // operand layout).
+// KC > 1: the grid is a cluster of KC CTAs per token, each taking an equal part of the token's
+// index row; they merge their accumulators among themselves (no combine kernel): each CTA writes
+// the 128-column chunks of O^T that other CTAs own (chunk c belongs to rank c % KC) with its
+// running max and sum, tells the others through their XCH barriers, and finishes its own chunks.
+template <int KC>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __grid_constant__ CUtensorMap qmap,
                                                                      const Params p) {
+    static_assert(KC >= 1 && KC <= 4, "cluster merge of 2 to 4 parts");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -246,6 +266,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
         for (int i = 0; i < 4; ++i) mbar_init(BAR(B_PVDONE + i), 1);
         mbar_init(BAR(B_OFREE), 128);
         mbar_init(BAR(B_DRAIN), 1);
+        mbar_init(BAR(B_XCH), KC > 1 ? KC - 1 : 1);     // one arrival per other CTA of the cluster
         *abort_flag = 0;
         vote[0] = -1;
         vote[1] = -1;
@@ -626,6 +647,97 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                                     __bfloat16_as_ushort(__float2bfloat16_rn(xv[k]));
                     }
                 }
+            } else if constexpr (KC > 1) {
+                // cluster merge of the token's KC parts (this CTA is part `rank`)
+                const int rank = (int)(cid % KC);
+                float *wsme = p.ws + (size_t)cid * SLOT;
+                if (live) {
+                    wsme[SLOT_O + hl] = any ? m_used : -INFINITY;
+                    wsme[SLOT_O + HM + hl] = l;
+                }
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    if (c % KC == rank) continue;
+                    uint32_t r[2][32];
+                    tmem_ld32(tmem + lane_off + O_COL + c * HM, r[0]);
+                    tmem_ld32(tmem + lane_off + O_COL + c * HM + 32, r[1]);
+                    tmem_ld_wait(r);
+                    float4 *dst = reinterpret_cast<float4 *>(wsme + c * 128 * HM) + dl;
+#pragma unroll
+                    for (int hq = 0; hq < HM / 4; ++hq)
+                        if (hq * 4 < p.h)
+                            dst[hq * 128] = make_float4(
+                                __uint_as_float(r[hq >> 3][4 * (hq & 7)]), __uint_as_float(r[hq >> 3][4 * (hq & 7) + 1]),
+                                __uint_as_float(r[hq >> 3][4 * (hq & 7) + 2]), __uint_as_float(r[hq >> 3][4 * (hq & 7) + 3]));
+                }
+                // every softmax thread's writes are in, then one release per other CTA
+                named_bar_sync(2, 128);
+                if (threadIdx.x == 0) {
+                    const uint32_t me = cluster_ctarank();
+                    for (uint32_t j = 0; j < (uint32_t)KC; ++j)
+                        if (j != me) mbar_arrive_release_cluster(mapa(BAR(B_XCH), j));
+                }
+                // the other parts' chunks and statistics
+                const bool okx = mbar_wait<true>(BAR(B_XCH), 0u, abort_flag, kWaitLimitNs);
+                float *wgt = reinterpret_cast<float *>(sbase + SM_BAR + WGT_OFF);
+                if (hl >= 0) {
+                    if (live && okx) {
+                        const float *part0 = p.ws + (size_t)(cid - rank) * SLOT;
+                        float mi[KC], li[KC];
+#pragma unroll
+                        for (int i = 0; i < KC; ++i) {
+                            mi[i] = part0[(size_t)i * SLOT + SLOT_O + hl];
+                            li[i] = part0[(size_t)i * SLOT + SLOT_O + HM + hl];
+                        }
+                        float top = sink2;
+#pragma unroll
+                        for (int i = 0; i < KC; ++i) top = fmaxf(top, mi[i]);
+                        float den = ex2(sink2 - top);
+#pragma unroll
+                        for (int i = 0; i < KC; ++i)
+                            if (mi[i] != -INFINITY) den += ex2(mi[i] - top) * li[i];
+                        const float inv = 1.0f / den;
+#pragma unroll
+                        for (int i = 0; i < KC; ++i) wgt[i * HM + hl] = mi[i] == -INFINITY ? 0.0f : ex2(mi[i] - top) * inv;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < KC; ++i) wgt[i * HM + hl] = 0.0f;
+                    }
+                }
+                if (bar_red_or(1, 128, !__all_sync(0xffffffffu, okx))) {
+                    failed = true;
+                    break;
+                }
+                uint16_t *obase = p.o + utok * p.h * (int64_t)D;
+#pragma unroll 1
+                for (int c = rank; c < 4; c += KC) {
+                    uint32_t r[2][32];
+                    tmem_ld32(tmem + lane_off + O_COL + c * HM, r[0]);
+                    tmem_ld32(tmem + lane_off + O_COL + c * HM + 32, r[1]);
+                    tmem_ld_wait(r);
+                    float acc[HM];
+#pragma unroll
+                    for (int j = 0; j < HM; ++j) acc[j] = __uint_as_float(r[j >> 5][j & 31]) * wgt[rank * HM + j];
+#pragma unroll 1
+                    for (int i = 0; i < KC; ++i) {
+                        if (i == rank) continue;
+                        const float4 *src = reinterpret_cast<const float4 *>(p.ws + (size_t)(cid - rank + i) * SLOT + c * 128 * HM) + dl;
+#pragma unroll
+                        for (int hq = 0; hq < HM / 4; ++hq) {
+                            if (hq * 4 < p.h) {
+                                const float4 v = src[hq * 128];
+                                acc[4 * hq] += wgt[i * HM + 4 * hq] * v.x;
+                                acc[4 * hq + 1] += wgt[i * HM + 4 * hq + 1] * v.y;
+                                acc[4 * hq + 2] += wgt[i * HM + 4 * hq + 2] * v.z;
+                                acc[4 * hq + 3] += wgt[i * HM + 4 * hq + 3] * v.w;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < HM; ++j)
+                        if (j < p.h)
+                            obase[(int64_t)j * D + c * 128 + dl] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+                }
             } else {
                 // partial: unnormalised O^T, running max and sum (log2 domain) for the combine
                 const int slot = tok == tok_begin ? 0 : 1;
@@ -662,6 +774,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+    // no CTA of a merging cluster leaves while another may still signal its XCH barrier (every
+    // wait before this point is bounded, so every CTA gets here)
+    if constexpr (KC > 1) cluster_sync();
 }
 
 // Merge the partials of every token that a range boundary cut, add the sink once, write bf16.
@@ -744,6 +859,7 @@ __global__ void __launch_bounds__(128) sparse_attn_ot_combine_kernel(const Combi
 
 constexpr int kMaxDev = 64;
 int g_sms[kMaxDev];
+int g_clusters[kMaxDev][5];   // co-resident clusters of 2, 3 and 4 CTAs
 bool g_ready[kMaxDev];
 std::mutex g_mutex;
 
@@ -753,17 +869,45 @@ int max_ctas(int dev) {
     if (g_ready[dev]) return g_sms[dev];
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (cudaFuncSetAttribute(sparse_attn_ot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(sparse_attn_ot_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(sparse_attn_ot_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(sparse_attn_ot_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(sparse_attn_ot_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess)
         return 0;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sparse_attn_ot_kernel, NTHREADS, SMEM_BYTES) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sparse_attn_ot_kernel<1>, NTHREADS, SMEM_BYTES) !=
             cudaSuccess ||
         per_sm < 1)
         return 0;
     g_sms[dev] = sms * per_sm;
+    for (int kc = 2; kc <= 4; ++kc) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(kc * sms), 1, 1);
+        cfg.blockDim = dim3(NTHREADS, 1, 1);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)kc;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        auto k = kc == 2 ? sparse_attn_ot_kernel<2> : kc == 3 ? sparse_attn_ot_kernel<3> : sparse_attn_ot_kernel<4>;
+        g_clusters[dev][kc] = cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess ? n : 0;
+    }
     g_ready[dev] = true;
     return g_sms[dev];
+}
+
+int max_clusters(int dev, int kc) {
+    if (max_ctas(dev) <= 0) return 0;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    return g_clusters[dev][kc];
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -801,6 +945,7 @@ constexpr int kSegCost = 2 * BN;
 struct Plan {
     int64_t ntok, G, K;
     bool split;
+    int kc;           // > 1: the token's parts form a cluster and merge in the kernel
 };
 
 bool plan(int64_t ntok, int topk, Plan &pl) {
@@ -812,7 +957,16 @@ bool plan(int64_t ntok, int topk, Plan &pl) {
     pl.G = split::choose_ranges(ntok, topk, gmax, BN);
     pl.K = split::seg_cost(ntok, pl.G, kSegCost);
     pl.split = split::splits_units(ntok, topk, pl.G, pl.K);
+    // every token split into the same number of parts (2 to 4): those CTAs form a cluster, when
+    // all the clusters fit on the GPU at once
+    const int64_t k = pl.G > ntok && pl.G % ntok == 0 ? pl.G / ntok : 1;
+    pl.kc = pl.split && pl.K == 0 && k >= 2 && k <= 4 && ntok <= max_clusters(dev, (int)k) ? (int)k : 1;
     return true;
+}
+
+size_t workspace_bytes(const Plan &pl) {
+    if (!pl.split) return 0;
+    return (size_t)pl.G * (pl.kc > 1 ? 1 : 2) * SLOT * sizeof(float);
 }
 
 }  // namespace ot
@@ -824,14 +978,19 @@ bool sparse_attn_ot_supports(int h, int d, bool fp8, bool pair, bool rope) {
 bool sparse_attn_ot_preferred(int64_t ntok) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= ot::kMaxDev) return false;
-    const int gmax = ot::max_ctas(dev);
-    return gmax > 0 && ntok >= 1 && ntok < gmax;
+    return ot::max_ctas(dev) > 0 && ntok >= 1;
+}
+
+int sparse_attn_ot_launches(int64_t ntok, int topk) {
+    ot::Plan pl;
+    if (topk <= 0 || !ot::plan(ntok, topk, pl)) return 1;
+    return pl.split && pl.kc == 1 ? 2 : 1;
 }
 
 size_t sparse_attn_ot_workspace_bytes(int64_t ntok, int topk) {
     ot::Plan pl;
-    if (topk <= 0 || !ot::plan(ntok, topk, pl) || !pl.split) return 0;
-    return (size_t)pl.G * 2 * ot::SLOT * sizeof(float);
+    if (topk <= 0 || !ot::plan(ntok, topk, pl)) return 0;
+    return ot::workspace_bytes(pl);
 }
 
 int launch_sparse_attn_ot(const AttnArgs &a, cudaStream_t stream, bool stall_first_tile) {
@@ -839,10 +998,11 @@ int launch_sparse_attn_ot(const AttnArgs &a, cudaStream_t stream, bool stall_fir
     ot::Plan pl;
     if (!ot::plan(ntok, a.topk, pl)) return DS_ECUDA;
     if (a.topk > 0 && ntok > (INT64_MAX / (pl.G + 1)) / (a.topk + pl.K)) return DS_EUNSUPPORTED;
-    const size_t need = pl.split ? (size_t)pl.G * 2 * ot::SLOT * sizeof(float) : 0;
+    const size_t need = ot::workspace_bytes(pl);
     if (a.workspace_bytes < need || (need && !a.workspace)) return DS_EWORKSPACE;
+    const bool combine = pl.split && pl.kc == 1;
     ot::CombineParams cpar;
-    if (pl.split) {
+    if (combine) {
         cpar.sink = a.sink;
         cpar.ws = static_cast<const float *>(a.workspace);
         cpar.o = a.o;
@@ -877,15 +1037,23 @@ int launch_sparse_attn_ot(const AttnArgs &a, cudaStream_t stream, bool stall_fir
     cfg.dynamicSmemBytes = ot::SMEM_BYTES;
     cfg.stream = stream;
     // programmatic dependent launch: the set-up overlaps the previous kernel on the stream
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)pl.kc;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pl.kc > 1 ? 2 : 1;
     CUtensorMap qmap;
     if (!ot::make_q_map(&qmap, a.q, ntok * a.h, a.h)) return DS_ECUDA;
-    if (cudaLaunchKernelEx(&cfg, ot::sparse_attn_ot_kernel, qmap, p) != cudaSuccess) return DS_ECUDA;
-    if (pl.split) {
+    auto kernel = pl.kc == 2   ? ot::sparse_attn_ot_kernel<2>
+                  : pl.kc == 3 ? ot::sparse_attn_ot_kernel<3>
+                  : pl.kc == 4 ? ot::sparse_attn_ot_kernel<4>
+                               : ot::sparse_attn_ot_kernel<1>;
+    if (cudaLaunchKernelEx(&cfg, kernel, qmap, p) != cudaSuccess) return DS_ECUDA;
+    if (combine) {
         cudaLaunchConfig_t ccfg = {};
         ccfg.gridDim = dim3((unsigned)cpar.ncut, (unsigned)(ot::D / ot::kCombineCols), 1);
         ccfg.blockDim = dim3(128, 1, 1);

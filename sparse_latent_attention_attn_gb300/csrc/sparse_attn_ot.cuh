@@ -12,13 +12,19 @@ namespace dsattn {
 // The shapes the kernel is built for: head_dim 512, at most 64 heads, bf16 rows, plain output,
 // one query per work unit.
 bool sparse_attn_ot_supports(int h, int d, bool fp8, bool pair, bool rope);
-// Whether it is the faster choice for ntok work units (fewer tokens than SMs: decode batches).
+// Whether it is the choice for ntok work units: wherever it is built for the shape (measured
+// faster than the cluster kernel on decode batches and on a 4096-query prefill chunk).
 bool sparse_attn_ot_preferred(int64_t ntok);
+// Kernels a launch enqueues: 1, or 2 when a combine kernel merges tokens cut across CTAs.
+int sparse_attn_ot_launches(int64_t ntok, int topk);
 // Workspace for its partials (0 when no token is cut).
 size_t sparse_attn_ot_workspace_bytes(int64_t ntok, int topk);
 int launch_sparse_attn_ot(const AttnArgs &a, cudaStream_t stream, bool stall_first_tile);
 // Test switch (ds_test_set_kernel): 0 automatic, 1 always the cluster kernel, 2 this kernel
 // wherever it is built for the shape.
 void set_test_kernel(int which);
+// The kernels ds_sparse_attn runs for a bf16 call of this shape: returns how many it launches
+// and stores 1 (cluster kernel) or 2 (one-CTA kernel) to *which.
+int sparse_attn_plan(int b, int m, int h, int d, int topk, int *which);
 
 }  // namespace dsattn

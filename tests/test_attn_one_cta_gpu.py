@@ -1,13 +1,13 @@
 """The one-CTA sparse_attn kernel (head_dim 512, at most 64 heads, transposed accumulator) against
 the oracle, through the C ABI.
 
-ds_sparse_attn picks this kernel by itself for decode batches (fewer tokens than SMs); the test
-switch ds_test_set_kernel forces either kernel, so every case here runs on both and each result
-is held to the attention tolerance against the oracle ("Module attn", sparse_attn and the
+ds_sparse_attn picks this kernel by itself wherever it is built for the shape; the test switch
+ds_test_set_kernel forces either kernel, so every case here runs on both and each result is held
+to the attention tolerance against the oracle ("Module attn", sparse_attn and the
 Precision paragraph: |gpu - ref| <= 1e-2 + 1.6e-2 |ref|).  Cases cover whole and cut tokens
-(partials merged by the combine kernel), ragged last tiles, odd head counts, entries that are
+(parts merged inside a cluster of 2, 3 or 4 CTAs, or by the combine kernel), ragged last tiles, odd head counts, entries that are
 -1, duplicated or out of range, rows with no valid entry, many parts per token, more tokens than
-SMs (several segments per CTA, forced), and scores that grow along the index row so the running
+SMs (several segments per CTA), and scores that grow along the index row so the running
 max moves and the accumulator is rescaled.
 """
 import numpy as np
@@ -126,6 +126,22 @@ def test_invalid_duplicate_and_out_of_range_entries(ds, kernel):
     assert ds.device_status() == 0
 
 
+def test_plan_query_names_the_kernel(ds):
+    """ds_sparse_attn_launches reports the kernel ds_sparse_attn picks and how many kernels it
+    enqueues (the combine kernel only where tokens are cut and not merged inside a cluster)."""
+    assert ds.sparse_attn_launches(32, 1, 64, 512, 640) == (1, ds.KERNEL_ONE_CTA)   # 4-CTA clusters merge
+    assert ds.sparse_attn_launches(64, 1, 64, 512, 128) == (1, ds.KERNEL_ONE_CTA)   # whole tokens
+    assert ds.sparse_attn_launches(4, 1, 64, 512, 700) == (2, ds.KERNEL_ONE_CTA)    # 5 parts: the combine
+    assert ds.sparse_attn_launches(256, 1, 128, 512, 2176)[1] == ds.KERNEL_CLUSTER  # 128 heads
+    assert ds.sparse_attn_launches(4, 1, 8, 64, 700)[1] == ds.KERNEL_CLUSTER        # head_dim 64
+    assert ds.sparse_attn_launches(4, 1, 64, 512, 0) == (1, ds.KERNEL_ONE_CTA)      # the zero fill
+    try:
+        ds.test_set_kernel(ds.KERNEL_CLUSTER)
+        assert ds.sparse_attn_launches(32, 1, 64, 512, 640)[1] == ds.KERNEL_CLUSTER
+    finally:
+        ds.test_set_kernel(ds.KERNEL_AUTO)
+
+
 def test_both_kernels_agree_and_repeat_exactly(ds):
     """On decode_comp's shape the two kernels give results within the attention tolerance of each
     other, and each repeats bit for bit."""
@@ -145,11 +161,13 @@ def test_both_kernels_agree_and_repeat_exactly(ds):
     assert ds.device_status() == 0
 
 
-def test_timed_out_wait_is_reported(ds):
+@pytest.mark.parametrize("b,topk", [(4, 700), (32, 640)])
+def test_timed_out_wait_is_reported(ds, b, topk):
     """The one-CTA kernel's bounded waits, made to run out with the stall hook (the gather warps
     withhold the first tile's arrivals): the call ends, raises DS_DEV_TIMEOUT, and the next call
-    is clean and correct."""
-    q, kv, sink, idx = _case(95, 4, 1, 64, 2048, 700)
+    is clean and correct.  With 32 tokens of 640 entries the CTAs of a token form a cluster that
+    merges in the kernel; with 4 tokens of 700 a combine kernel merges the parts."""
+    q, kv, sink, idx = _case(95, b, 1, 64, 2048, topk)
     scale = 512 ** -0.5
     assert ds.device_status() == 0
     ds.test_set_kernel(KERNELS["one_cta"])
