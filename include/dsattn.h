@@ -370,8 +370,8 @@ int ds_sparse_attn_launches(int b, int m, int h, int d, int topk, int *kernel);
  * ds_test_set_kernel -- test hook for the choice of attention kernel (no counterpart on the
  * pages).  ds_sparse_attn runs one of two kernels with the same operation and tolerance: the
  * 2-CTA cluster kernel (any supported shape) or, for d = 512 and h <= 64, the one-CTA kernel
- * with a transposed accumulator (ds_sparse_attn_rope and ds_sparse_attn_fp8kv always run the
- * cluster kernel).  which = 0: that automatic choice (default); 1: always the cluster kernel;
+ * with a transposed accumulator (ds_sparse_attn_rope likewise; ds_sparse_attn_fp8kv always runs
+ * the cluster kernel).  which = 0: that automatic choice (default); 1: always the cluster kernel;
  * 2: the one-CTA kernel wherever it is built for the shape (the same as 0 today).
  * Process-wide; nothing in the library sets it.  The workspace of
  * ds_sparse_attn_workspace_bytes suffices for either choice.

@@ -5,7 +5,8 @@
 // Precision paragraph; "DeepSeek V4.1", attention/attend, sparse_attn_kernel): for every query
 // token and head, softmax over the index-listed rows of the shared latent KV tensor plus an
 // attention sink that counts in the denominator only, the rows reused as values, f32 arithmetic,
-// bf16 output.
+// bf16 output; optionally with the inverse RoPE of the output fused in ("DeepSeek V4.1",
+// attention/query-latent, Attention.forward).
 //
 // Why a second kernel: with head_dim 512 an accumulator O[heads x 512] in the usual orientation
 // (heads as TMEM lanes) takes all 512 TMEM columns even when only 64 of the 128 lanes hold heads,
@@ -137,6 +138,10 @@ struct Params {
     float scale_log2; // softmax scale * log2(e)
     unsigned int *status;
     int stall_first_tile;   // test switch (ds_test_set_stall): withhold the first tile's arrivals
+    // fused inverse RoPE of the output (ROPE kernels), see AttnArgs
+    const float2 *rope;
+    int rd;
+    int64_t rope_pos0;
 };
 
 // Instruction descriptor of kind::f16: bf16 A and B, f32 accumulator, dense; A and B each
@@ -185,6 +190,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// The bf16 value of output column d (this lane) of one head: with ROPE, the last rd columns are
+// rotated back as ds_apply_rotary would rotate the stored bf16 pairs.  Lanes d and d ^ 1 hold a
+// pair (2j, 2j + 1); each packs the pair from its own value and its neighbour's (one shuffle, so
+// every lane of the warp calls this when `warp_rotates`), rotates it and keeps its own half.
+// cs_row: the token's table row (rd / 2 (cos, sin) pairs).
+template <bool ROPE>
+__device__ __forceinline__ uint16_t out_bf16(float x, int d, const float2 *cs_row, int rd, bool warp_rotates) {
+    if constexpr (ROPE) {
+        if (warp_rotates) {
+            const float y = __shfl_xor_sync(0xffffffffu, x, 1);
+            if (d >= D - rd) {
+                const bool odd = (d & 1) != 0;
+                const uint32_t v = odd ? pack_bf16x2(y, x) : pack_bf16x2(x, y);
+                const uint32_t r = rope_rotate_bf16x2(v, __ldg(cs_row + (((d & ~1) - (D - rd)) >> 1)), true);
+                return odd ? (uint16_t)(r >> 16) : (uint16_t)(r & 0xffffu);
+            }
+        }
+    }
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
     const bool ok = mbar_wait(bar, parity, abort, kWaitLimitNs);
     return __all_sync(0xffffffffu, ok);
@@ -228,7 +254,8 @@ struct TileIter {
 // index row; they merge their accumulators among themselves (no combine kernel): each CTA writes
 // the 128-column chunks of O^T that other CTAs own (chunk c belongs to rank c % KC) with its
 // running max and sum, tells the others through their XCH barriers, and finishes its own chunks.
-template <int KC>
+// ROPE: the output's last rd columns are rotated back in the epilogue (ds_sparse_attn_rope).
+template <int KC, bool ROPE>
 __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __grid_constant__ CUtensorMap qmap,
                                                                      const Params p) {
     static_assert(KC >= 1 && KC <= 4, "cluster merge of 2 to 4 parts");
@@ -627,12 +654,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                 // staging the chunk in shared memory, with or without pairing neighbour lanes, and
                 // than TMA stores of the staged chunk.)
                 uint16_t *obase = p.o + utok * p.h * (int64_t)D;
+                const float2 *cs_row = nullptr;
+                if constexpr (ROPE) cs_row = p.rope + (p.rope_pos0 + utok % p.m) * (p.rd / 2);
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t r[2][32];
                     tmem_ld32(tmem + lane_off + O_COL + c * HM, r[0]);
                     tmem_ld32(tmem + lane_off + O_COL + c * HM + 32, r[1]);
                     tmem_ld_wait(r);
+                    const bool rot = ROPE && c * 128 + 32 * warp + 31 >= D - p.rd;
 #pragma unroll
                     for (int j = 0; j < HM; j += 4) {
                         const float4 iv = *reinterpret_cast<const float4 *>(inv_h + j);
@@ -641,10 +671,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                                              __uint_as_float(r[j >> 5][(j + 2) & 31]) * iv.z,
                                              __uint_as_float(r[j >> 5][(j + 3) & 31]) * iv.w};
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            if (j + k < p.h)
-                                obase[(int64_t)(j + k) * D + c * 128 + dl] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(xv[k]));
+                        for (int k = 0; k < 4; ++k) {
+                            const uint16_t v = out_bf16<ROPE>(xv[k], c * 128 + dl, cs_row, p.rd, rot);
+                            if (j + k < p.h) obase[(int64_t)(j + k) * D + c * 128 + dl] = v;
+                        }
                     }
                 }
             } else if constexpr (KC > 1) {
@@ -709,8 +739,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                     break;
                 }
                 uint16_t *obase = p.o + utok * p.h * (int64_t)D;
+                const float2 *cs_row = nullptr;
+                if constexpr (ROPE) cs_row = p.rope + (p.rope_pos0 + utok % p.m) * (p.rd / 2);
 #pragma unroll 1
                 for (int c = rank; c < 4; c += KC) {
+                    const bool rot = ROPE && c * 128 + 32 * warp + 31 >= D - p.rd;
                     uint32_t r[2][32];
                     tmem_ld32(tmem + lane_off + O_COL + c * HM, r[0]);
                     tmem_ld32(tmem + lane_off + O_COL + c * HM + 32, r[1]);
@@ -734,9 +767,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                         }
                     }
 #pragma unroll
-                    for (int j = 0; j < HM; ++j)
-                        if (j < p.h)
-                            obase[(int64_t)j * D + c * 128 + dl] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+                    for (int j = 0; j < HM; ++j) {
+                        const uint16_t v = out_bf16<ROPE>(acc[j], c * 128 + dl, cs_row, p.rd, rot);
+                        if (j < p.h) obase[(int64_t)j * D + c * 128 + dl] = v;
+                    }
                 }
             } else {
                 // partial: unnormalised O^T, running max and sum (log2 domain) for the combine
@@ -789,6 +823,10 @@ struct CombineParams {
     const float *sink;
     const float *ws;
     uint16_t *o;
+    const float2 *rope;           // fused inverse RoPE (ROPE combine), see AttnArgs
+    int64_t rope_pos0;
+    int rd;
+    int m;
     int h;
     int interleave;
     int64_t nunits;
@@ -796,6 +834,7 @@ struct CombineParams {
     int4 cut[kMaxCut];            // {unit, first part, parts, slot bits}
 };
 
+template <bool ROPE>
 __global__ void __launch_bounds__(128) sparse_attn_ot_combine_kernel(const CombineParams cp) {
     grid_dependency_wait();   // launched as a programmatic dependent of the attention kernel
     __shared__ float wgt[32][HM];
@@ -846,10 +885,14 @@ __global__ void __launch_bounds__(128) sparse_attn_ot_combine_kernel(const Combi
         }
     }
     uint16_t *dst = cp.o + utok * cp.h * (int64_t)D + d;
+    const float2 *cs_row = nullptr;
+    if constexpr (ROPE) cs_row = cp.rope + (cp.rope_pos0 + utok % cp.m) * (cp.rd / 2);
+    const bool rot = ROPE && (int)blockIdx.y * kCombineCols + kCombineCols - 1 >= D - cp.rd;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int hh = 16 * g + j;
-        if (hh < cp.h) dst[(int64_t)hh * D] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+        const uint16_t v = out_bf16<ROPE>(acc[j], d, cs_row, cp.rd, rot);
+        if (hh < cp.h) dst[(int64_t)hh * D] = v;
     }
 }
 
@@ -869,17 +912,14 @@ int max_ctas(int dev) {
     if (g_ready[dev]) return g_sms[dev];
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (cudaFuncSetAttribute(sparse_attn_ot_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(sparse_attn_ot_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(sparse_attn_ot_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(sparse_attn_ot_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess)
-        return 0;
+    const void *kernels[8] = {(const void *)sparse_attn_ot_kernel<1, false>, (const void *)sparse_attn_ot_kernel<2, false>,
+                              (const void *)sparse_attn_ot_kernel<3, false>, (const void *)sparse_attn_ot_kernel<4, false>,
+                              (const void *)sparse_attn_ot_kernel<1, true>,  (const void *)sparse_attn_ot_kernel<2, true>,
+                              (const void *)sparse_attn_ot_kernel<3, true>,  (const void *)sparse_attn_ot_kernel<4, true>};
+    for (const void *k : kernels)
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) return 0;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sparse_attn_ot_kernel<1>, NTHREADS, SMEM_BYTES) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sparse_attn_ot_kernel<1, false>, NTHREADS, SMEM_BYTES) !=
             cudaSuccess ||
         per_sm < 1)
         return 0;
@@ -897,7 +937,9 @@ int max_ctas(int dev) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        auto k = kc == 2 ? sparse_attn_ot_kernel<2> : kc == 3 ? sparse_attn_ot_kernel<3> : sparse_attn_ot_kernel<4>;
+        auto k = kc == 2   ? sparse_attn_ot_kernel<2, false>
+                 : kc == 3 ? sparse_attn_ot_kernel<3, false>
+                           : sparse_attn_ot_kernel<4, false>;
         g_clusters[dev][kc] = cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess ? n : 0;
     }
     g_ready[dev] = true;
@@ -971,8 +1013,8 @@ size_t workspace_bytes(const Plan &pl) {
 
 }  // namespace ot
 
-bool sparse_attn_ot_supports(int h, int d, bool fp8, bool pair, bool rope) {
-    return d == ot::D && h >= 1 && h <= ot::HM && !fp8 && !pair && !rope;
+bool sparse_attn_ot_supports(int h, int d, bool fp8, bool pair) {
+    return d == ot::D && h >= 1 && h <= ot::HM && !fp8 && !pair;
 }
 
 bool sparse_attn_ot_preferred(int64_t ntok) {
@@ -1006,6 +1048,10 @@ int launch_sparse_attn_ot(const AttnArgs &a, cudaStream_t stream, bool stall_fir
         cpar.sink = a.sink;
         cpar.ws = static_cast<const float *>(a.workspace);
         cpar.o = a.o;
+        cpar.rope = reinterpret_cast<const float2 *>(a.rope);
+        cpar.rope_pos0 = a.rope_pos0;
+        cpar.rd = a.rd;
+        cpar.m = a.m;
         cpar.h = a.h;
         cpar.interleave = a.m > 1 ? 1 : 0;
         cpar.nunits = ntok;
@@ -1030,6 +1076,9 @@ int launch_sparse_attn_ot(const AttnArgs &a, cudaStream_t stream, bool stall_fir
     p.scale_log2 = a.scale * ot::kLog2e;
     p.status = a.status;
     p.stall_first_tile = stall_first_tile ? 1 : 0;
+    p.rope = reinterpret_cast<const float2 *>(a.rope);
+    p.rd = a.rd;
+    p.rope_pos0 = a.rope_pos0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.G, 1, 1);
@@ -1048,10 +1097,11 @@ int launch_sparse_attn_ot(const AttnArgs &a, cudaStream_t stream, bool stall_fir
     cfg.numAttrs = pl.kc > 1 ? 2 : 1;
     CUtensorMap qmap;
     if (!ot::make_q_map(&qmap, a.q, ntok * a.h, a.h)) return DS_ECUDA;
-    auto kernel = pl.kc == 2   ? ot::sparse_attn_ot_kernel<2>
-                  : pl.kc == 3 ? ot::sparse_attn_ot_kernel<3>
-                  : pl.kc == 4 ? ot::sparse_attn_ot_kernel<4>
-                               : ot::sparse_attn_ot_kernel<1>;
+    const bool rope = a.rope != nullptr;
+    auto kernel = pl.kc == 2   ? (rope ? ot::sparse_attn_ot_kernel<2, true> : ot::sparse_attn_ot_kernel<2, false>)
+                  : pl.kc == 3 ? (rope ? ot::sparse_attn_ot_kernel<3, true> : ot::sparse_attn_ot_kernel<3, false>)
+                  : pl.kc == 4 ? (rope ? ot::sparse_attn_ot_kernel<4, true> : ot::sparse_attn_ot_kernel<4, false>)
+                               : (rope ? ot::sparse_attn_ot_kernel<1, true> : ot::sparse_attn_ot_kernel<1, false>);
     if (cudaLaunchKernelEx(&cfg, kernel, qmap, p) != cudaSuccess) return DS_ECUDA;
     if (combine) {
         cudaLaunchConfig_t ccfg = {};
@@ -1060,7 +1110,8 @@ int launch_sparse_attn_ot(const AttnArgs &a, cudaStream_t stream, bool stall_fir
         ccfg.stream = stream;
         ccfg.attrs = attr;
         ccfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&ccfg, ot::sparse_attn_ot_combine_kernel, cpar) != cudaSuccess) return DS_ECUDA;
+        auto comb = rope ? ot::sparse_attn_ot_combine_kernel<true> : ot::sparse_attn_ot_combine_kernel<false>;
+        if (cudaLaunchKernelEx(&ccfg, comb, cpar) != cudaSuccess) return DS_ECUDA;
     }
     return DS_OK;
 }

@@ -9,9 +9,9 @@
 
 namespace dsattn {
 
-// The shapes the kernel is built for: head_dim 512, at most 64 heads, bf16 rows, plain output,
-// one query per work unit.
-bool sparse_attn_ot_supports(int h, int d, bool fp8, bool pair, bool rope);
+// The shapes the kernel is built for: head_dim 512, at most 64 heads, bf16 rows, one query per
+// work unit (with or without the fused inverse RoPE of the output).
+bool sparse_attn_ot_supports(int h, int d, bool fp8, bool pair);
 // Whether it is the choice for ntok work units: wherever it is built for the shape (measured
 // faster than the cluster kernel on decode batches and on a 4096-query prefill chunk).
 bool sparse_attn_ot_preferred(int64_t ntok);

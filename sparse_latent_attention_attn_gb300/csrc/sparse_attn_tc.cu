@@ -1424,8 +1424,8 @@ size_t sparse_attn_tc_workspace_bytes(int b, int m, int h, int d, int topk, bool
         default: return 0;
     }
     // the one-CTA kernel serves some of the same calls (the query does not know which: it also
-    // answers for the fp8 row store and the fused rotation), so the larger need is returned
-    if (sparse_attn_ot_supports(h, d, false, pair, false)) {
+    // answers for the fp8 row store), so the larger need is returned
+    if (sparse_attn_ot_supports(h, d, false, pair)) {
         const size_t ot = sparse_attn_ot_workspace_bytes(ntok, topk);
         if (ot > need) need = ot;
     }
@@ -1448,7 +1448,7 @@ int tc_launches(int64_t ntok, int topk) {
 int sparse_attn_plan(int b, int m, int h, int d, int topk, int *which) {
     const int64_t ntok = (int64_t)b * m;
     const int force = tc::g_test_kernel.load(std::memory_order_relaxed);
-    const bool ot = force != 1 && sparse_attn_ot_supports(h, d, false, false, false) && ntok * h <= INT32_MAX &&
+    const bool ot = force != 1 && sparse_attn_ot_supports(h, d, false, false) && ntok * h <= INT32_MAX &&
                     (force == 2 || sparse_attn_ot_preferred(ntok));
     if (which) *which = ot ? 2 : 1;
     if (ntok == 0 || topk == 0) return ntok == 0 ? 0 : 1;
@@ -1466,7 +1466,7 @@ void set_test_kernel(int which) { tc::g_test_kernel.store(which, std::memory_ord
 int launch_sparse_attn_tc(const AttnArgs &a, cudaStream_t stream) {
     const int force = tc::g_test_kernel.load(std::memory_order_relaxed);
     const int64_t ntok = (int64_t)a.b * a.m;
-    if (force != 1 && sparse_attn_ot_supports(a.h, a.d, a.kv8 != nullptr, a.pair, a.rope != nullptr) &&
+    if (force != 1 && sparse_attn_ot_supports(a.h, a.d, a.kv8 != nullptr, a.pair) &&
         ntok * a.h <= INT32_MAX && (force == 2 || sparse_attn_ot_preferred(ntok)))
         return launch_sparse_attn_ot(a, stream, tc::g_test_stall.load(std::memory_order_relaxed) != 0);
     if (a.kv8) return a.d == 512 ? tc::launch<512, true>(a, stream) : DS_EUNSUPPORTED;

@@ -614,23 +614,28 @@ def test_kv_rope_ring_write_bit_exact(ds, b, s, d, W, p0, rd):
     assert np.array_equal(bits(ring), ring_o)
 
 
+@pytest.mark.parametrize("kernel", ["cluster", "one_cta"])
 @pytest.mark.parametrize("d,h,b,m,topk,rd,p0", [(512, 64, 100, 2, 300, 64, 4000),    # cut tokens: the combine
                                                  (512, 128, 3, 1, 2176, 64, 131072),  # whole tokens, decode
                                                  (512, 16, 1, 5, 200, 512, 0),        # every column rotated
+                                                 (512, 64, 32, 1, 640, 64, 16384),    # 4-CTA clusters merge
+                                                 (512, 40, 6, 1, 300, 24, 77),        # 2 parts; rd not a multiple of 32
                                                  (64, 4, 1, 12, 8, 16, 0),            # the ratio-0 fixture's shape
                                                  (256, 32, 60, 3, 129, 32, 77)])
-def test_sparse_attn_rope_equals_attention_then_inverse_rotation(ds, d, h, b, m, topk, rd, p0):
-    """The inverse RoPE of the output fused into the attention epilogue and the combine
-    ("DeepSeek V4.1", attention/query-latent, Attention.forward rotates o back by its position):
-    bit-identical to ds_sparse_attn followed by ds_apply_rotary(inverse) on the same (cluster)
-    kernel, which the fused rotation always runs, and to the oracle's rotation of that attention
-    output; the attention itself matches the oracle within the tolerance."""
+def test_sparse_attn_rope_equals_attention_then_inverse_rotation(ds, kernel, d, h, b, m, topk, rd, p0):
+    """The inverse RoPE of the output fused into the attention epilogue, the in-cluster merge and
+    the combine ("DeepSeek V4.1", attention/query-latent, Attention.forward rotates o back by its
+    position): bit-identical to ds_sparse_attn followed by ds_apply_rotary(inverse) on the same
+    kernel (each kernel where it is built for the shape), and to the oracle's rotation of that
+    attention output; the attention itself matches the oracle within the tolerance."""
+    if kernel == "one_cta" and (d != 512 or h > 64):
+        pytest.skip("the one-CTA kernel is built for head_dim 512 and at most 64 heads")
     q, kv, sink, idx = _case(700 + d + m, b, m, h, d, 2 * topk, topk, 0.05)
     table = oracle.rope_table(p0 + m, rd, 10000.0)
     tg = torch.from_numpy(table).cuda()
     qg, kvg, sg, ig = q.cuda(), kv.cuda(), sink.cuda(), idx.cuda()
-    fused = ds.sparse_attn_rope(qg, kvg, sg, ig, d ** -0.5, rd, tg, p0)
-    with _kernel(ds, ds.KERNEL_CLUSTER):
+    with _kernel(ds, ds.KERNEL_CLUSTER if kernel == "cluster" else ds.KERNEL_ONE_CTA):
+        fused = ds.sparse_attn_rope(qg, kvg, sg, ig, d ** -0.5, rd, tg, p0)
         plain = ds.sparse_attn(qg, kvg, sg, ig, d ** -0.5)
     ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), idx.numpy(), d ** -0.5)
     assert_close_bf16(bits(plain), ref)
