@@ -641,11 +641,14 @@ def run_ours(args):
             roof = {"bound": "tensor", "achieved": flops / attn_s / 1e12, "peak": peaks["bf16_tflops"],
                     "unit": "TFLOP/s"}
         roof["frac"] = roof["achieved"] / roof["peak"]
-        roof["traffic"] = profiled_traffic(w.name, 1)
+        # the capture matching this run: the prefill pairs and the fp8 row store have their own
+        profile_name = w.name + ("_pairs" if args.prefill_pairs else "") + ("_fp8" if args.kv == "fp8" else "")
+        roof["traffic"] = profiled_traffic(profile_name, 1)
         roof["peak_source"] = peaks["source"]
-        roof["kernel"] = ("sparse_attn_ot_kernel (one CTA per work range, transposed accumulator)"
+        roof["kernel"] = ("sparse_attn_ot_kernel (one CTA per work range, transposed accumulator; tokens cut "
+                          "across CTAs merge inside a cluster or in a combine kernel)"
                           if sets[0].attn_kernel == dsattn.KERNEL_ONE_CTA else
-                          "sparse_attn_tc_kernel (2-CTA cluster, d split)") + " + combine when tokens are cut"
+                          "sparse_attn_tc_kernel (2-CTA cluster, d split) + combine when tokens are cut")
         roof["kernel_source_sha256_16"] = kernel_source_hash()
         roof["kernel_ms"] = attn_s * 1e3
         roof["roofline_ms"] = max(t_hbm, t_tc) * 1e3
