@@ -130,7 +130,9 @@ size_t ds_sparse_attn_workspace_bytes(int b, int m, int h, int d, int topk);
  * o          device bf16 [b][m][h][d], written
  * workspace  device scratch of at least ds_sparse_attn_workspace_bytes(b, m, h, d, topk) bytes,
  *            256-byte aligned (may be NULL when that size is 0); contents need no initialisation
- *            and are not meaningful after the call.
+ *            and are not meaningful after the call.  That size covers either attention kernel;
+ *            the call checks the need of the kernel it runs (DS_EWORKSPACE when it is larger
+ *            than workspace_bytes, before anything is enqueued).
  * Supported: d in {64, 128, 256, 512}; 1 <= h <= 128; topk >= 0; pointers 16-byte aligned.
  * Errors: DS_EINVAL, DS_EUNSUPPORTED, DS_EWORKSPACE, DS_ECUDA.
  */
@@ -281,7 +283,7 @@ int ds_sparse_attn_fp8kv(const uint16_t *q, const uint8_t *kv_codes, const int8_
  * until the process exits.  Nothing is allocated by the call.
  *
  * Arguments, layouts, results and errors are those of ds_sparse_attn, except that a shape whose
- * scratch need (ds_sparse_attn_workspace_bytes) exceeds the capacity is refused with
+ * scratch need (that of the attention kernel the call runs) exceeds the capacity is refused with
  * DS_EWORKSPACE before anything is launched.
  * The first call on each device looks up that device's copy of the array (cudaGetSymbolAddress)
  * and so should happen before any stream capture on that device.  Every call on a device shares
@@ -360,11 +362,13 @@ void ds_test_set_stall(int on);
 /*
  * ds_sparse_attn_launches -- the kernels a ds_sparse_attn call of this shape enqueues on the
  * current device (no counterpart on the pages; for accounting and tests).  Returns how many (0 for
- * an empty batch; 1 for topk = 0, the zero fill), and stores to *kernel (may be NULL) which
- * attention kernel runs: 1 the 2-CTA cluster kernel, 2 the one-CTA kernel (see
- * ds_test_set_kernel).  Pure host function.  Returns DS_EINVAL for a shape ds_sparse_attn rejects.
+ * an empty batch; 1 for topk = 0, the zero fill); stores to *kernel which attention kernel runs
+ * (1 the 2-CTA cluster kernel, 2 the one-CTA kernel; see ds_test_set_kernel) and to
+ * *workspace_bytes the workspace that kernel needs (at most ds_sparse_attn_workspace_bytes).
+ * Either pointer may be NULL.  Pure host function.  Returns DS_EINVAL for a shape ds_sparse_attn
+ * rejects.
  */
-int ds_sparse_attn_launches(int b, int m, int h, int d, int topk, int *kernel);
+int ds_sparse_attn_launches(int b, int m, int h, int d, int topk, int *kernel, size_t *workspace_bytes);
 
 /*
  * ds_test_set_kernel -- test hook for the choice of attention kernel (no counterpart on the

@@ -52,8 +52,9 @@ int sparse_attn_bf16(const uint16_t *q, const uint16_t *kv, int64_t n, const flo
     if ((int64_t)b * m == 0) return DS_OK;
     if (!q || !o || !sink || (topk > 0 && (!idx || !kv))) return DS_EINVAL;
     if (!aligned16(q) || !aligned16(o) || (kv && !aligned16(kv))) return DS_EINVAL;
-    const size_t need = ds_sparse_attn_workspace_bytes(b, m, h, d, topk);
-    if (workspace_bytes < need || (need > 0 && !workspace)) return DS_EWORKSPACE;
+    // The workspace is checked against the need of the kernel that will run (each launch checks
+    // it before enqueueing anything); ds_sparse_attn_workspace_bytes, the larger need of the two
+    // attention kernels, always suffices.
     AttnArgs a{q, kv, nullptr, nullptr, n, sink, idx, topk, scale, o, b, m, h, d, workspace, workspace_bytes,
                status_word(), rope, rd, rope_pos0};
     if (!a.status) return DS_ECUDA;
@@ -306,9 +307,9 @@ int ds_indexer_topk(const uint16_t *q, const uint16_t *k, const float *w, int b,
 
 void ds_test_set_stall(int on) { set_test_stall(on != 0); }
 
-int ds_sparse_attn_launches(int b, int m, int h, int d, int topk, int *kernel) {
+int ds_sparse_attn_launches(int b, int m, int h, int d, int topk, int *kernel, size_t *workspace_bytes) {
     if (b < 0 || m < 0 || h < 1 || h > 128 || topk < 0 || !supported_head_dim(d)) return DS_EINVAL;
-    return sparse_attn_plan(b, m, h, d, topk, kernel);
+    return sparse_attn_plan(b, m, h, d, topk, kernel, workspace_bytes);
 }
 
 int ds_test_set_kernel(int which) {

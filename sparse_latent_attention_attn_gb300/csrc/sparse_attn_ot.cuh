@@ -23,8 +23,9 @@ int launch_sparse_attn_ot(const AttnArgs &a, cudaStream_t stream, bool stall_fir
 // Test switch (ds_test_set_kernel): 0 automatic, 1 always the cluster kernel, 2 this kernel
 // wherever it is built for the shape.
 void set_test_kernel(int which);
-// The kernels ds_sparse_attn runs for a bf16 call of this shape: returns how many it launches
-// and stores 1 (cluster kernel) or 2 (one-CTA kernel) to *which.
-int sparse_attn_plan(int b, int m, int h, int d, int topk, int *which);
+// The kernels ds_sparse_attn runs for a bf16 call of this shape: returns how many it launches,
+// stores 1 (cluster kernel) or 2 (one-CTA kernel) to *which and the workspace that kernel needs to
+// *workspace (either pointer may be null).
+int sparse_attn_plan(int b, int m, int h, int d, int topk, int *which, size_t *workspace);
 
 }  // namespace dsattn

@@ -1436,28 +1436,33 @@ void set_test_stall(bool on) { tc::g_test_stall.store(on ? 1 : 0, std::memory_or
 
 namespace {
 template <int D>
-int tc_launches(int64_t ntok, int topk) {
+int tc_launches(int64_t ntok, int topk, size_t *workspace) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= tc::kMaxDev) return 1;
     const int gmax = tc::max_clusters<D>(dev);
     if (gmax <= 0) return 1;
+    if (workspace) *workspace = tc::variant_workspace_bytes<D, false>(dev, ntok, topk);
     return tc::splits_tokens(ntok, topk, tc::choose_clusters(ntok, topk, gmax)) ? 2 : 1;
 }
 }  // namespace
 
-int sparse_attn_plan(int b, int m, int h, int d, int topk, int *which) {
+int sparse_attn_plan(int b, int m, int h, int d, int topk, int *which, size_t *workspace) {
     const int64_t ntok = (int64_t)b * m;
     const int force = tc::g_test_kernel.load(std::memory_order_relaxed);
     const bool ot = force != 1 && sparse_attn_ot_supports(h, d, false, false) && ntok * h <= INT32_MAX &&
                     (force == 2 || sparse_attn_ot_preferred(ntok));
     if (which) *which = ot ? 2 : 1;
+    if (workspace) *workspace = 0;
     if (ntok == 0 || topk == 0) return ntok == 0 ? 0 : 1;
-    if (ot) return sparse_attn_ot_launches(ntok, topk);
+    if (ot) {
+        if (workspace) *workspace = sparse_attn_ot_workspace_bytes(ntok, topk);
+        return sparse_attn_ot_launches(ntok, topk);
+    }
     switch (d) {
-        case 64: return tc_launches<64>(ntok, topk);
-        case 128: return tc_launches<128>(ntok, topk);
-        case 256: return tc_launches<256>(ntok, topk);
-        case 512: return tc_launches<512>(ntok, topk);
+        case 64: return tc_launches<64>(ntok, topk, workspace);
+        case 128: return tc_launches<128>(ntok, topk, workspace);
+        case 256: return tc_launches<256>(ntok, topk, workspace);
+        case 512: return tc_launches<512>(ntok, topk, workspace);
         default: return 0;
     }
 }

@@ -77,7 +77,8 @@ _lib.ds_test_set_stall.argtypes = [_i32]
 _lib.ds_test_set_stall.restype = None
 _lib.ds_test_set_kernel.argtypes = [_i32]
 _lib.ds_test_set_kernel.restype = _i32
-_lib.ds_sparse_attn_launches.argtypes = [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]
+_lib.ds_sparse_attn_launches.argtypes = [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32),
+                                         ctypes.POINTER(ctypes.c_size_t)]
 _lib.ds_sparse_attn_launches.restype = _i32
 _lib.ds_status_string.argtypes = [_i32]
 _lib.ds_status_string.restype = ctypes.c_char_p
@@ -470,11 +471,19 @@ KERNEL_AUTO, KERNEL_CLUSTER, KERNEL_ONE_CTA = 0, 1, 2
 def sparse_attn_launches(b: int, m: int, h: int, d: int, topk: int) -> tuple[int, int]:
     """(kernels a sparse_attn call of this shape launches, the attention kernel it runs:
     KERNEL_CLUSTER or KERNEL_ONE_CTA)."""
+    n, which, _ = sparse_attn_plan(b, m, h, d, topk)
+    return n, which
+
+
+def sparse_attn_plan(b: int, m: int, h: int, d: int, topk: int) -> tuple[int, int, int]:
+    """(kernels launched, attention kernel, workspace bytes that kernel needs) for a sparse_attn
+    call of this shape."""
     which = ctypes.c_int(0)
-    n = _lib.ds_sparse_attn_launches(b, m, h, d, topk, ctypes.byref(which))
+    ws = ctypes.c_size_t(0)
+    n = _lib.ds_sparse_attn_launches(b, m, h, d, topk, ctypes.byref(which), ctypes.byref(ws))
     if n < 0:
         raise DsError("ds_sparse_attn_launches", n)
-    return n, which.value
+    return n, which.value, ws.value
 
 
 def test_set_kernel(which: int) -> None:

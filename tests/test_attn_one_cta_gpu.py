@@ -76,6 +76,7 @@ CASES = [
     (8, 1, 1, 64, 12000, 8192, 0.02),    # one token over 32 CTAs
     (9, 64, 1, 64, 128, 128, 0.0),       # decode_window's shape: whole tokens, no combine
     (10, 2, 1, 8, 200, 70, 0.0),         # 8 heads, a 6-entry last tile
+    (11, 8, 2, 40, 900, 300, 0.05),      # two queries per sequence, 40 heads, 2-CTA merges
 ]
 
 
