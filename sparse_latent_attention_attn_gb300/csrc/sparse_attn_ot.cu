@@ -20,9 +20,10 @@
 //    memory (K-major).
 //  * O^T += V^T P^T: M = 128 columns of d (one chunk), N = 64 heads, K = 64 entries; V^T is the
 //    same row tile read MN-major (d contiguous), P^T is P written K-major by the softmax.
-//  * The softmax runs one thread per head on the score layout; a rescale of the running max
-//    (lazy, as in sparse_attn_tc.cu) multiplies the head's column of O^T, which every softmax
-//    thread does for its lane (d) of the accumulator, after a vote among the four softmax warps.
+//  * The softmax runs two threads per head (the score layout's lane and, with half the columns
+//    handed over by shuffles, the idle lane 16 above it); a rescale of the running max (lazy, as
+//    in sparse_attn_tc.cu) multiplies the head's column of O^T, which every softmax thread does
+//    for its lane (d) of the accumulator, after a vote among the four softmax warps.
 //  * Tiles are 64 consecutive index entries, not compacted: -1 and out-of-range entries are
 //    masked in the softmax (their rows are neither loaded nor counted).
 //  * Work ranges, the cost line and the cut tokens are those of attn_split.cuh; a cut token's
@@ -471,11 +472,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
     } else if (warp < 4) {
         // ============================ softmax + epilogue (warps 0-3) ============================
         setmaxnreg_inc<REG_SOFTMAX>();
-        // Score layout of the 64-row MMA: head 16 w + i (i < 16) on lane 32 w + i.  Lanes 16-31 of
-        // each warp hold no head; they take part in the warp-wide TMEM loads and in the O^T work,
-        // where every thread is one column d = 128 c + 32 w + lane of each chunk c.
-        const int hl = lane < 16 ? 16 * warp + lane : -1;
-        const bool live = hl >= 0 && hl < p.h;
+        // Score layout of the 64-row MMA: head 16 w + i (i < 16) on lane 32 w + i; lanes 16-31 of
+        // each warp hold no scores.  So lane i takes columns 0-31 of head 16 w + i and lane i + 16
+        // columns 32-63, handed over by one shuffle per value: both lanes serve the head (the same
+        // running max, each its own part of the sum and of P).  In the O^T work every thread is one
+        // column d = 128 c + 32 w + lane of each chunk c.
+        const int hl = 16 * warp + (lane & 15);
+        const bool upper = lane >= 16;
+        const bool live = hl < p.h;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const float sink2 = live ? p.sink[hl] * kLog2e : 0.0f;
         const int dl = 32 * warp + lane;
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                 ok = !*abort_flag;
                 ok = ok && warp_wait(BAR(B_FULL + stage), (uint32_t)(J / NST) & 1u, abort_flag);
                 ok = ok && warp_wait(BAR(B_SFULL + sb), (uint32_t)(J / NSB) & 1u, abort_flag);
-                float s[BN];
+                float s[32];
                 float tmax = -INFINITY;
                 if (ok) {
                     tc_fence_after();
@@ -523,21 +527,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                     if (it.t == it.ntile - 1 && (it.tok + 1) * T < e1)
                         load_q(unit_at(it.tok + 1, p.ntok, p.interleave));
                     const uint64_t mk = tile_mask[stage];
-                    const uint32_t mlo = (uint32_t)mk, mhi = (uint32_t)(mk >> 32);
+                    const uint32_t mh = upper ? (uint32_t)(mk >> 32) : (uint32_t)mk;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        s[j] = ((mlo >> j) & 1u) ? __uint_as_float(r0[j]) : -INFINITY;
-                        s[32 + j] = ((mhi >> j) & 1u) ? __uint_as_float(r1[j]) : -INFINITY;
+                        const uint32_t x = __shfl_sync(0xffffffffu, r1[j], lane & 15);
+                        s[j] = ((mh >> j) & 1u) ? __uint_as_float(upper ? x : r0[j]) : -INFINITY;
                     }
                     float mx[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
-                    for (int j = 16; j < BN; j += 8)
+                    for (int j = 16; j < 32; j += 8)
 #pragma unroll
                         for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[j + i]);
-                    tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+                    const float half = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    tmax = fmaxf(half, __shfl_xor_sync(0xffffffffu, half, 16)) * p.scale_log2;
                 }
                 // a head whose running max moves by more than the threshold asks every softmax
                 // thread to rescale O^T (each thread holds one d of every head's column)
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                         l *= f;
                         m_used = m_new;
                     }
-                    if (hl >= 0) fac[hl] = f;
+                    if (!upper) fac[hl] = f;
                     named_bar_sync(2, 128);
                     // O^T holds every P V before this tile (J >= 1: a segment's first tile never
                     // rescales, its running max starts at -inf)
@@ -590,12 +595,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                     ok = warp_wait(BAR(B_PVDONE + ((J - NPB) & 3)), (uint32_t)((J - NPB) >> 2) & 1u, abort_flag);
                 if (ok) {
                     // p = 2^(s * scale_log2 - m); P goes to the MMA in bf16, the row sum stays f32
-                    uint32_t pk[32];
+                    uint32_t pk[16];
                     if (live) {
                         float ls[4] = {0.f, 0.f, 0.f, 0.f};
                         const float neg_m = m_used == -INFINITY ? 0.0f : -m_used;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
+                        for (int j = 0; j < 16; ++j) {
                             const float p0 = ex2(fmaf(s[2 * j], p.scale_log2, neg_m));
                             const float p1 = ex2(fmaf(s[2 * j + 1], p.scale_log2, neg_m));
                             ls[j & 3] += p0 + p1;
@@ -604,16 +609,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) pk[j] = 0u;
+                        for (int j = 0; j < 16; ++j) pk[j] = 0u;
                     }
-                    // row hl of P (K-major for the P^T operand): 16-byte unit u at u ^ (hl % 8)
-                    if (hl >= 0) {
-                        const uint32_t prow = base + SM_P + (J % NPB) * P_BYTES + hl * 128;
+                    // row hl of P (K-major for the P^T operand): 16-byte unit u at u ^ (hl % 8); the
+                    // lower lane writes units 0-3 (entries 0-31), the upper lane units 4-7
+                    const uint32_t prow = base + SM_P + (J % NPB) * P_BYTES + hl * 128;
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            st_shared_v4(prow + ((u ^ (hl & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
-                                         pk[4 * u + 3]);
-                    }
+                    for (int u = 0; u < 4; ++u)
+                        st_shared_v4(prow + (((u + (upper ? 4 : 0)) ^ (hl & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                                     pk[4 * u + 2], pk[4 * u + 3]);
                     // P stores (and a rescale's TMEM stores) are made visible to the MMA, then one
                     // arrival per warp
                     fence_proxy_async_smem();
@@ -634,7 +638,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
             ok = ok && warp_wait(BAR(B_PVDONE + (Jl & 3)), (uint32_t)(Jl >> 2) & 1u, abort_flag);
             if (ok) tc_fence_after();
             const bool any = live && m_used != -INFINITY;
-            if (whole && hl >= 0) {
+            l += __shfl_xor_sync(0xffffffffu, l, 16);   // the head's sum: both halves of its columns
+            if (whole && !upper) {
                 float inv = 0.0f;
                 if (live) {
                     const float top = fmaxf(m_used, sink2);
@@ -681,7 +686,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                 // cluster merge of the token's KC parts (this CTA is part `rank`)
                 const int rank = (int)(cid % KC);
                 float *wsme = p.ws + (size_t)cid * SLOT;
-                if (live) {
+                if (live && !upper) {
                     wsme[SLOT_O + hl] = any ? m_used : -INFINITY;
                     wsme[SLOT_O + HM + hl] = l;
                 }
@@ -710,7 +715,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                 // the other parts' chunks and statistics
                 const bool okx = mbar_wait<true>(BAR(B_XCH), 0u, abort_flag, kWaitLimitNs);
                 float *wgt = reinterpret_cast<float *>(sbase + SM_BAR + WGT_OFF);
-                if (hl >= 0) {
+                if (!upper) {
                     if (live && okx) {
                         const float *part0 = p.ws + (size_t)(cid - rank) * SLOT;
                         float mi[KC], li[KC];
@@ -776,7 +781,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                 // partial: unnormalised O^T, running max and sum (log2 domain) for the combine
                 const int slot = tok == tok_begin ? 0 : 1;
                 float *ws = p.ws + ((size_t)cid * 2 + slot) * SLOT;
-                if (live) {
+                if (live && !upper) {
                     ws[SLOT_O + hl] = any ? m_used : -INFINITY;
                     ws[SLOT_O + HM + hl] = l;
                 }
