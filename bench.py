@@ -18,6 +18,7 @@ import dataclasses
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -141,11 +142,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _code_tokens(text: str) -> str:
+    """The source without comments and whitespace: what the compiler sees, so a summary taken on
+    the code stays valid across comment and layout edits."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", "", text)
+
+
 def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
     for rel in (ATTN_KERNEL_SOURCES if sources is None else sources):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -26,18 +26,18 @@
 //    for its lane (d) of the accumulator, after a vote among the four softmax warps.
 //  * Tiles are 64 consecutive index entries, not compacted: -1 and out-of-range entries are
 //    masked in the softmax (their rows are neither loaded nor counted).
-//  * Work ranges, the cost line and the cut tokens are those of attn_split.cuh; a cut token's
-//    parts leave f32 partials (O^T, running max and sum) that a combine kernel merges with the
-//    sink.
+//  * Work ranges, the cost line and the cut tokens are those of attn_split.cuh.  When every token
+//    is split into the same 2-4 parts, a token's parts run as one cluster and merge their f32
+//    accumulators among themselves; otherwise a cut token's parts leave f32 partials (O^T, running
+//    max and sum) that a combine kernel merges with the sink.
 //  * Warp roles (16 warps): 0-3 softmax, q loads and epilogue; 4-11 row gather (cp.async,
-//    swizzled in flight); 12 TMEM allocation and single-thread MMA issue; 13-15 none (they complete the
-//    last warpgroup, so the softmax warpgroup can take registers from the others).
+//    swizzled in flight); 12 TMEM allocation and single-thread MMA issue; 13-15 none (they
+//    complete the last warpgroup, so the softmax warpgroup can take registers from the others).
 //  * Every wait is bounded: past a time limit the kernel flags DS_DEV_TIMEOUT, drains its own
 //    copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <atomic>
 #include <mutex>
 
 #include "attn_split.cuh"
@@ -71,7 +71,6 @@ constexpr int SM_BAR = SM_P + NPB * P_BYTES;
 constexpr int BAR_BYTES = 2048;
 constexpr int SMEM_BYTES = SM_BAR + BAR_BYTES + 1024;   // + alignment of the base to 1024
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(NPB * P_BYTES == HM * 128 * 2, "the epilogue stages one chunk of bf16 output in the P buffers");
 
 // TMEM columns: O^T chunk c (d = 128 c + lane) at columns [64 c, 64 c + 64), one per head; then
 // the score buffers (64-row MMA: head r on lane 32 (r / 16) + r % 16, entry j on column j)
@@ -403,8 +402,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                     if (mbar_test_wait(BAR(B_FULL + stage), (uint32_t)(s.J / NST) & 1u) &&
                         mbar_test_wait(BAR(B_SFREE + sb), ((uint32_t)(s.J / NSB) & 1u) ^ 1u) &&
                         (s.t != 0 || mbar_test_wait(BAR(B_QFULL), (uint32_t)s.seg & 1u))) {
-                        // rows and q were written by cp.async (generic proxy); the MMA reads them
-                        // through the async proxy
+                        // the rows were written by cp.async (generic proxy), q by TMA; the MMA reads
+                        // them through the async proxy
                         fence_proxy_async_smem();
                         tc_fence_after();
                         // 16 columns of d = 32 bytes inside the 128-byte swizzle atom of chunk k / 4;
@@ -701,9 +700,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
 #pragma unroll
                     for (int hq = 0; hq < HM / 4; ++hq)
                         if (hq * 4 < p.h)
-                            dst[hq * 128] = make_float4(
-                                __uint_as_float(r[hq >> 3][4 * (hq & 7)]), __uint_as_float(r[hq >> 3][4 * (hq & 7) + 1]),
-                                __uint_as_float(r[hq >> 3][4 * (hq & 7) + 2]), __uint_as_float(r[hq >> 3][4 * (hq & 7) + 3]));
+                            dst[hq * 128] = make_float4(__uint_as_float(r[hq >> 3][4 * (hq & 7)]),
+                                                        __uint_as_float(r[hq >> 3][4 * (hq & 7) + 1]),
+                                                        __uint_as_float(r[hq >> 3][4 * (hq & 7) + 2]),
+                                                        __uint_as_float(r[hq >> 3][4 * (hq & 7) + 3]));
                 }
                 // every softmax thread's writes are in, then one release per other CTA
                 named_bar_sync(2, 128);
@@ -733,7 +733,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                             if (mi[i] != -INFINITY) den += ex2(mi[i] - top) * li[i];
                         const float inv = 1.0f / den;
 #pragma unroll
-                        for (int i = 0; i < KC; ++i) wgt[i * HM + hl] = mi[i] == -INFINITY ? 0.0f : ex2(mi[i] - top) * inv;
+                        for (int i = 0; i < KC; ++i)
+                            wgt[i * HM + hl] = mi[i] == -INFINITY ? 0.0f : ex2(mi[i] - top) * inv;
                     } else {
 #pragma unroll
                         for (int i = 0; i < KC; ++i) wgt[i * HM + hl] = 0.0f;
@@ -759,7 +760,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
 #pragma unroll 1
                     for (int i = 0; i < KC; ++i) {
                         if (i == rank) continue;
-                        const float4 *src = reinterpret_cast<const float4 *>(p.ws + (size_t)(cid - rank + i) * SLOT + c * 128 * HM) + dl;
+                        const float4 *src =
+                            reinterpret_cast<const float4 *>(p.ws + (size_t)(cid - rank + i) * SLOT + c * 128 * HM) + dl;
 #pragma unroll
                         for (int hq = 0; hq < HM / 4; ++hq) {
                             if (hq * 4 < p.h) {
@@ -795,9 +797,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
 #pragma unroll
                     for (int hq = 0; hq < HM / 4; ++hq)
                         if (hq * 4 < p.h)
-                            dst[(size_t)hq * D] = make_float4(
-                                __uint_as_float(r[hq >> 3][4 * (hq & 7)]), __uint_as_float(r[hq >> 3][4 * (hq & 7) + 1]),
-                                __uint_as_float(r[hq >> 3][4 * (hq & 7) + 2]), __uint_as_float(r[hq >> 3][4 * (hq & 7) + 3]));
+                            dst[(size_t)hq * D] = make_float4(__uint_as_float(r[hq >> 3][4 * (hq & 7)]),
+                                                              __uint_as_float(r[hq >> 3][4 * (hq & 7) + 1]),
+                                                              __uint_as_float(r[hq >> 3][4 * (hq & 7) + 2]),
+                                                              __uint_as_float(r[hq >> 3][4 * (hq & 7) + 3]));
                 }
             }
             tc_fence_before();
