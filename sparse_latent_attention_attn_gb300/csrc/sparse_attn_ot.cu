@@ -99,8 +99,9 @@ constexpr size_t SLOT = (size_t)SLOT_O + 2 * HM;
 
 // barrier slots (8 bytes each) in the SM_BAR block
 enum : int {
-    B_FULL = 0,                 // [NST] gather -> softmax, MMA: the tile's rows and mask landed
-    B_EMPTY = B_FULL + NST,     // [NST] MMA -> gather: stage free (its P V is done)
+    B_FULL = 0,                 // [NST] gather -> softmax, MMA: columns 0..255 of the rows and the mask landed
+    B_FULH = B_FULL + NST,      // [NST] gather -> MMA: columns 256..511 of the rows landed
+    B_EMPTY = B_FULH + NST,     // [NST] MMA -> gather: stage free (its P V is done)
     B_QFULL = B_EMPTY + NST,    // TMA -> MMA: q rows of the segment landed
     B_SFULL = B_QFULL + 1,      // [NSB] MMA -> softmax: scores ready
     B_SFREE = B_SFULL + NSB,    // [NSB] softmax -> MMA: score buffer read
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(BAR(B_FULL + s), NGATHER + 1);   // every gather thread's copies + the mask writer
+            mbar_init(BAR(B_FULH + s), NGATHER);
             mbar_init(BAR(B_EMPTY + s), 1);
         }
         mbar_init(BAR(B_QFULL), 1);                    // armed with the q bytes; the TMA completes it
@@ -324,16 +326,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
 
     if (warp >= W_GATHER && warp < W_GATHER + 8) {
         // ==================== row gather: cp.async into 128-byte-swizzled stages ====================
-        // Warp gw copies 16-byte unit u = 32 (gw % 2) + lane of rows gw / 2, gw / 2 + 4, ...: each
-        // warp instruction moves half a row (512 contiguous bytes).  Unit u sits in column chunk
-        // u / 8, swizzled to unit (u % 8) ^ (row % 8) of the row's 128 bytes.  A row the tile does
-        // not load is masked in the softmax (P = 0) but still multiplied, so it must hold finite
+        // Warp gw copies rows gw, gw + 8, ..., gw + 56, first their columns 0..255 (16-byte units
+        // u = lane), then columns 256..511 (u = 32 + lane), each half behind its own barrier, so
+        // the MMA can start on the first half of d while the second is in flight.  Every warp
+        // instruction moves half a row (512 contiguous bytes).  Unit u sits in column chunk u / 8,
+        // swizzled to unit (u % 8) ^ (row % 8) of the row's 128 bytes.  A row the tile does not
+        // load is masked in the softmax (P = 0) but still multiplied, so it must hold finite
         // values: at a stage's first use such rows are zeroed; later they keep an earlier tile's
         // rows.
         const int gw = warp - W_GATHER;
-        const int rsub = gw >> 1;
-        const int u = (gw & 1) * 32 + lane;
-        const int chunk = u >> 3, u8 = u & 7;
+        const int u8 = lane & 7;
         const bool writer = gw == 0 && lane == 0;
         bool ok = true, bad = false;
         TileIter it;
@@ -354,28 +356,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
                 ok = false;
                 break;
             }
-            const uint16_t *kvb = p.kv + (utok / p.m) * p.n * (int64_t)D + u * 8;
-            const uint32_t dst0 = base + SM_KV + stage * STAGE_BYTES + chunk * CHUNK;
-            // the row numbers of this warp's 16 rows first (independent shuffles), then the copies
-            int vr[BN / 4];
+            // the row numbers of this warp's 8 rows first (independent shuffles), then the copies
+            int vr[BN / 8];
 #pragma unroll
-            for (int i = 0; i < BN / 4; ++i) {
-                const int r = rsub + 4 * i;
+            for (int i = 0; i < BN / 8; ++i) {
+                const int r = gw + 8 * i;
                 vr[i] = __shfl_sync(0xffffffffu, r < 32 ? v0 : v1, r & 31);
             }
 #pragma unroll
-            for (int i = 0; i < BN / 4; ++i) {
-                const int r = rsub + 4 * i;
-                const uint32_t mk = r < 32 ? m0 : m1;
-                const uint32_t dst = dst0 + r * 128 + ((u8 ^ (r & 7)) << 4);
-                if ((mk >> (r & 31)) & 1u) cp_async_16(dst, kvb + (int64_t)vr[i] * D);
-                else if (it.J < NST) cp_async_zero16(dst, p.kv);
-            }
-            if (!(p.stall_first_tile && it.J == 0)) {
-                cp_async_arrive_noinc(BAR(B_FULL + stage));
-                if (writer) {
-                    tile_mask[stage] = ((uint64_t)m1 << 32) | m0;
-                    mbar_arrive(BAR(B_FULL + stage));
+            for (int hf = 0; hf < 2; ++hf) {
+                const int u = 32 * hf + lane;
+                const uint16_t *kvb = p.kv + (utok / p.m) * p.n * (int64_t)D + u * 8;
+                const uint32_t dst0 = base + SM_KV + stage * STAGE_BYTES + (u >> 3) * CHUNK;
+#pragma unroll
+                for (int i = 0; i < BN / 8; ++i) {
+                    const int r = gw + 8 * i;
+                    const uint32_t mk = r < 32 ? m0 : m1;
+                    const uint32_t dst = dst0 + r * 128 + ((u8 ^ (r & 7)) << 4);
+                    if ((mk >> (r & 31)) & 1u) cp_async_16(dst, kvb + (int64_t)vr[i] * D);
+                    else if (it.J < NST) cp_async_zero16(dst, p.kv);
+                }
+                if (!(p.stall_first_tile && it.J == 0)) {
+                    cp_async_arrive_noinc(BAR((hf == 0 ? B_FULL : B_FULH) + stage));
+                    if (hf == 0 && writer) {
+                        tile_mask[stage] = ((uint64_t)m1 << 32) | m0;
+                        mbar_arrive(BAR(B_FULL + stage));
+                    }
                 }
             }
             it.next(e0, e1, T);
@@ -386,7 +392,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
         // ================================= MMA issue (lane 0) =================================
         // Two streams in tile order: S = Q K^T for the next tile whose rows have landed (once its
         // score buffer has been read), and O^T += V^T P^T for the oldest tile whose P is written.
-        // Whichever is ready goes first.
+        // Whichever is ready goes first.  S goes in two halves of d, each as soon as its columns
+        // have landed; a P V may go between them.
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc(HM, BN, false, false);
             constexpr uint32_t IDESC_PV = idesc(128, HM, true, false);
@@ -395,28 +402,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_ot_kernel(const __gri
             v.start(tok_begin, e0, e1, T);
             uint64_t idle_since = 0;
             uint32_t idle = 0;
+            bool s_half = false;   // the first half of tile s.J's S is issued
+            // S over d columns [16 k0, 16 k1): 16 columns of d = 32 bytes inside the 128-byte
+            // swizzle atom of chunk k / 4; 8-row groups 1024 B apart, for Q (A) and the rows (B)
+            auto issue_s = [&](int stage, int sb, int k0, int k1) {
+                // the rows were written by cp.async (generic proxy), q by TMA; the MMA reads them
+                // through the async proxy
+                fence_proxy_async_smem();
+                tc_fence_after();
+                const uint64_t qd0 = smem_desc_sw128(base + SM_Q, 16, 1024);
+                const uint64_t kd0 = smem_desc_sw128(base + SM_KV + stage * STAGE_BYTES, 16, 1024);
+#pragma unroll
+                for (int k = k0; k < k1; ++k) {
+                    const uint64_t off = (uint64_t)(((k >> 2) * CHUNK + (k & 3) * 32) >> 4);
+                    mma_bf16_ss(tmem + S_COL + sb * BN, qd0 + off, kd0 + off, IDESC_S, k > 0 ? 1u : 0u);
+                }
+            };
             for (;;) {
                 bool progressed = false;
                 if (s.valid) {
                     const int stage = s.J % NST, sb = s.J % NSB;
-                    if (mbar_test_wait(BAR(B_FULL + stage), (uint32_t)(s.J / NST) & 1u) &&
+                    if (!s_half && mbar_test_wait(BAR(B_FULL + stage), (uint32_t)(s.J / NST) & 1u) &&
                         mbar_test_wait(BAR(B_SFREE + sb), ((uint32_t)(s.J / NSB) & 1u) ^ 1u) &&
                         (s.t != 0 || mbar_test_wait(BAR(B_QFULL), (uint32_t)s.seg & 1u))) {
-                        // the rows were written by cp.async (generic proxy), q by TMA; the MMA reads
-                        // them through the async proxy
-                        fence_proxy_async_smem();
-                        tc_fence_after();
-                        // 16 columns of d = 32 bytes inside the 128-byte swizzle atom of chunk k / 4;
-                        // 8-row groups 1024 B apart, for Q (A) and the rows (B) alike
-                        const uint64_t qd0 = smem_desc_sw128(base + SM_Q, 16, 1024);
-                        const uint64_t kd0 = smem_desc_sw128(base + SM_KV + stage * STAGE_BYTES, 16, 1024);
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            const uint64_t off = (uint64_t)(((k >> 2) * CHUNK + (k & 3) * 32) >> 4);
-                            mma_bf16_ss(tmem + S_COL + sb * BN, qd0 + off, kd0 + off, IDESC_S, k > 0 ? 1u : 0u);
-                        }
+                        issue_s(stage, sb, 0, D / 32);
+                        s_half = true;
+                        progressed = true;
+                    }
+                    if (s_half && mbar_test_wait(BAR(B_FULH + stage), (uint32_t)(s.J / NST) & 1u)) {
+                        issue_s(stage, sb, D / 32, D / 16);
                         mma_commit(BAR(B_SFULL + sb));
                         s.next(e0, e1, T);
+                        s_half = false;
                         progressed = true;
                     }
                 }
