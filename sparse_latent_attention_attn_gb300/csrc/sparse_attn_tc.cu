@@ -174,7 +174,12 @@ constexpr int SEND_OFF = ABORT_OFF + 4;
 // pair mode: per stage, the 64-bit masks of the tile's rows listed by the pair's first and second
 // query {A lo, A hi, B lo, B hi}
 constexpr int META2_OFF = 512;
-static_assert(SEND_OFF + 4 <= META2_OFF && META2_OFF + 16 * 5 <= 1024, "barrier block");
+// d split: per score tile J (slot J % 4), the next token's offset from the CTA's first token when
+// tile J is the last of its segment and a token follows in the range, else -1.  The MMA thread
+// writes it before issuing S(J) and arrives on that tile's S barrier, which the exchange warps
+// wait on.
+constexpr int SINFO_OFF = META2_OFF + 16 * 5;
+static_assert(SEND_OFF + 4 <= META2_OFF && SINFO_OFF + 16 <= 1024, "barrier block");
 // pair mode: an index entry carries its row in the low 29 bits and the queries listing it above
 constexpr int32_t kRowMask = (1 << 29) - 1, kPairA = 1 << 29, kPairB = 1 << 30;
 
@@ -286,6 +291,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
     uint4 *meta2 = reinterpret_cast<uint4 *>(sbase + C::SM_BAR + META2_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + ABORT_OFF);
     volatile int *s_end = reinterpret_cast<volatile int *>(sbase + C::SM_BAR + SEND_OFF);
+    int *sinfo = reinterpret_cast<int *>(sbase + C::SM_BAR + SINFO_OFF);
     int4 *lmeta = reinterpret_cast<int4 *>(sbase + C::SM_BAR + LMETA_OFF);
     int32_t *list = reinterpret_cast<int32_t *>(sbase + C::SM_LIST);
 
@@ -304,7 +310,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             mbar_init(BAR(B_EMPTY + s), 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(BAR(B_SFULL + i), 1);
+            // the MMA commit; with the d split also the MMA thread's arrival after writing sinfo
+            mbar_init(BAR(B_SFULL + i), C::CL == 2 ? 2 : 1);
             mbar_init(BAR(B_SFREE + i), C::CL == 2 ? 8 : 4);   // one arrival per reading warp
 
         }
@@ -615,6 +622,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                         } else if ((C::NP == 0 || pq_head >= J - C::NP + 1) &&
                                    mbar_test_wait(BAR(B_SFREE + (J & 1)), ((J >> 1) & 1) ^ 1) &&
                                    (!first || mbar_test_wait(BAR(B_QREADY), seg & 1))) {
+                            if constexpr (C::CL == 2) {
+                                // whether this tile ends its segment, for the exchange warps (they
+                                // load the next token's Q once this S is done)
+                                sinfo[J & 3] = mt.y && (tok + 1) * T < e1 ? (int)(tok + 1 - tok_begin) : -1;
+                                mbar_arrive(BAR(B_SFULL + (J & 1)));
+                            }
                             // the rows were written by cp.async (generic proxy); the MMA reads them
                             // through the async proxy
                             fence_proxy_async_smem();
@@ -700,8 +713,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             }
             (void)ok;
             if constexpr (C::CL == 2) {
-                // end marker for the exchange warps: no score tile J follows
+                // end marker for the exchange warps: no score tile J follows (both arrivals the
+                // barrier expects)
                 *s_end = J;
+                mbar_arrive(BAR(B_SFULL + (J & 1)));
                 mbar_arrive(BAR(B_SFULL + (J & 1)));
             }
             if (*abort_flag) {   // let issued MMAs finish before TMEM is freed
@@ -715,7 +730,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
         // Warp w reads TMEM lane quarter w % 4 of each finished score tile and sends it to the
         // peer's exchange buffer, so the softmax warps never wait on the cluster network to send.
         // Quarters without a live head are not sent (the receiver expects only the others).
+        // After the last score tile of a segment these warps also put the next token's q into
+        // TMEM (its S products are done with the current one), while the softmax warps finish the
+        // segment and write its output.
         const int quarter = warp & 3;
+        const int qt = quarter * 32 + lane;               // head row = TMEM lane
         const bool live_q = quarter * 32 < p.hm;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         constexpr uint32_t XSTRIDE = C::X_STRIDE;
@@ -738,6 +757,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             }
             if (!warp_wait(BAR(B_SFULL + sb), ph, abort_flag)) break;
             if (*s_end == J) break;
+            const int next_tok = sinfo[J & 3];
             tc_fence_after();
             uint32_t r0[32], r1[32];
             tmem_ld32(tmem + lane_off + C::S_COL + sb * BN, r0);
@@ -766,6 +786,41 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             if (live_q && lane == 0) {
                 bulk_copy_to_peer(xpeer + xs * XSTRIDE, stage_q, C::XQ, xfull_peer + 8u * xs);
                 bulk_commit_group();
+            }
+            if (next_tok >= 0) {
+                // the next token's q: this CTA's DH columns of row qt into TMEM columns
+                // [Q_COL, Q_COL + DH / 2) of lane qt, 32 columns per round (these warps have few
+                // registers), zeros for rows that are not a live head
+                const LaneRow lr =
+                    lane_row<PAIR>(unit_at(tok_begin + next_tok, p.ntok, p.interleave), qt, p.h, p.m, p.useq);
+                const uint4 *src =
+                    reinterpret_cast<const uint4 *>(p.q + (lr.tok * p.h + lr.head) * (int64_t)D + crank * C::DH);
+#pragma unroll 1
+                for (int c = 0; c < C::NCHUNK; ++c) {
+                    uint32_t r[32];
+                    if (p.wide) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint32_t w8[8];
+                            if (lr.live) ld_global_nc_v8(src + c * 8 + 2 * k, w8);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) r[8 * k + i] = lr.live ? w8[i] : 0u;
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint4 v = lr.live ? __ldg(src + c * 8 + k) : make_uint4(0, 0, 0, 0);
+                            r[4 * k] = v.x;
+                            r[4 * k + 1] = v.y;
+                            r[4 * k + 2] = v.z;
+                            r[4 * k + 3] = v.w;
+                        }
+                    }
+                    tmem_st32(tmem + lane_off + C::Q_COL + c * 32, r);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(BAR(B_QREADY));
             }
         }
         // every copy to the peer must have landed before either CTA of the cluster may exit (the
@@ -848,6 +903,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
             int2 cur = meta[it % NSTAGE];
             uint4 cur2 = make_uint4(0, 0, 0, 0);
             if constexpr (PAIR) cur2 = meta2[it % NSTAGE];
+            const bool seg_empty = cur.x == 0;
             if (cur.x == 0) {
                 // a segment without a single valid row: its only tile loads nothing; once all
                 // 128 threads and the MMA thread have seen it, thread 0 hands the stage back
@@ -1008,8 +1064,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                 }
                 if (!ok) break;
             }
-            // every S of this segment has been read, so the next token's Q may replace this one
-            if ((tok + 1) * T < e1) load_q(tok + 1);
+            // every S of this segment has been read, so the next token's Q may replace this one.
+            // With the d split the exchange warps load it after the segment's last score tile; a
+            // segment without rows has no score tile, so its successor's q is loaded here, once
+            // the q this segment was given has landed (both write the same TMEM columns)
+            if ((tok + 1) * T < e1) {
+                if constexpr (C::CL == 2) {
+                    if (seg_empty) {
+                        if (!warp_wait(BAR(B_QREADY), (uint32_t)seg & 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        load_q(tok + 1);
+                    }
+                } else {
+                    load_q(tok + 1);
+                }
+            }
             if (any) {
                 // O is final once the segment's last P V is done.  A parity wait is only exact
                 // when the previous completion of the same barrier (four tiles back) has happened,
