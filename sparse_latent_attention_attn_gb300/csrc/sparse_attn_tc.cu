@@ -23,8 +23,8 @@
 //    warps work on the previous tile; both CTAs add the same two f32 halves (addition commutes, so
 //    the sums are bit-identical) and run the identical softmax.
 //  * Warp roles (16 warps): 0-3 softmax and epilogue (thread = head = TMEM lane); 4-7 and 14-15
-//    row gather, plus 8-11 when d is not split; 8-11 score exchange when it is; 12 index
-//    compaction; 13 TMEM allocation + single-thread MMA issue, in whatever order its inputs
+//    row gather, plus 8-11 when d is not split; 8-11 score exchange when it is (and the next
+//    token's q into TMEM after a segment's last score tile); 12 index compaction; 13 TMEM allocation + single-thread MMA issue, in whatever order its inputs
 //    become ready.
 //  * Persistent clusters take contiguous ranges of the flattened (token, index entry) space, so
 //    the load is balanced whatever the batch; the ranges also charge each token a fixed cost for
