@@ -95,6 +95,10 @@ SCORE_CASES = [
     (4, 1, 300, 32, 128, 0, 0),        # prefill, 8 queries per block
     (5, 2, 2, 48, 128, 9000, 0),       # two queries per sequence at once
     (6, 1, 1, 256, 64, 700, 0),        # 256 heads: one query fills N
+    # more query blocks than SMs (several waves of CTAs), ragged blocks and chunks
+    (7, 1, 700, 64, 128, 0, 0),        # 350 blocks of 2 queries, 2 key tiles each
+    (8, 2, 400, 16, 64, 2000, 3),      # 8 queries per block, 3 key chunks per block, start_pos > 0
+    (9, 1, 600, 256, 64, 0, 0),        # 256 heads: one query per block, N = 256
 ]
 
 
