@@ -22,8 +22,9 @@
 //    passes over the row's scores in L2), then one pass that writes the positions above the cut
 //    and the first ties at the cut, in position order, through a block-wide scan of per-thread
 //    counts.
-//  * Warp roles of the score kernel: 0-3 epilogue (thread = key = TMEM lane), 4 TMA producer
-//    (one lane), 5 TMEM allocation + MMA issue (one lane).  Every wait is bounded (2 s), after
+//  * Warp roles of the score kernel: 0 .. NEPI-1 epilogue (thread = key = TMEM lane; with
+//    NEPI = 8 two warps share each lane quarter and split the block's queries), then the TMA
+//    producer (one lane) and TMEM allocation + MMA issue (one lane).  Every wait is bounded (2 s), after
 //    which the CTA flags DS_DEV_TIMEOUT, lets its issued MMAs finish, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -40,8 +41,13 @@ using namespace ptx;
 
 constexpr int BM = 128;             // keys per tile: M of the MMA, TMEM lanes
 constexpr int NSTAGE_MAX = 4;       // key tiles in flight, at most (barrier slots)
-constexpr int NTHREADS = 192;       // 6 warps
-constexpr int W_TMA = 4, W_MMA = 5;
+// warps: NEPI epilogue warps (4, or 8 when a query block holds several queries), the TMA producer,
+// the MMA warp
+template <int NEPI>
+struct Roles {
+    static constexpr int W_TMA = NEPI, W_MMA = NEPI + 1;
+    static constexpr int NTHREADS = (NEPI + 2) * 32;
+};
 constexpr int CHUNK_TILES_MAX = 16; // key tiles per CTA, at most (2048 keys)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -101,11 +107,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
-template <int D>
-__global__ void __launch_bounds__(NTHREADS)
+template <int D, int NEPI>
+__global__ void __launch_bounds__(Roles<NEPI>::NTHREADS, 2)
     indexer_scores_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                           const ScoreParams p) {
     using C = Cfg<D>;
+    constexpr int W_TMA = Roles<NEPI>::W_TMA, W_MMA = Roles<NEPI>::W_MMA;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -142,7 +149,7 @@ __global__ void __launch_bounds__(NTHREADS)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(BAR(B_AFULL + i), 1);
-            mbar_init(BAR(B_AFREE + i), 4);     // one arrival per epilogue warp
+            mbar_init(BAR(B_AFREE + i), NEPI);  // one arrival per epilogue warp
         }
         mbar_init(BAR(B_Q), 1);
         mbar_init(BAR(B_DRAIN), 1);
@@ -201,12 +208,15 @@ __global__ void __launch_bounds__(NTHREADS)
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
+    } else if (warp < NEPI) {
         // ===================================== epilogue =====================================
-        const int tid = threadIdx.x;                      // key within the tile = TMEM lane
-        for (int e = tid; e < nq * p.H; e += 128) w_s[e] = p.w[((int64_t)bi * p.s + i0) * p.H + e];
-        named_bar_sync(1, 128);
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int tid = (warp & 3) * 32 + lane;           // key within the tile = TMEM lane
+        for (int e = threadIdx.x; e < nq * p.H; e += 32 * NEPI) w_s[e] = p.w[((int64_t)bi * p.s + i0) * p.H + e];
+        named_bar_sync(1, 32 * NEPI);
+        // the warps of a lane quarter split the block's queries: warp w takes qi = w / 4 + k NEPI / 4
+        constexpr int QSTEP = NEPI / 4;
+        const int qg = warp / 4;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         float *srow = p.scores + ((int64_t)bi * p.s + i0) * p.ld;
         for (int it = 0; it < nlive; ++it) {
             const int acc = it & 1;
@@ -214,7 +224,7 @@ __global__ void __launch_bounds__(NTHREADS)
             if (!ok) break;
             tc_fence_after();
             const int64_t t = (j0 + it) * BM + tid;
-            for (int qi = 0; qi < nq; ++qi) {
+            for (int qi = qg; qi < nq; qi += QSTEP) {
                 float sum = 0.0f;
                 // up to 64 heads per wait: four 16-column loads in flight, then one wait
                 for (int h0 = 0; h0 < p.H; h0 += 64) {
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(NTHREADS)
         }
         // tiles no query of the block can see yet
         for (int64_t t = jl * BM + tid; t < min(j1 * BM, p.Tv); t += 128)
-            for (int qi = 0; qi < nq; ++qi) srow[qi * p.ld + t] = -INFINITY;
+            for (int qi = qg; qi < nq; qi += QSTEP) srow[qi * p.ld + t] = -INFINITY;
     }
 
     __syncthreads();
@@ -526,11 +536,15 @@ int launch_scores(const IndexerArgs &a, float *scores, int64_t ld, cudaStream_t 
     if (grid > 0x7fffffff) return DS_EUNSUPPORTED;
     p.nstage = stages_for(N);
     const int smem = C::smem_bytes(N, p.nstage);
-    if (cudaFuncSetAttribute(indexer_scores_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    // a block of several queries: eight epilogue warps, two per lane quarter, each taking half the
+    // queries (the epilogue's per-tile chain is what paces these shapes); one query: four
+    const bool wide = QB >= 2;
+    auto kernel = wide ? indexer_scores_kernel<D, 8> : indexer_scores_kernel<D, 4>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return DS_ECUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.blockDim = dim3(wide ? Roles<8>::NTHREADS : Roles<4>::NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -538,7 +552,7 @@ int launch_scores(const IndexerArgs &a, float *scores, int64_t ld, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, indexer_scores_kernel<D>, kmap, qmap, p) != cudaSuccess) return DS_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, kmap, qmap, p) != cudaSuccess) return DS_ECUDA;
     return DS_OK;
 }
 
