@@ -609,7 +609,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) sparse_attn_tc_kernel(const Param
                     const int stage = it % NSTAGE;
                     if (mbar_test_wait(BAR(B_FULL + stage), (it / NSTAGE) & 1)) {
                         const int2 mt = meta[stage];
-                        if (mt.x == 0) {
+                        if (mt.x == 0 && !mbar_test_wait(BAR(B_QREADY), seg & 1)) {
+                            // a segment without a single valid row still waits for the q it was
+                            // given (unused), so this thread's QREADY waits follow the segments one
+                            // phase at a time: a parity wait is only exact one phase ahead, and a
+                            // Q written while S reads it would corrupt the product
+                        } else if (mt.x == 0) {
                             // a segment without a single valid row: nothing to multiply; the softmax
                             // warps hand the stage back once this thread has read the meta too
                             mbar_arrive(BAR(B_ZREAD));

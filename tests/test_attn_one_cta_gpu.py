@@ -127,6 +127,22 @@ def test_invalid_duplicate_and_out_of_range_entries(ds, kernel):
     assert ds.device_status() == 0
 
 
+def test_tokens_without_rows_inside_ranges(ds, kernel):
+    """More tokens than CTAs or clusters, so each work range holds several tokens, some of
+    them listing no valid row at all (scattered, three in a row, and the last): such a token's
+    output is 0, and the tokens after it in the same range get their own q (the cluster kernel
+    loads it in the softmax warps after a segment without rows, in its exchange warps after any
+    other segment)."""
+    q, kv, sink, idx = _case(85, 300, 1, 64, 500, 200, 0.05)
+    empty = [5, 6, 100, 151, 152, 153, 299]
+    for t in empty:
+        idx[t] = -1
+    o = _check(ds, q, kv, sink, idx, f"{kernel} empty tokens")
+    for t in empty:
+        assert (o[t].float() == 0).all()
+    assert ds.device_status() == 0
+
+
 def test_plan_query_names_the_kernel(ds):
     """ds_sparse_attn_launches reports the kernel ds_sparse_attn picks and how many kernels it
     enqueues (the combine kernel only where tokens are cut and not merged inside a cluster)."""
