@@ -372,6 +372,22 @@ def test_attn_all_invalid_rows_give_zero(ds):
     assert (o[1, 2].float() == 0).all() and (o[0, 0].float() == 0).all()
 
 
+@pytest.mark.parametrize("d,h,b", [(64, 8, 400), (256, 32, 300), (512, 128, 200)])
+def test_attn_tokens_without_rows_inside_ranges(ds, d, h, b):
+    """More tokens than clusters, so each work range holds several tokens, some listing no valid
+    row (scattered, three in a row, the last): zeros out for those, and the right q for the
+    tokens after them in the same range (cluster kernel at every head_dim it takes; d < 512
+    loads each q in the softmax warps, d = 512 after a segment without rows only)."""
+    q, kv, sink, idx = _case(90 + d, b, 1, h, d, 300, 150, 0.05)
+    empty = [3, 4, 150, 151, 152, b - 1]
+    for t in empty:
+        idx[t] = -1
+    o, _ = _check_case(ds, q, kv, sink, idx, d ** -0.5)
+    for t in empty:
+        assert (o[t].float() == 0).all()
+    assert ds.device_status() == 0
+
+
 def test_attn_empty_topk(ds):
     q, kv, sink, idx = _case(21, 2, 2, 16, 64, 10, 0)
     o, _ = _check_case(ds, q, kv, sink, idx, 0.125)
@@ -534,6 +550,25 @@ def test_attn_fp8kv_is_bit_identical_to_bf16_on_decoded_rows(ds, case):
         o_bf16, _ = _check_case(ds, q, kv_dec, sink, idx, 512 ** -0.5)
     o_f8 = ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), 512 ** -0.5)
     assert torch.equal(o_f8, o_bf16)
+    assert ds.device_status() == 0
+
+
+def test_attn_fp8kv_tokens_without_rows_inside_ranges(ds):
+    """The fp8 row store's gather with tokens listing no valid row inside multi-token ranges:
+    bit-identical to ds_sparse_attn on the decoded rows, zeros for those tokens."""
+    b, h, n, topk = 200, 128, 600, 200
+    q, _, sink, idx = _case(95, b, 1, h, 512, n, topk, 0.05)
+    empty = [0, 7, 8, 9, 120, b - 1]
+    for t in empty:
+        idx[t] = -1
+    kv = torch.randn((b, n, 512), generator=torch.Generator().manual_seed(96)).to(torch.bfloat16)
+    codes, exps = ds.kv_quantize_fp8(kv.cuda())
+    kv_dec = _bf16_from_bits(oracle.kv_dequantize_fp8(codes.cpu().numpy(), exps.cpu().numpy()))
+    o_bf16, _ = _check_case(ds, q, kv_dec, sink, idx, 512 ** -0.5)
+    o_f8 = ds.sparse_attn_fp8kv(q.cuda(), codes, exps, sink.cuda(), idx.cuda(), 512 ** -0.5)
+    assert torch.equal(o_f8, o_bf16)
+    for t in empty:
+        assert (o_f8[t].float() == 0).all()
     assert ds.device_status() == 0
 
 
@@ -786,6 +821,26 @@ def test_prefill_pairs_empty_and_shared_rows(ds):
     ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), idx.numpy(), d ** -0.5)
     assert_close_bf16(bits(o), ref)
     assert (o[0, 0:2].float() == 0).all() and (o[0, 3].float() == 0).all()
+    assert ds.device_status() == 0
+
+
+def test_prefill_pairs_without_rows_inside_ranges(ds):
+    """More query pairs than clusters (several pairs per work range), some pairs listing no
+    row at all, one pair where only the second query lists rows."""
+    b, m, h, d, n = 1, 700, 16, 512, 400
+    g = torch.Generator().manual_seed(640)
+    q = torch.randn((b, m, h, d), generator=g).to(torch.bfloat16)
+    kv = torch.randn((b, n, d), generator=g).to(torch.bfloat16)
+    sink = torch.randn((h,), generator=g)
+    idx = torch.stack([torch.randperm(n, generator=g)[:100] for _ in range(b * m)]).view(b, m, 100).to(torch.int32)
+    for j in (10, 11, 200, 201, 202, 349):     # pairs (2j, 2j + 1) with nothing
+        idx[0, 2 * j:2 * j + 2] = -1
+    idx[0, 2 * 50] = -1                        # pair 50: only its second query
+    o = ds.sparse_attn_prefill(q.cuda(), kv.cuda(), sink.cuda(), idx.cuda(), d ** -0.5)
+    ref = oracle.sparse_attn(bits(q), bits(kv), sink.numpy(), idx.numpy(), d ** -0.5)
+    assert_close_bf16(bits(o), ref)
+    for j in (10, 11, 200, 201, 202, 349):
+        assert (o[0, 2 * j:2 * j + 2].float() == 0).all()
     assert ds.device_status() == 0
 
 
