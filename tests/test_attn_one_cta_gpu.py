@@ -77,6 +77,8 @@ CASES = [
     (9, 64, 1, 64, 128, 128, 0.0),       # decode_window's shape: whole tokens, no combine
     (10, 2, 1, 8, 200, 70, 0.0),         # 8 heads, a 6-entry last tile
     (11, 8, 2, 40, 900, 300, 0.05),      # two queries per sequence, 40 heads, 2-CTA merges
+    (12, 45, 1, 48, 1000, 400, 0.05),    # 45 tokens in 3 parts each: 3-CTA merges
+    (13, 15, 3, 64, 900, 384, 0.05),     # the same with three queries per sequence
 ]
 
 
