@@ -145,6 +145,29 @@ def test_tokens_without_rows_inside_ranges(ds, kernel):
     assert ds.device_status() == 0
 
 
+def test_twenty_thousand_tokens_sampled(ds, kernel):
+    """20000 tokens of 16 entries, far more than CTAs: every work range walks over a hundred
+    tokens (segment changes, q loads and index arithmetic over long ranges).  Sampled tokens,
+    the first and last ones and those at range-like boundaries among them, against the oracle."""
+    b, h, d, n, topk = 20000, 64, 512, 16, 16
+    g = torch.Generator(device="cuda").manual_seed(97)
+    q = torch.randn((b, 1, h, d), generator=g, device="cuda").to(torch.bfloat16)
+    kv = torch.randn((b, n, d), generator=g, device="cuda").to(torch.bfloat16)
+    sink = torch.randn((h,), generator=g, device="cuda")
+    idx = torch.argsort(torch.rand((b, 1, n), generator=g, device="cuda"), dim=-1)[..., :topk].to(torch.int32)
+    idx[torch.rand((b, 1, topk), generator=g, device="cuda") < 0.05] = -1
+    scale = d ** -0.5
+    o = ds.sparse_attn(q, kv, sink, idx, scale)
+    torch.cuda.synchronize()
+    pick = [0, 1, 2, 131, 132, 151, 152, 153, 9999, 10000, 19997, 19998, 19999]
+    pick += torch.randint(0, b, (24,), generator=torch.Generator().manual_seed(98)).tolist()
+    sk = sink.cpu().numpy()
+    for t in pick:
+        ref = oracle.sparse_attn(bits(q[t:t + 1]), bits(kv[t:t + 1]), sk, idx[t:t + 1].cpu().numpy(), scale)
+        assert_close_bf16(bits(o[t:t + 1]), ref, f"{kernel} token {t}")
+    assert ds.device_status() == 0
+
+
 def test_plan_query_names_the_kernel(ds):
     """ds_sparse_attn_launches reports the kernel ds_sparse_attn picks and how many kernels it
     enqueues (the combine kernel only where tokens are cut and not merged inside a cluster)."""
