@@ -572,6 +572,29 @@ def test_attn_fp8kv_tokens_without_rows_inside_ranges(ds):
     assert ds.device_status() == 0
 
 
+def test_attn_fp8kv_decode_large_full_size(ds):
+    """The fp8 row store on decode_large at full size, in the launch configuration
+    `bench.py --kv fp8` times (256 sequences, 128 heads, 2176 entries over 32896 rows each): the
+    whole output bit-identical to ds_sparse_attn on the round-tripped rows, and three sampled
+    sequences against the oracle on those rows."""
+    w = wl.WORKLOADS[4]
+    gs = GpuStep(w)
+    gs.run()
+    torch.cuda.synchronize()
+    codes, exps = ds.kv_quantize_fp8(gs.kv)
+    kv_rt = gs.kv.clone()
+    ds.kv_quant_ring_write(kv_rt, None, 0, 1)          # every row through the round trip, in place
+    q, sink = gs.inp.q, gs.inp.sink
+    o_bf16 = ds.sparse_attn(q, kv_rt, sink, gs.idx, w.scale)
+    o_f8 = ds.sparse_attn_fp8kv(q, codes, exps, sink, gs.idx, w.scale)
+    assert torch.equal(o_f8, o_bf16)
+    for bi in (0, 101, 255):
+        ref = oracle.sparse_attn(bits(q[bi:bi + 1]), bits(kv_rt[bi:bi + 1]), sink.cpu().numpy(),
+                                 gs.idx[bi:bi + 1].cpu().numpy(), w.scale)
+        assert_close_bf16(bits(o_f8[bi:bi + 1]), ref, f"fp8 decode_large sequence {bi}")
+    assert ds.device_status() == 0
+
+
 def test_attn_fp8kv_ring_then_attend(ds):
     """The fp8 ring write into the leading rows of an fp8 row store, then attention over window
     and compressed rows: equal to the bf16 pipeline (round-tripped ring inside a bf16 kv)."""
