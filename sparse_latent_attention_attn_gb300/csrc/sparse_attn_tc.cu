@@ -1250,6 +1250,52 @@ __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const C
         return cp.ws + ((size_t)(kf + i) * 2 + ((slots >> i) & 1u)) * SLOT;
     };
     const float sink2 = cp.sink[lr.head] * kLog2e;
+    const int c0 = blockIdx.y * (D < kCombineCols ? D : kCombineCols);
+    if (np == 2) {
+        // two parts (a cut between two neighbouring ranges): every load of both parts in flight
+        // at once, the statistics beside the columns
+        constexpr int COLS2 = D < kCombineCols ? D : kCombineCols;
+        const float *p0 = part(0), *p1 = part(1);
+        const float4 *s0 = reinterpret_cast<const float4 *>(p0) + (size_t)(c0 / 4) * SLOT_HEADS + hh;
+        const float4 *s1 = reinterpret_cast<const float4 *>(p1) + (size_t)(c0 / 4) * SLOT_HEADS + hh;
+        const float m0 = p0[SLOT_HEADS * D + hh], m1 = p1[SLOT_HEADS * D + hh];
+        const float l0 = p0[SLOT_HEADS * D + SLOT_HEADS + hh], l1 = p1[SLOT_HEADS * D + SLOT_HEADS + hh];
+        float4 x0[COLS2 / 4], x1[COLS2 / 4];
+#pragma unroll
+        for (int k = 0; k < COLS2 / 4; ++k) {
+            x0[k] = s0[(size_t)k * SLOT_HEADS];
+            x1[k] = s1[(size_t)k * SLOT_HEADS];
+        }
+        const float top2 = fmaxf(sink2, fmaxf(m0, m1));
+        float den2 = exp2f(sink2 - top2);
+        if (m0 != -INFINITY) den2 += exp2f(m0 - top2) * l0;
+        if (m1 != -INFINITY) den2 += exp2f(m1 - top2) * l1;
+        const float inv2 = 1.0f / den2;
+        const float w0 = m0 == -INFINITY ? 0.0f : exp2f(m0 - top2) * inv2;
+        const float w1 = m1 == -INFINITY ? 0.0f : exp2f(m1 - top2) * inv2;
+        float acc2[COLS2];
+#pragma unroll
+        for (int k = 0; k < COLS2 / 4; ++k) {
+            acc2[4 * k] = 0.0f + w0 * x0[k].x;
+            acc2[4 * k + 1] = 0.0f + w0 * x0[k].y;
+            acc2[4 * k + 2] = 0.0f + w0 * x0[k].z;
+            acc2[4 * k + 3] = 0.0f + w0 * x0[k].w;
+            acc2[4 * k] += w1 * x1[k].x;
+            acc2[4 * k + 1] += w1 * x1[k].y;
+            acc2[4 * k + 2] += w1 * x1[k].z;
+            acc2[4 * k + 3] += w1 * x1[k].w;
+        }
+        uint4 *dst2 = reinterpret_cast<uint4 *>(cp.o + (tok * cp.h + lr.head) * (int64_t)D + c0);
+        const float2 *cs_row2 = nullptr;
+        if constexpr (ROPE) cs_row2 = cp.rope + (cp.rope_pos0 + tok % cp.m) * (cp.rd / 2);
+#pragma unroll
+        for (int k = 0; k < COLS2 / 8; ++k)
+            dst2[k] = make_uint4(out_pair<D, ROPE>(acc2[8 * k], acc2[8 * k + 1], c0 + 8 * k, cs_row2, cp.rd),
+                                 out_pair<D, ROPE>(acc2[8 * k + 2], acc2[8 * k + 3], c0 + 8 * k + 2, cs_row2, cp.rd),
+                                 out_pair<D, ROPE>(acc2[8 * k + 4], acc2[8 * k + 5], c0 + 8 * k + 4, cs_row2, cp.rd),
+                                 out_pair<D, ROPE>(acc2[8 * k + 6], acc2[8 * k + 7], c0 + 8 * k + 6, cs_row2, cp.rd));
+        return;
+    }
     float top = sink2;
     for (int i = 0; i < np; ++i) top = fmaxf(top, part(i)[SLOT_HEADS * D + hh]);
     float den = exp2f(sink2 - top);
@@ -1258,7 +1304,6 @@ __global__ void __launch_bounds__(SLOT_HEADS) sparse_attn_combine_kernel(const C
         if (mi != -INFINITY) den += exp2f(mi - top) * part(i)[SLOT_HEADS * D + SLOT_HEADS + hh];
     }
     const float inv = 1.0f / den;
-    const int c0 = blockIdx.y * COLS;
     float acc[COLS];
 #pragma unroll
     for (int j = 0; j < COLS; ++j) acc[j] = 0.0f;
