@@ -650,8 +650,9 @@ def run_ours(args):
             roof = {"bound": "tensor", "achieved": flops / attn_s / 1e12, "peak": peaks["bf16_tflops"],
                     "unit": "TFLOP/s"}
         roof["frac"] = roof["achieved"] / roof["peak"]
-        # the capture matching this run: the prefill pairs and the fp8 row store have their own
-        profile_name = w.name + ("_pairs" if args.prefill_pairs else "") + ("_fp8" if args.kv == "fp8" else "")
+        # the capture matching this run: the prefill pairs and the fp8 row store (whose workload
+        # name ends in _fp8kv) have their own
+        profile_name = w.name + ("_pairs" if args.prefill_pairs else "")
         roof["traffic"] = profiled_traffic(profile_name, 1)
         roof["peak_source"] = peaks["source"]
         roof["kernel"] = ("sparse_attn_ot_kernel (one CTA per work range, transposed accumulator; tokens cut "
